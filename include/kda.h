@@ -1,0 +1,136 @@
+/*
+ * kda.h — C ABI of the GB300 (sm_103a) Kimi Delta Attention library.
+ *
+ * The operation (flashinfer "kda_backward" page, "Supported contract"; FLA
+ * chunk_kda call contract on the Kimi-K3 "fused_chunk" page): per sequence n
+ * and head h, a value-first fp32 state S in R^{V x K} (K = V = 128) evolves as
+ *
+ *   q^ = q / sqrt(|q|^2 + 1e-6),  k^ = k / sqrt(|k|^2 + 1e-6)
+ *   beta_t = sigmoid(beta_raw_t)
+ *   g_t[c] = lower_bound * sigmoid(exp(A_log[h]) * (g_raw_t[c] + dt_bias[h,c]))
+ *   S_t = S_{t-1} diag(exp(g_t)) (I - beta_t k^_t k^_t^T) + beta_t v_t k^_t^T
+ *   o_t = scale * S_t q^_t
+ *
+ * with the decay applied per KEY channel c (the kda-neuron-kernels log, fix
+ * T-KDA-02). kda_fwd computes o and the final state; kda_bwd returns the
+ * gradients of L = sum_t <o_t, do_t> + <S_T, dhT> w.r.t. q, k, v, g_raw,
+ * beta_raw, A_log, dt_bias and the initial state (the list on the flashinfer
+ * page).
+ *
+ * Conventions
+ *  - bf16 tensors are passed as raw 16-bit patterns (kda_bf16).
+ *  - Token tensors are contiguous [B*T, H, 128] (fixed-length batches, B rows
+ *    of T tokens) or [T_total, H, 128] with B = 1 when packed. beta_raw and
+ *    dbeta_raw are [B*T, H].
+ *  - A_log, dA_log: [H] fp32. dt_bias, ddt_bias: [H, 128] fp32 (one bias per
+ *    key channel of the gate).
+ *  - States h0, hT, dhT, dh0: [N, H, V, K] fp32, value-first.
+ *  - cu_seqlens: DEVICE pointer to N+1 int64 offsets (0 = cu[0] <= ... <=
+ *    cu[N] = T_total) for packed variable-length input; NULL for B fixed
+ *    sequences of T tokens (then N = B). Empty sequences are allowed.
+ *  - All device pointers must be 16-byte aligned.
+ *  - Nullable inputs (h0, dhT) mean zero. Nullable outputs (hT, dh0) are
+ *    skipped.
+ *  - `stream` is a cudaStream_t. Calls are asynchronous: nothing is
+ *    synchronised or allocated inside the launch path.
+ *
+ * Ownership: the caller owns every buffer, including the workspace. kda_fwd
+ * stores its per-chunk intermediates and state checkpoints in the workspace;
+ * kda_bwd must receive the same workspace, unchanged, with the same inputs.
+ * One workspace must not be used by two calls in flight at the same time.
+ *
+ * Errors: argument problems are reported synchronously as kda_status codes.
+ * Problems found on the device (malformed cu_seqlens, a wait that timed out)
+ * set a status word in the workspace; later kernels of the same call skip
+ * their work, and kda_get_device_status() returns the word.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t kda_bf16;
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_NULL = 1,        /* a required pointer is NULL */
+    KDA_ERR_ALIGN = 2,       /* a pointer is not 16-byte aligned */
+    KDA_ERR_SHAPE = 3,       /* B, T, H or N out of range / inconsistent */
+    KDA_ERR_UNSUPPORTED = 4, /* K or V != 128, lower_bound not in [-5, 0), bad scale */
+    KDA_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
+    KDA_ERR_OFFSETS = 6,     /* (device) cu_seqlens not 0 .. T_total non-decreasing */
+    KDA_ERR_TIMEOUT = 7,     /* (device) a bounded wait inside a kernel gave up */
+    KDA_ERR_CUDA = 8         /* a CUDA launch or attribute call failed */
+} kda_status;
+
+typedef struct {
+    int64_t B;           /* fixed-length batch rows; 1 when packed */
+    int64_t T;           /* tokens per row; total tokens when packed */
+    int64_t H;           /* heads */
+    int64_t N;           /* sequences: B when cu_seqlens is NULL, else len(cu_seqlens) - 1 */
+    int32_t K;           /* key dimension, must be 128 */
+    int32_t V;           /* value dimension, must be 128 */
+    float scale;         /* output scale, finite and > 0 (the pages fix 1/sqrt(128)) */
+    float lower_bound;   /* gate lower bound lb, in [-5, 0) (FLA chunk_kda lower_bound) */
+} kda_shape;
+
+/* Bytes of workspace kda_fwd and kda_bwd need for this shape (the same buffer
+ * serves both; pass at least this many bytes to each). Returns 0 for an
+ * invalid shape. */
+size_t kda_workspace_size(const kda_shape* shape);
+
+/* Forward. Writes o [B*T, H, 128] bf16 and, if hT != NULL, the final states
+ * [N, H, 128, 128] fp32. Fills the workspace with what kda_bwd needs. */
+kda_status kda_fwd(const kda_shape* shape,
+                   const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                   const kda_bf16* g_raw, const kda_bf16* beta_raw,
+                   const float* A_log, const float* dt_bias,
+                   const float* h0, const int64_t* cu_seqlens,
+                   kda_bf16* o, float* hT,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Backward of the kda_fwd call that filled `workspace`, with the same inputs.
+ * do_ is the output adjoint [B*T, H, 128] bf16; dhT the final-state adjoint
+ * (NULL = 0). Writes dq, dk, dv, dg_raw [B*T, H, 128] bf16, dbeta_raw
+ * [B*T, H] bf16, dA_log [H] fp32, ddt_bias [H, 128] fp32 (written, not
+ * accumulated) and, if dh0 != NULL, dh0 [N, H, 128, 128] fp32. The parameter
+ * gradients are summed over all tokens of all sequences in a fixed order
+ * (bitwise reproducible). */
+kda_status kda_bwd(const kda_shape* shape,
+                   const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                   const kda_bf16* g_raw, const kda_bf16* beta_raw,
+                   const float* A_log, const float* dt_bias,
+                   const float* h0, const int64_t* cu_seqlens,
+                   const kda_bf16* do_, const float* dhT,
+                   kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg_raw,
+                   kda_bf16* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0,
+                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream` and returns the device status word of `workspace`
+ * (KDA_OK, KDA_ERR_OFFSETS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
+ * stream reported an error. Clears nothing. */
+kda_status kda_get_device_status(const void* workspace, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* kda_status_string(kda_status s);
+
+/* Diagnostics: one CTA computes D[128 x N] = A[128 x Kd] * B[N x Kd]^T with
+ * tcgen05 kind::tf32 (operands rounded to tf32), A stored in shared memory
+ * K-major (a_mn = 0) or MN-major (a_mn = 1), likewise B. D holds 2*128*N
+ * floats: the product, then (2 * product + row index) after a round trip
+ * through tcgen05.st / tcgen05.ld. A, B, D are device pointers, row-major.
+ * N in {32, 64, ..., 256}, Kd in {32, 64, 96, 128}. Used by the tests to
+ * check the descriptors and the TMEM data path. */
+int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, const float* B,
+                           float* D, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,213 @@
+// C ABI entry points (include/kda.h): argument validation, workspace layout,
+// the chunk table built on the device from cu_seqlens, and kernel launches.
+#include <cmath>
+#include "kda_internal.cuh"
+
+namespace kda {
+
+size_t fwd_intra_smem_bytes();
+size_t fwd_scan_smem_bytes();
+size_t bwd_scan_smem_bytes();
+size_t bwd_state_smem_bytes();
+size_t bwd_intra_smem_bytes();
+
+__global__ void kda_fwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+                                     const uint16_t*, const float*, const float*, int, float, uint8_t*, Layout);
+__global__ void kda_fwd_scan_kernel(const float*, uint16_t*, float*, int, float, uint8_t*, Layout);
+__global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, float, uint8_t*, Layout);
+__global__ void kda_bwd_state_kernel(const uint16_t*, int, float, uint8_t*, Layout);
+__global__ void kda_bwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+                                     const uint16_t*, const float*, const float*, const uint16_t*, int, float,
+                                     uint16_t*, uint16_t*, uint16_t*, uint16_t*, uint16_t*, uint8_t*, Layout);
+__global__ void kda_param_reduce_kernel(int, float*, float*, uint8_t*, Layout);
+
+// Chunk table from the offsets: validates cu_seqlens (cu[0] = 0, non-decreasing,
+// cu[N] = T_total), lists the chunks of every sequence in order (a chunk never
+// crosses a sequence boundary), the first chunk of each sequence, and the
+// sequences ordered by decreasing chunk count (longest first, for the scans).
+// One CTA; N is small next to the token count.
+__global__ void __launch_bounds__(1024)
+    kda_chunk_table_kernel(const int64_t* __restrict__ cu, int64_t N, int64_t T_total, int64_t T_fixed,
+                           uint8_t* __restrict__ ws, Layout lay) {
+    __shared__ int carry;
+    __shared__ int bad;
+    __shared__ int scan[1024];
+    ChunkInfo* chunks = reinterpret_cast<ChunkInfo*>(ws + lay.chunks);
+    int* first = reinterpret_cast<int*>(ws + lay.seq_first);
+    int* order = reinterpret_cast<int*>(ws + lay.seq_order);
+    const int tid = threadIdx.x;
+    auto cu_at = [&](int64_t i) -> int64_t { return cu ? cu[i] : i * T_fixed; };
+    if (tid == 0) {
+        carry = 0;
+        bad = (cu_at(0) != 0 || cu_at(N) != T_total) ? 1 : 0;
+    }
+    __syncthreads();
+    for (int64_t b = 0; b < N; b += blockDim.x) {
+        const int64_t n = b + tid;
+        int nch = 0;
+        if (n < N) {
+            const int64_t L = cu_at(n + 1) - cu_at(n);
+            if (L < 0) atomicOr(&bad, 1);
+            nch = L > 0 ? (int)((L + C - 1) / C) : 0;
+        }
+        scan[tid] = nch;
+        __syncthreads();
+        for (int off = 1; off < (int)blockDim.x; off <<= 1) {
+            const int x = tid >= off ? scan[tid - off] : 0;
+            __syncthreads();
+            scan[tid] += x;
+            __syncthreads();
+        }
+        const int excl = carry + scan[tid] - nch;
+        if (n < N) first[n] = excl;
+        __syncthreads();
+        if (tid == blockDim.x - 1) carry += scan[tid];
+        __syncthreads();
+    }
+    const int total = carry;
+    if (tid == 0) first[N] = total;
+    __syncthreads();
+    if (bad || total > lay.nc_max) {
+        for (int64_t i = tid; i < lay.nc_max; i += blockDim.x) chunks[i] = ChunkInfo{0, 0, 0, 0};
+        for (int64_t n = tid; n <= N; n += blockDim.x) first[n] = 0;
+        for (int64_t n = tid; n < N; n += blockDim.x) order[n] = (int)n;
+        if (tid == 0) raise_status(ws, KDA_ERR_OFFSETS);
+        return;
+    }
+    for (int64_t n = tid; n < N; n += blockDim.x) {
+        const int64_t t0 = cu_at(n), L = cu_at(n + 1) - t0;
+        const int f = first[n];
+        for (int64_t c = 0; c * C < L; ++c) {
+            const int64_t rem = L - c * C;
+            chunks[f + c] = ChunkInfo{(int32_t)(t0 + c * C), (int32_t)(rem < C ? rem : C), (int32_t)n, (int32_t)c};
+        }
+    }
+    for (int64_t i = total + tid; i < lay.nc_max; i += blockDim.x) chunks[i] = ChunkInfo{0, 0, 0, 0};
+    // longest first: rank of sequence n by (chunk count desc, index asc)
+    for (int64_t n = tid; n < N; n += blockDim.x) {
+        const int cn = first[n + 1] - first[n];
+        int rank = 0;
+        for (int64_t m = 0; m < N; ++m) {
+            const int cm = first[m + 1] - first[m];
+            rank += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+        }
+        order[rank] = (int)n;
+    }
+}
+
+__global__ void kda_clear_status_kernel(uint8_t* ws) { *reinterpret_cast<int*>(ws) = 0; }
+
+}  // namespace kda
+
+using namespace kda;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_shape(const kda_shape* sh, bool packed) {
+    if (!sh) return KDA_ERR_NULL;
+    if (sh->K != 128 || sh->V != 128) return KDA_ERR_UNSUPPORTED;
+    if (!(sh->lower_bound >= -5.0f && sh->lower_bound < 0.0f)) return KDA_ERR_UNSUPPORTED;
+    if (!(std::isfinite(sh->scale) && sh->scale > 0.0f)) return KDA_ERR_UNSUPPORTED;
+    if (sh->B < 1 || sh->T < 0 || sh->H < 1 || sh->H > 65535 || sh->N < 0) return KDA_ERR_SHAPE;
+    if (packed) {
+        if (sh->B != 1 || sh->N < 1 || sh->N > 65535) return KDA_ERR_SHAPE;
+    } else {
+        if (sh->N != sh->B || sh->B > 65535) return KDA_ERR_SHAPE;
+    }
+    if (sh->B * sh->T * sh->H >= (int64_t(1) << 31)) return KDA_ERR_SHAPE;
+    return KDA_OK;
+}
+
+Layout layout_of(const kda_shape* sh, bool packed) { return make_layout(sh->B, sh->T, sh->H, sh->N, packed); }
+
+template <typename K>
+kda_status set_smem(K kernel, size_t bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
+               ? KDA_OK
+               : KDA_ERR_CUDA;
+}
+
+kda_status common_checks(const kda_shape* shape, const int64_t* cu, void* ws, size_t ws_bytes, Layout* lay) {
+    const bool packed = cu != nullptr;
+    kda_status st = check_shape(shape, packed);
+    if (st != KDA_OK) return st;
+    *lay = layout_of(shape, packed);
+    if (!ws || ws_bytes < lay->total) return KDA_ERR_WORKSPACE;
+    if (!aligned16(ws) || (packed && (reinterpret_cast<uintptr_t>(cu) & 7u))) return KDA_ERR_ALIGN;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" size_t kda_workspace_size(const kda_shape* shape) {
+    if (!shape) return 0;
+    // the same shape may be used with or without offsets; cover both layouts
+    const bool ok_p = check_shape(shape, true) == KDA_OK, ok_f = check_shape(shape, false) == KDA_OK;
+    if (!ok_p && !ok_f) return 0;
+    const size_t a = ok_p ? make_layout(shape->B, shape->T, shape->H, shape->N, true).total : 0;
+    const size_t b = ok_f ? make_layout(shape->B, shape->T, shape->H, shape->N, false).total : 0;
+    return a > b ? a : b;
+}
+
+extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                              const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log,
+                              const float* dt_bias, const float* h0, const int64_t* cu_seqlens, kda_bf16* o,
+                              float* hT, void* workspace, size_t workspace_bytes, void* stream) {
+    Layout lay;
+    kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay);
+    if (st != KDA_OK) return st;
+    if (!q || !k || !v || !g_raw || !beta_raw || !A_log || !dt_bias || !o) return KDA_ERR_NULL;
+    const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, o};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGN;
+    if ((h0 && !aligned16(h0)) || (hT && !aligned16(hT))) return KDA_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int H = (int)shape->H;
+    const int64_t T_total = shape->B * shape->T;
+    if ((st = set_smem(kda_fwd_intra_kernel, fwd_intra_smem_bytes())) != KDA_OK) return st;
+    if ((st = set_smem(kda_fwd_scan_kernel, fwd_scan_smem_bytes())) != KDA_OK) return st;
+
+    kda_clear_status_kernel<<<1, 1, 0, s>>>(ws);
+    kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
+    if (lay.nc_max > 0 && T_total > 0)
+        kda_fwd_intra_kernel<<<dim3((unsigned)lay.nc_max, (unsigned)H), 256, fwd_intra_smem_bytes(), s>>>(
+            q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, ws, lay);
+    if (shape->N > 0)
+        kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, fwd_scan_smem_bytes(), s>>>(
+            h0, o, hT, H, shape->scale, ws, lay);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status kda_bwd(const kda_shape*, const kda_bf16*, const kda_bf16*, const kda_bf16*,
+                              const kda_bf16*, const kda_bf16*, const float*, const float*, const float*,
+                              const int64_t*, const kda_bf16*, const float*, kda_bf16*, kda_bf16*, kda_bf16*,
+                              kda_bf16*, kda_bf16*, float*, float*, float*, void*, size_t, void*) {
+    return KDA_ERR_UNSUPPORTED;
+}
+
+extern "C" kda_status kda_get_device_status(const void* workspace, void* stream) {
+    if (!workspace) return KDA_ERR_NULL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    return static_cast<kda_status>(word);
+}
+
+extern "C" const char* kda_status_string(kda_status s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_NULL: return "KDA_ERR_NULL";
+        case KDA_ERR_ALIGN: return "KDA_ERR_ALIGN";
+        case KDA_ERR_SHAPE: return "KDA_ERR_SHAPE";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+        case KDA_ERR_WORKSPACE: return "KDA_ERR_WORKSPACE";
+        case KDA_ERR_OFFSETS: return "KDA_ERR_OFFSETS";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    }
+    return "KDA_ERR_UNKNOWN";
+}

@@ -1,0 +1,211 @@
+// Forward state scan: one CTA per (sequence, head), chunks in order. The fp32
+// state S (V x K = 128 x 128, value-first) lives in tensor memory (lane v =
+// value row, column k = key channel). Per chunk, with the intra-chunk images
+// W, Q^*Gamma, (K^*e^{G_L-G})^T, Aqk, U, exp(G_L):
+//   Ut^T = U^T - S0 W^T                  (tcgen05, M=128 N=64 K=128)
+//   O^T  = S0 (Q^*Gamma)^T + Ut^T Aqk^T  (tcgen05)
+//   S_L  = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G})
+//   o    = scale * O
+// (chunk form of S_t = S_{t-1} diag(e^{g_t}) (I - b k^ k^T) + b v k^T,
+//  o_t = scale S_t q^_t; flashinfer "kda_backward" contract). S0 of every
+// chunk, rounded to tf32 as the MMAs use it, is checkpointed to the
+// workspace for the backward, together with Ut.
+#include "kda_internal.cuh"
+#include "umma.cuh"
+
+namespace kda {
+
+namespace {
+struct ScanSmem {
+    // operand tiles, 1024-byte aligned (panels)
+    uint8_t S0[kTileDD];       // [128 v][128 k]
+    uint8_t W[kTileCK];        // [64 c][128 k]     \ one bulk group
+    uint8_t QB[kTileCK];       // [64 c][128 k]     /
+    uint8_t KBT[kTileCK];      // [128 k][64 c]     \ one bulk group
+    uint8_t AQK[kTileCC];      // [64 i][64 j]      /
+    uint8_t UT[kTileCK];       // [128 v][64 c]
+    float gam[D];
+    uint64_t barA, barB, barM1, barM2;
+    uint32_t tmem;
+};
+}  // namespace
+
+size_t fwd_scan_smem_bytes() { return sizeof(ScanSmem) + 1024; }
+
+__global__ void __launch_bounds__(128, 1)
+    kda_fwd_scan_kernel(const float* __restrict__ h0, uint16_t* __restrict__ o, float* __restrict__ hT, int H,
+                        float scale, uint8_t* __restrict__ ws, Layout lay) {
+    extern __shared__ uint8_t smem_raw[];
+    ScanSmem& s = *reinterpret_cast<ScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (read_status(ws) != 0) return;
+    const int h = blockIdx.x;
+    const int n = reinterpret_cast<const int*>(ws + lay.seq_order)[blockIdx.y];
+    const int cf = reinterpret_cast<const int*>(ws + lay.seq_first)[n];
+    const int cl = reinterpret_cast<const int*>(ws + lay.seq_first)[n + 1];
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int v = tid;   // state row / TMEM lane owned by this thread
+    const size_t sidx = ((size_t)n * H + h) * D * D;
+
+    if (warp == 0) {
+        tmem_alloc(&s.tmem, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&s.barA, 1); mbar_init(&s.barB, 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s.tmem;
+    const uint32_t tS = tm, tUT = tm + 128, tOT = tm + 192;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    // initial state into TMEM
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = h0 ? h0[sidx + (size_t)v * D + c0 + j] : 0.0f;
+        tmem_st32(tS + lane_base + c0, r);
+    }
+
+    auto issue_A = [&](int chunk) {
+        const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
+        mbar_arrive_expect_tx(&s.barA, (uint32_t)(2 * kTileCK));
+        bulk_g2s(s.W, img + ImgOff::W, (uint32_t)(2 * kTileCK), &s.barA);
+    };
+    auto issue_B = [&](int chunk) {
+        const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
+        mbar_arrive_expect_tx(&s.barB, (uint32_t)(kTileCK + kTileCC));
+        bulk_g2s(s.KBT, img + ImgOff::KBT, (uint32_t)(kTileCK + kTileCC), &s.barB);
+    };
+    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;   // bulk groups (thread 0)
+    if (tid == 0 && cf < cl) { issue_A(cf); issue_B(cf); a_issued = b_issued = 1; }
+
+    bool ok = true;
+    const uint32_t idS0W = idesc_tf32(128, 64, 0, 0);
+    const uint32_t idS = idesc_tf32(128, 128, 0, 0);
+    for (int chunk = cf; chunk < cl && ok; ++chunk) {
+        const uint32_t par = (uint32_t)((chunk - cf) & 1);
+        const ChunkInfo ci = chunks[chunk];
+        const size_t tile = (size_t)chunk * H + h;
+        const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
+        const float* gU = reinterpret_cast<const float*>(img + ImgOff::U);
+        s.gam[v] = reinterpret_cast<const float*>(img + ImgOff::GAML)[v];
+        if (tid == 0) bulk_wait_read_all();   // previous checkpoint copy finished reading S0
+        __syncthreads();
+
+        // S0: TMEM -> registers -> tf32 operand in smem; decayed state back to TMEM
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float r[32];
+            tmem_ld32(tS + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4) {
+                const float4 q4 = make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]),
+                                              tf32_round(r[j + 3]));
+                *reinterpret_cast<float4*>(s.S0 + panel_off(v, c0 + j, D)) = q4;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
+            tmem_st32(tS + lane_base + c0, r);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+
+        if (tid == 0) {
+            bulk_s2g(ws + lay.s0 + tile * kTileDD, s.S0, (uint32_t)kTileDD);
+            bulk_commit();
+            if (!mbar_wait(&s.barA, par)) ok = false;
+            else ++a_done;
+            if (ok) {
+                const uint32_t a = smem_u32(s.S0), bw = smem_u32(s.W), bq = smem_u32(s.QB);
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_tf32(tUT, desc_kmajor(a, D, ks), desc_kmajor(bw, C, ks), idS0W, ks > 0);
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_tf32(tOT, desc_kmajor(a, D, ks), desc_kmajor(bq, C, ks), idS0W, ks > 0);
+                umma_commit(&s.barM1);
+            }
+        }
+        // U column v of this chunk
+        float u[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) u[c] = gU[c * D + v];
+        ok = mbar_wait(&s.barM1, par) && ok;
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && chunk + 1 < cl) { issue_A(chunk + 1); ++a_issued; }
+
+        // Ut^T = U^T - S0 W^T  -> tf32 operand [v][c]; Ut -> workspace [c][v] panels
+        uint8_t* gUt = ws + lay.ut + tile * kTileCK;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            float r[32];
+            tmem_ld32(tUT + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = tf32_round(u[c0 + j] - r[j]);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(s.UT + panel_off(v, c0 + j, D)) =
+                    make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gUt + panel_off(c0 + j, v, C)) = r[j];
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            if (!mbar_wait(&s.barB, par)) ok = false;
+            else ++b_done;
+            if (ok) {
+                const uint32_t a = smem_u32(s.UT), bq = smem_u32(s.AQK), bk = smem_u32(s.KBT);
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32(tOT, desc_kmajor(a, D, ks), desc_kmajor(bq, C, ks), idS0W, 1);
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32(tS, desc_kmajor(a, D, ks), desc_kmajor(bk, D, ks), idS, 1);
+                umma_commit(&s.barM2);
+            }
+        }
+        ok = mbar_wait(&s.barM2, par) && ok;
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && chunk + 1 < cl) { issue_B(chunk + 1); ++b_issued; }
+
+        // o = scale * O
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            float r[32];
+            tmem_ld32(tOT + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int i = c0 + j;
+                if (i < ci.L) o[((size_t)(ci.t0 + i) * H + h) * D + v] = f2bf(scale * r[j]);
+            }
+        }
+    }
+    if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
+
+    // final state
+    if (ok && hT) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float r[32];
+            tmem_ld32(tS + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hT[sidx + (size_t)v * D + c0 + j] = r[j];
+        }
+    }
+    if (tid == 0) {
+        // drain copies still in flight (only after an aborted scan), bounded
+        for (; a_done < a_issued; ++a_done) mbar_wait(&s.barA, (uint32_t)(a_done & 1));
+        for (; b_done < b_issued; ++b_done) mbar_wait(&s.barB, (uint32_t)(b_done & 1));
+        bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+}  // namespace kda

@@ -1,0 +1,123 @@
+// Internal definitions shared by the KDA kernels: chunk geometry, workspace
+// layout, device status word, small math helpers.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+constexpr int D = 128;         // K = V = 128
+constexpr int C = 64;          // chunk length
+constexpr int SUB = 16;        // sub-block length inside a chunk
+constexpr int NSUB = C / SUB;  // sub-blocks per chunk
+
+// Per-tile (chunk, head) image sizes in the workspace, bytes.
+constexpr size_t kTileCK = (size_t)C * D * 4;     // [64][128] fp32
+constexpr size_t kTileCC = (size_t)C * C * 4;     // [64][64]  fp32
+constexpr size_t kTileDD = (size_t)D * D * 4;     // [128][128] fp32
+
+// Forward intra-chunk images per tile, written by the intra-chunk kernel.
+// "panels" = the 128-byte-swizzled K-major operand layout of umma.cuh
+// (values rounded to tf32); R = rows of the image.
+//   read by the forward scan:
+//     W    [64][128]  panels R=64    W = T (K^ * Gamma)
+//     QB   [64][128]  panels R=64    Q^ * Gamma
+//     KBT  [128][64]  panels R=128   (K^ * exp(G_L - G))^T
+//     AQK  [64][64]   panels R=64    Aqk (decayed q^.k^, j <= i)
+//     U    [64][128]  row-major fp32 U = T V (not rounded)
+//     GAML [128]      fp32           exp(G_L)
+//   read by the backward scan:
+//     WT   [128][64]  panels R=128   W^T
+//     QBT  [128][64]  panels R=128   (Q^ * Gamma)^T
+//     KB   [64][128]  panels R=64    K^ * exp(G_L - G)
+//     AQKT [64][64]   panels R=64    Aqk^T
+struct ImgOff {
+    static constexpr size_t W = 0;
+    static constexpr size_t QB = W + kTileCK;
+    static constexpr size_t KBT = QB + kTileCK;
+    static constexpr size_t AQK = KBT + kTileCK;
+    static constexpr size_t FWD_BULK = AQK + kTileCC;   // bytes bulk-loaded by the forward scan
+    static constexpr size_t U = FWD_BULK;
+    static constexpr size_t GAML = U + kTileCK;
+    static constexpr size_t WT = GAML + 1024;
+    static constexpr size_t QBT = WT + kTileCK;
+    static constexpr size_t KB = QBT + kTileCK;
+    static constexpr size_t AQKT = KB + kTileCK;
+    static constexpr size_t BWD_BULK = AQKT + kTileCC - WT;  // bytes bulk-loaded by the backward scan
+    static constexpr size_t BYTES = AQKT + kTileCC;
+};
+
+// Backward state-product outputs per tile (row-major fp32).
+struct BgOff {
+    static constexpr size_t DQB = 0;                 // dQbar [64][128]
+    static constexpr size_t DW = DQB + kTileCK;      // dW    [64][128]
+    static constexpr size_t DKB = DW + kTileCK;      // dKbar [64][128]
+    static constexpr size_t DAQK = DKB + kTileCK;    // dAqk  [64][64] (scale included)
+    static constexpr size_t DGAM = DAQK + kTileCC;   // sum_v dS_L * S0 [128]
+    static constexpr size_t BYTES = ((DGAM + D * 4) + 1023) & ~size_t(1023);
+};
+
+struct ChunkInfo {
+    int32_t t0;   // first token (global, packed index)
+    int32_t L;    // rows in this chunk (1..64); 0 = unused slot
+    int32_t n;    // sequence
+    int32_t c;    // chunk index inside the sequence
+};
+
+struct Layout {
+    int64_t nc_max;      // chunk slots
+    int64_t H;
+    size_t status, chunks, seq_first, seq_order;
+    size_t img, s0, ut, ds, dut, bg, part;
+    size_t total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+__host__ __device__ inline int64_t chunk_slots(int64_t B, int64_t T, int64_t N, bool packed) {
+    return packed ? (B * T) / C + N + 1 : B * ((T + C - 1) / C);
+}
+
+__host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, int64_t N, bool packed) {
+    Layout l;
+    l.nc_max = chunk_slots(B, T, N, packed);
+    l.H = H;
+    const int64_t tiles = l.nc_max * H;
+    size_t o = 0;
+    l.status = o;      o = align_up(o + 256, 1024);
+    l.chunks = o;      o = align_up(o + (size_t)l.nc_max * sizeof(ChunkInfo), 1024);
+    l.seq_first = o;   o = align_up(o + (size_t)(N + 1) * 4, 1024);
+    l.seq_order = o;   o = align_up(o + (size_t)(N + 1) * 4, 1024);
+    l.img = o;         o += (size_t)tiles * ImgOff::BYTES;
+    l.s0 = o;          o += (size_t)tiles * kTileDD;
+    l.ut = o;          o += (size_t)tiles * kTileCK;
+    l.ds = o;          o += (size_t)tiles * kTileDD;
+    l.dut = o;         o += (size_t)tiles * kTileCK;
+    l.bg = o;          o += (size_t)tiles * BgOff::BYTES;
+    l.part = o;        o = align_up(o + (size_t)tiles * (D + 4) * 4, 1024);
+    l.total = o;
+    return l;
+}
+
+// Device status word helpers (first int32 of the workspace).
+__device__ __forceinline__ int read_status(const uint8_t* ws) {
+    return *reinterpret_cast<const volatile int*>(ws);
+}
+__device__ __forceinline__ void raise_status(uint8_t* ws, int code) {
+    atomicCAS(reinterpret_cast<int*>(ws), 0, code);
+}
+
+__device__ __forceinline__ float bf2f(uint16_t x) { return __uint_as_float(((uint32_t)x) << 16); }
+__device__ __forceinline__ uint16_t f2bf(float x) {
+    __nv_bfloat16 b = __float2bfloat16_rn(x);
+    return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// sigmoid via the CUDA exponential and an IEEE division
+__device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+}  // namespace kda

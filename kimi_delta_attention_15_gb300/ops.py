@@ -1,0 +1,166 @@
+"""Thin Python binding of the C ABI in ``include/kda.h``.
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``_build/libkda.so``. PyTorch provides device memory and streams.
+Loading fails loudly (RuntimeError) when the library is missing; there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KDA_OK = 0
+_STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_ALIGN", 3: "KDA_ERR_SHAPE",
+           4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_WORKSPACE", 6: "KDA_ERR_OFFSETS",
+           7: "KDA_ERR_TIMEOUT", 8: "KDA_ERR_CUDA"}
+
+SCALE = 1.0 / math.sqrt(128.0)
+LOWER_BOUND = -5.0
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code, where=""):
+        self.code = int(code)
+        super().__init__(f"{where}: {_STATUS.get(self.code, self.code)}")
+
+
+class Shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
+                ("scale", ctypes.c_float), ("lower_bound", ctypes.c_float)]
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True):
+    """Load ``libkda.so`` (building it first if asked and missing)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            if not build_if_missing:
+                raise RuntimeError(f"KDA CUDA library not built: {path}")
+            _build.build()
+        lib = ctypes.CDLL(path)
+        P, S, I64 = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int64
+        lib.kda_workspace_size.argtypes = [ctypes.POINTER(Shape)]
+        lib.kda_workspace_size.restype = S
+        lib.kda_fwd.argtypes = [ctypes.POINTER(Shape)] + [P] * 11 + [P, S, P]
+        lib.kda_fwd.restype = ctypes.c_int
+        lib.kda_bwd.argtypes = [ctypes.POINTER(Shape)] + [P] * 19 + [P, S, P]
+        lib.kda_bwd.restype = ctypes.c_int
+        lib.kda_get_device_status.argtypes = [P, P]
+        lib.kda_get_device_status.restype = ctypes.c_int
+        lib.kda_status_string.argtypes = [ctypes.c_int]
+        lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
+        lib.kda_diag_umma_selftest.restype = ctypes.c_int
+        _lib = lib
+        return lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def make_shape(T: int, H: int, N: int, B: int = 1, scale: float = SCALE,
+               lower_bound: float = LOWER_BOUND) -> Shape:
+    return Shape(B=B, T=T, H=H, N=N, K=128, V=128, scale=scale, lower_bound=lower_bound)
+
+
+def workspace_size(shape: Shape) -> int:
+    return int(load().kda_workspace_size(ctypes.byref(shape)))
+
+
+def _check(code, where):
+    if code != KDA_OK:
+        raise KdaError(code, where)
+
+
+def _shape_of(q, cu_seqlens, B, scale, lower_bound):
+    if cu_seqlens is not None:
+        T, H = q.shape[0], q.shape[1]
+        return make_shape(T, H, cu_seqlens.numel() - 1, 1, scale, lower_bound)
+    if q.dim() == 4:
+        B_, T, H = q.shape[0], q.shape[1], q.shape[2]
+        return make_shape(T, H, B_, B_, scale, lower_bound)
+    T, H = q.shape[0], q.shape[1]
+    return make_shape(T // B, H, B, B, scale, lower_bound)
+
+
+def alloc_workspace(shape: Shape, device) -> torch.Tensor:
+    return torch.empty(workspace_size(shape), dtype=torch.uint8, device=device)
+
+
+def fwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B: int = 1,
+        scale: float = SCALE, lower_bound: float = LOWER_BOUND, workspace=None, o=None,
+        hT=None, want_hT: bool = True, stream=None):
+    """kda_fwd. Token tensors [T, H, 128] bf16 (or [B, T, H, 128]); returns (o, hT, workspace)."""
+    lib = load()
+    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    if workspace is None:
+        workspace = alloc_workspace(shape, q.device)
+    if o is None:
+        o = torch.empty_like(v)
+    if hT is None and want_hT:
+        hT = torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32, device=q.device)
+    code = lib.kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                       _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(hT),
+                       _ptr(workspace), workspace.numel(), _stream_handle(stream))
+    _check(code, "kda_fwd")
+    return o, hT, workspace
+
+
+def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seqlens=None,
+        dhT=None, *, B: int = 1, scale: float = SCALE, lower_bound: float = LOWER_BOUND,
+        grads=None, want_dh0: bool = True, stream=None):
+    """kda_bwd with the workspace filled by ``fwd``. Returns a dict of gradients."""
+    lib = load()
+    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
+                     dg_raw=torch.empty_like(g_raw), dbeta_raw=torch.empty_like(beta_raw),
+                     dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias),
+                     dh0=(torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32,
+                                      device=q.device) if want_dh0 else None))
+    code = lib.kda_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+                       _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), _ptr(do), _ptr(dhT),
+                       _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg_raw"]),
+                       _ptr(grads["dbeta_raw"]), _ptr(grads["dA_log"]), _ptr(grads["ddt_bias"]),
+                       _ptr(grads.get("dh0")), _ptr(workspace), workspace.numel(),
+                       _stream_handle(stream))
+    _check(code, "kda_bwd")
+    return grads
+
+
+def device_status(workspace, stream=None) -> int:
+    return int(load().kda_get_device_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def umma_selftest(A, B, a_mn: int, b_mn: int):
+    """Diagnostic: D = A @ B^T through tcgen05 kind::tf32 (see include/kda.h)."""
+    lib = load()
+    N, Kd = B.shape
+    D = torch.empty(2, 128, N, dtype=torch.float32, device=A.device)
+    code = lib.kda_diag_umma_selftest(a_mn, b_mn, N, Kd, _ptr(A), _ptr(B), _ptr(D), _stream_handle())
+    _check(code, "kda_diag_umma_selftest")
+    return D
