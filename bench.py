@@ -1,0 +1,354 @@
+#!/usr/bin/env python3
+"""Throughput of the KDA forward + full backward on GB300.
+
+One step = kda_fwd + kda_bwd (every kernel of the hot path) on the fixed
+T=8192, H=96, K=V=128 workload (bf16 tokens, fp32 parameters and state), with
+inputs resident in HBM. Metric: token*heads per second of fwd+bwd (also
+TFLOP/s on the fixed algorithmic count of 421,888 flop per token*head).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+N > 1 runs under torchrun: every rank runs its own copy of the workload
+(independent sequences and heads: weak scaling, no collective on the data
+path); the time is the max over ranks. `--impl reference` times the fp64 CPU
+oracle on the host cores, on a bounded sample of the same workload (rank 0).
+Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FLOP_PER_TH = 421_888           # fwd 140,629 + bwd 281,259 per token*head (C = 64, d = 128)
+METRIC = "fwd+bwd tokens·heads/s and TFLOP/s (% of bf16 TC peak) at T=8192,H=96,K=V=128"
+UNIT = "tokens*heads/s"
+L2_FLUSH_BYTES = 512 << 20
+
+# Per-kernel algorithmic traffic and MMA work per (chunk, head) tile: the
+# tensors each kernel reads and writes once at its interface, and the flops
+# of its products (triangular products counted at half size).
+KB = 1024
+KERNEL_MODEL = {
+    # name: (bytes per tile, flops per tile)
+    "fwd_intra": ((64 + 0.125) * KB + 288.5 * KB, 2.5e6),
+    "fwd_scan": (256.5 * KB, 7.34e6),
+    "bwd_scan": (224.5 * KB, 7.34e6),
+    "bwd_state": (320.5 * KB, 6.82e6),
+    "bwd_wy": (208.0 * KB, 4.1e6),
+    "bwd_pair": (225.0 * KB, 2.62e6),
+}
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                                          "-i", str(self.index), "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append([x.strip() for x in line.split(",")])
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in self.rows:
+            for i, nme in enumerate(names):
+                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                    reasons.add(nme)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def reduce_max(value, ws, device=None):
+    """Max of a float over ranks (identity at world size 1)."""
+    if ws == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_oracle_sample(inp, heads, nthreads):
+    """Time the fp64 oracle (forward + backward) on `heads` heads of the workload."""
+    import oracle
+    sub = {}
+    for k, v in inp.items():
+        if k in ("q", "k", "v", "g_raw", "do"):
+            sub[k] = v[:, :heads]
+        elif k == "beta_raw":
+            sub[k] = v[:, :heads]
+        elif k in ("A_log", "dt_bias"):
+            sub[k] = v[:heads]
+        elif k in ("h0", "dhT"):
+            sub[k] = None if v is None else v[:, :heads]
+        else:
+            sub[k] = v
+    t0 = time.perf_counter()
+    oracle.forward(sub, nthreads=nthreads)
+    oracle.backward(sub, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return dt, sub["q"].shape[0] * heads
+
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from kimi_delta_attention_15_gb300 import inputs as I
+    import oracle
+    w = I.WORKLOADS[I.HEADLINE]
+    inp = I.make_inputs(w)
+    cores = oracle.default_threads()
+    heads = max(1, min(w.H, cores))
+    oracle.build()
+    for _ in range(args.warmup):
+        cpu_oracle_sample(inp, heads, cores)
+    total, units = 0.0, 0
+    for _ in range(args.steps):
+        dt, n = cpu_oracle_sample(inp, heads, cores)
+        total += dt
+        units += n
+    value = units / total
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "K": 128, "V": 128, "global_batch": 1,
+                       "seq_len": w.T, "parallelism": "host threads"},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": f"{heads} of {w.H} heads x {w.T} tokens, fwd+bwd, per step"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gb300(args, ws, rank, local):
+    import torch
+    from kimi_delta_attention_15_gb300 import inputs as I, ops
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = _init_dist(ws, "nccl")
+    w = I.WORKLOADS[I.HEADLINE]
+    inp = I.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    shape = ops.make_shape(w.T, w.H, 1)
+    wsp = ops.alloc_workspace(shape, dev)
+    o = torch.empty_like(d["v"])
+    hT = torch.empty(1, w.H, 128, 128, device=dev)
+    grads = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]), dv=torch.empty_like(d["v"]),
+                 dg_raw=torch.empty_like(d["g_raw"]), dbeta_raw=torch.empty_like(d["beta_raw"]),
+                 dA_log=torch.empty_like(d["A_log"]), ddt_bias=torch.empty_like(d["dt_bias"]),
+                 dh0=torch.empty(1, w.H, 128, 128, device=dev))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], workspace=wsp,
+                o=o, hT=hT)
+        ops.bwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], d["do"], wsp,
+                grads=grads)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if ops.device_status(wsp) != 0:
+        raise RuntimeError("device status after warm-up: %d" % ops.device_status(wsp))
+
+    timer = ops.KernelTimer()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    per_kernel = {k: 0.0 for k in ops.KERNEL_SLOTS}
+    clocks = ClockSampler(local)
+    if ws > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()                      # evict L2 between steps
+        starts[i].record(stream)
+        with timer:
+            step()
+        ends[i].record(stream)
+        ends[i].synchronize()
+        for k, v in timer.times_ms().items():
+            per_kernel[k] += v
+    torch.cuda.synchronize()
+    if ws > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = reduce_max(sum(step_ms), ws, dev)
+    ms_per_step = total_ms / args.steps
+    value = ws * w.token_heads / (ms_per_step * 1e-3)
+    tflops = ws * w.token_heads * FLOP_PER_TH / (ms_per_step * 1e-3) / 1e12
+    hbm, bf16, bf16s, peak_src = _peaks()
+
+    # dominant kernel and its roofline
+    kms = {k: v / args.steps for k, v in per_kernel.items()}
+    dom = max(KERNEL_MODEL, key=lambda k: kms[k])
+    tiles = 128 * w.H
+    bytes_tile, flops_tile = KERNEL_MODEL[dom]
+    t_s = kms[dom] * 1e-3
+    gbs = bytes_tile * tiles / t_s / 1e9
+    tfl = flops_tile * tiles / t_s / 1e12
+    hbm_frac, tc_frac = gbs / hbm, tfl / bf16
+    bound = "hbm" if hbm_frac >= tc_frac else "tensor"
+    roof = ({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": hbm_frac}
+            if bound == "hbm" else
+            {"bound": "tensor", "achieved": tfl, "peak": bf16, "unit": "TFLOP/s", "frac": tc_frac})
+    roof.update({"kernel": dom, "traffic": None, "peak_source": peak_src,
+                 "kernel_ms": {k: round(v, 4) for k, v in kms.items()}})
+
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16 io, tf32 mma, fp32 accum/state", "data": "synthetic",
+            "config": {"workload": w.name, "T": w.T, "H": w.H, "K": 128, "V": 128, "global_batch": 1,
+                       "seq_len": w.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
+                       "l2": "flushed (512 MiB write) before every timed step"},
+            "tflops": tflops, "pct_bf16_peak": tflops / bf16,
+            "roofline": roof, "clocks": clk, "gpu_launches": 9 * args.steps}
+
+    # end to end through the public API with pinned host buffers
+    if not args.no_e2e:
+        line["e2e"] = e2e(args, inp, dev)
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        import oracle
+        cores = oracle.default_threads()
+        heads = max(1, min(w.H, cores))
+        dt, n = cpu_oracle_sample(inp, heads, cores)
+        line["cpu_baseline"] = {"value": n / dt, "unit": UNIT, "cores": cores, "kind": "oracle",
+                                "sample": f"{heads} of {w.H} heads x {w.T} tokens, fwd+bwd, {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        dist.destroy_process_group()
+
+
+def e2e(args, inp, dev):
+    """Same metric with host buffers: H2D of every input from pinned memory,
+    kda_fwd + kda_bwd, D2H of the output and every gradient, all timed."""
+    import torch
+    from kimi_delta_attention_15_gb300 import ops, inputs as I
+    w = I.WORKLOADS[I.HEADLINE]
+    names = ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "do")
+    host = {k: inp[k].pin_memory() for k in names}
+    dv = {k: torch.empty_like(host[k], device=dev) for k in names}
+    shape = ops.make_shape(w.T, w.H, 1)
+    wsp = ops.alloc_workspace(shape, dev)
+    out_host = {"o": torch.empty_like(host["v"]).pin_memory()}
+    for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias"):
+        out_host["d" + k] = torch.empty_like(host[k]).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    stream = torch.cuda.current_stream()
+
+    def step():
+        for k in names:
+            dv[k].copy_(host[k], non_blocking=True)
+        o, _, _ = ops.fwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"],
+                          workspace=wsp, want_hT=False)
+        g = ops.bwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"], dv["do"],
+                    wsp, want_dh0=False)
+        out_host["o"].copy_(o, non_blocking=True)
+        for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias"):
+            out_host["d" + k].copy_(g["d" + k], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(args.steps):
+        step()
+    e.record(stream)
+    e.synchronize()
+    ms = s.elapsed_time(e) / args.steps
+    return {"value": w.token_heads / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        if ws > 1:
+            _init_dist(ws, "gloo")
+        run_reference(args, ws, rank)
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    run_gb300(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

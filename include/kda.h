@@ -105,7 +105,8 @@ kda_status kda_bwd(const kda_shape* shape,
                    const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
                    const kda_bf16* g_raw, const kda_bf16* beta_raw,
                    const float* A_log, const float* dt_bias,
-                   const float* h0, const int64_t* cu_seqlens,
+                   const float* h0 /* unused: the forward's checkpoints carry it; may be NULL */,
+                   const int64_t* cu_seqlens,
                    const kda_bf16* do_, const float* dhT,
                    kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg_raw,
                    kda_bf16* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0,
@@ -116,16 +117,28 @@ kda_status kda_bwd(const kda_shape* shape,
  * stream reported an error. Clears nothing. */
 kda_status kda_get_device_status(const void* workspace, void* stream);
 
+/* Profiling hook. When `events` is non-NULL (an array of `count` cudaEvent_t
+ * created by the caller), kda_fwd records events[0..3] and kda_bwd
+ * events[4..9] on the call's stream around its kernels:
+ *   [0,1) status clear + chunk table   [1,2) intra-chunk   [2,3) forward scan
+ *   [4,5) backward scan  [5,6) state products  [6,7) WY backward
+ *   [7,8) pair/gate backward  [8,9) parameter reduction
+ * (events[3] and events[9] mark the end of each call). Process-wide setting,
+ * not thread-safe; pass NULL to switch it off. Returns KDA_OK. */
+int kda_set_profile_events(void* const* events, int count);
+
 /* Human-readable name of a status code (static string). */
 const char* kda_status_string(kda_status s);
 
 /* Diagnostics: one CTA computes D[128 x N] = A[128 x Kd] * B[N x Kd]^T with
- * tcgen05 kind::tf32 (operands rounded to tf32), A stored in shared memory
- * K-major (a_mn = 0) or MN-major (a_mn = 1), likewise B. D holds 2*128*N
- * floats: the product, then (2 * product + row index) after a round trip
- * through tcgen05.st / tcgen05.ld. A, B, D are device pointers, row-major.
- * N in {32, 64, ..., 256}, Kd in {32, 64, 96, 128}. Used by the tests to
- * check the descriptors and the TMEM data path. */
+ * tcgen05 kind::tf32 (operands rounded to tf32), both operands stored in
+ * shared memory K-major with the 128-byte swizzle the kernels use (a_mn and
+ * b_mn must be 0: tf32 operands are K-major only; anything else returns
+ * KDA_ERR_UNSUPPORTED). D holds 2*128*N floats: the product, then
+ * (2 * product + row index) after a round trip through tcgen05.st /
+ * tcgen05.ld. A, B, D are device pointers, row-major. N in {16, 32, ..., 256},
+ * Kd in {32, 64, 96, 128} (else KDA_ERR_SHAPE). Used by the tests to check
+ * the descriptors and the TMEM data path. */
 int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, const float* B,
                            float* D, void* stream);
 

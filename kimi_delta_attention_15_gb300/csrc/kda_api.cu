@@ -9,16 +9,19 @@ size_t fwd_intra_smem_bytes();
 size_t fwd_scan_smem_bytes();
 size_t bwd_scan_smem_bytes();
 size_t bwd_state_smem_bytes();
-size_t bwd_intra_smem_bytes();
+size_t bwd_wy_smem_bytes();
+size_t bwd_pair_smem_bytes();
 
 __global__ void kda_fwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
                                      const uint16_t*, const float*, const float*, int, float, uint8_t*, Layout);
 __global__ void kda_fwd_scan_kernel(const float*, uint16_t*, float*, int, float, uint8_t*, Layout);
 __global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, float, uint8_t*, Layout);
 __global__ void kda_bwd_state_kernel(const uint16_t*, int, float, uint8_t*, Layout);
-__global__ void kda_bwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
-                                     const uint16_t*, const float*, const float*, const uint16_t*, int, float,
-                                     uint16_t*, uint16_t*, uint16_t*, uint16_t*, uint16_t*, uint8_t*, Layout);
+__global__ void kda_bwd_wy_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*, const float*,
+                                  const float*, int, float, uint16_t*, uint8_t*, Layout);
+__global__ void kda_bwd_pair_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+                                    const float*, const float*, int, float, uint16_t*, uint16_t*, uint16_t*,
+                                    uint16_t*, uint8_t*, Layout);
 __global__ void kda_param_reduce_kernel(int, float*, float*, uint8_t*, Layout);
 
 // Chunk table from the offsets: validates cu_seqlens (cu[0] = 0, non-decreasing,
@@ -103,6 +106,13 @@ using namespace kda;
 
 namespace {
 
+// Optional per-kernel timing events (kda_set_profile_events).
+const cudaEvent_t* g_prof = nullptr;
+int g_prof_n = 0;
+inline void prof(int slot, cudaStream_t s) {
+    if (g_prof && slot < g_prof_n) cudaEventRecord(g_prof[slot], s);
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 kda_status check_shape(const kda_shape* sh, bool packed) {
@@ -170,22 +180,72 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     if ((st = set_smem(kda_fwd_intra_kernel, fwd_intra_smem_bytes())) != KDA_OK) return st;
     if ((st = set_smem(kda_fwd_scan_kernel, fwd_scan_smem_bytes())) != KDA_OK) return st;
 
+    prof(0, s);
     kda_clear_status_kernel<<<1, 1, 0, s>>>(ws);
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
+    prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
         kda_fwd_intra_kernel<<<dim3((unsigned)lay.nc_max, (unsigned)H), 256, fwd_intra_smem_bytes(), s>>>(
             q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, ws, lay);
+    prof(2, s);
     if (shape->N > 0)
         kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, fwd_scan_smem_bytes(), s>>>(
             h0, o, hT, H, shape->scale, ws, lay);
+    prof(3, s);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-extern "C" kda_status kda_bwd(const kda_shape*, const kda_bf16*, const kda_bf16*, const kda_bf16*,
-                              const kda_bf16*, const kda_bf16*, const float*, const float*, const float*,
-                              const int64_t*, const kda_bf16*, const float*, kda_bf16*, kda_bf16*, kda_bf16*,
-                              kda_bf16*, kda_bf16*, float*, float*, float*, void*, size_t, void*) {
-    return KDA_ERR_UNSUPPORTED;
+extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                              const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log,
+                              const float* dt_bias, const float* h0, const int64_t* cu_seqlens, const kda_bf16* do_,
+                              const float* dhT, kda_bf16* dq, kda_bf16* dk, kda_bf16* dv, kda_bf16* dg_raw,
+                              kda_bf16* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+    (void)h0;   // the forward's checkpoints in the workspace carry the initial state
+    Layout lay;
+    kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay);
+    if (st != KDA_OK) return st;
+    if (!q || !k || !v || !g_raw || !beta_raw || !A_log || !dt_bias || !do_ || !dq || !dk || !dv || !dg_raw ||
+        !dbeta_raw || !dA_log || !ddt_bias)
+        return KDA_ERR_NULL;
+    const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, do_, dq, dk, dv, dg_raw, dbeta_raw, dA_log, ddt_bias};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return KDA_ERR_ALIGN;
+    if ((dhT && !aligned16(dhT)) || (dh0 && !aligned16(dh0))) return KDA_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const int H = (int)shape->H;
+    const float lb = shape->lower_bound, scale = shape->scale;
+    if ((st = set_smem(kda_bwd_scan_kernel, bwd_scan_smem_bytes())) != KDA_OK) return st;
+    if ((st = set_smem(kda_bwd_state_kernel, bwd_state_smem_bytes())) != KDA_OK) return st;
+    if ((st = set_smem(kda_bwd_wy_kernel, bwd_wy_smem_bytes())) != KDA_OK) return st;
+    if ((st = set_smem(kda_bwd_pair_kernel, bwd_pair_smem_bytes())) != KDA_OK) return st;
+    const dim3 tiles((unsigned)lay.nc_max, (unsigned)H);
+    prof(4, s);
+    if (shape->N > 0)
+        kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, bwd_scan_smem_bytes(), s>>>(
+            do_, dhT, dh0, H, scale, ws, lay);
+    prof(5, s);
+    if (lay.nc_max > 0)
+        kda_bwd_state_kernel<<<tiles, 128, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws, lay);
+    prof(6, s);
+    if (lay.nc_max > 0)
+        kda_bwd_wy_kernel<<<tiles, 256, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,
+                                                                   ws, lay);
+    prof(7, s);
+    if (lay.nc_max > 0)
+        kda_bwd_pair_kernel<<<tiles, 256, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
+                                                                       dq, dk, dg_raw, dbeta_raw, ws, lay);
+    prof(8, s);
+    kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);
+    prof(9, s);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" int kda_set_profile_events(void* const* events, int count) {
+    g_prof = reinterpret_cast<const cudaEvent_t*>(events);
+    g_prof_n = events ? count : 0;
+    return KDA_OK;
 }
 
 extern "C" kda_status kda_get_device_status(const void* workspace, void* stream) {

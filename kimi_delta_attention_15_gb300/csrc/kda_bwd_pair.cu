@@ -1,0 +1,287 @@
+// Backward, last per-chunk stage: one CTA per (chunk, head), all chunks in
+// parallel. Gathers every adjoint of q^, k^ and of the in-chunk cumulative
+// log-decay G, then applies the reverse cumulative sum (g_t = G_t - G_{t-1})
+// and the chains of the gate, the beta sigmoid and the L2 norms:
+//   pair terms  B_ij = sum_c k^_ic k^_jc e^{G_ic-G_jc},  Aqk_ij = sum_c q^_ic k^_jc e^{G_ic-G_jc}
+//     with dB (WY kernel) and dAqk (state-products kernel), for column block J:
+//     a = dM[:,J] Kt_J,  b = dM[:,J]^T Xt_J   (Xt_J = x^ e^{G-G_eJ}, Kt_J = k^_J e^{G_eJ-G_J})
+//     dx += e^{G-G_eJ} a,  dk_J += e^{G_eJ-G_J} b,  dG += Xt_J a,  dG_J -= Kt_J b
+//     (both dG terms use the same tf32-rounded operands as the products, so the
+//      pairs inside [t, L) cancel in the reverse cumulative sum as they must);
+//   dq^ += dQbar Gamma, dk^ += dKt Gamma + dKbar e^{G_L-G},
+//   dG  += dQbar Q^Gamma + dKt K^Gamma - dKbar Kbar,
+//   dG_L = sum_i dKbar_i Kbar_i + dgam exp(G_L).
+// dg_t = sum_{i>=t} dG_i + dG_L is assembled as
+//   sum_{i>=t} (dG_i without the Kbar term) + sum_{i<t} dKbar_i Kbar_i + dgam exp(G_L)
+// which is the same sum without the cancellation of the Kbar terms.
+// Then du = dg lb s (1 - s), dg_raw = du exp(A_log), and the per-chunk
+// partial sums of ddt_bias and dA_log go to the workspace.
+#include "kda_internal.cuh"
+#include "kda_prep.cuh"
+#include "mma_sync.cuh"
+#include "umma.cuh"
+
+namespace kda {
+
+namespace {
+struct PairSmem {
+    float qe[C * PS];   // q^ E-      -> dq^
+    float ke[C * PS];   // k^ E-      -> dk^
+    float kp[C * PS];   // k^ E+      -> dG'
+    float em[C * PS];   // E-         -> dKbar Kbar, then its exclusive prefix over rows
+    float ep[C * PS];   // E+
+    float dB[C * PC];
+    float dA[C * PC];   // dAqk
+    Factors fa;
+    float beta[C], inq[C], ink[C];
+    float red[D];
+};
+}  // namespace
+
+size_t bwd_pair_smem_bytes() { return sizeof(PairSmem); }
+
+__global__ void __launch_bounds__(256, 1)
+    kda_bwd_pair_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                        const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
+                        const float* __restrict__ A_log, const float* __restrict__ dt_bias, int H, float lb,
+                        uint16_t* __restrict__ dq, uint16_t* __restrict__ dk, uint16_t* __restrict__ dg_raw,
+                        uint16_t* __restrict__ dbeta_raw, uint8_t* __restrict__ ws, Layout lay) {
+    extern __shared__ uint8_t smem_raw[];
+    PairSmem& s = *reinterpret_cast<PairSmem*>(smem_raw);
+    if (read_status(ws) != 0) return;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
+    if (ci.L <= 0) return;
+    const int L = ci.L, t0 = ci.t0;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const size_t tile = (size_t)chunk * H + h;
+    const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
+    const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
+    const float a_h = __expf(A_log[h]);
+
+    prep_rows(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp, s.beta,
+              s.inq, s.ink);
+    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+        const int r = idx >> 6, c = idx & 63;
+        s.dB[r * PC + c] = reinterpret_cast<const float*>(wy + WyOff::DB)[idx];
+        s.dA[r * PC + c] = reinterpret_cast<const float*>(bg + BgOff::DAQK)[idx];
+    }
+    __syncthreads();
+    block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);
+    __syncthreads();
+    block_factors(&s.fa);
+    __syncthreads();
+
+    // each warp owns rows 16rb + {gid, gid+8}, columns 64ch + 8nt + 2tig + {0,1}
+    const int rb = warp & 3, ch = warp >> 2;
+    float adq[8][4], adk[8][4], adg[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { adq[nt][e] = 0.0f; adk[nt][e] = 0.0f; adg[nt][e] = 0.0f; }
+
+    // (a) row side: rows of block I = rb, columns blocks J <= I
+    {
+        const int I = rb;
+        for (int m = 0; m < 2; ++m) {
+            const float* dM = m == 0 ? s.dB : s.dA;
+            const float* base = m == 0 ? s.ke : s.qe;
+            for (int J = 0; J <= I; ++J) {
+                float acc[8][4];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
+                    const int r0 = I * SUB + gid, r1 = r0 + 8;
+                    const uint32_t a0 = tf32_bits(dM[r0 * PC + j0]), a1 = tf32_bits(dM[r1 * PC + j0]);
+                    const uint32_t a2 = tf32_bits(dM[r0 * PC + j1]), a3 = tf32_bits(dM[r1 * PC + j1]);
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        const int c = ch * 64 + nt * 8 + gid;
+                        mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(s.kp[j0 * PS + c]),
+                                        tf32_bits(s.kp[j1 * PS + c]));
+                    }
+                }
+                const float* f = s.fa.F[I][J];
+#pragma unroll
+                for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+                        const float fc = f[col];
+                        const float R = s.em[row * PS + col] * fc;
+                        const float Xt = __uint_as_float(tf32_bits(base[row * PS + col] * fc));
+                        if (m == 0) adk[nt][e] += R * acc[nt][e];
+                        else adq[nt][e] += R * acc[nt][e];
+                        adg[nt][e] += Xt * acc[nt][e];
+                    }
+            }
+        }
+    }
+    // (b) column side: rows j of block J = rb, row blocks I >= J
+    {
+        const int J = rb;
+        float acc[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        for (int m = 0; m < 2; ++m) {
+            const float* dM = m == 0 ? s.dB : s.dA;
+            const float* base = m == 0 ? s.ke : s.qe;
+            for (int I = J; I < NSUB; ++I) {
+                const float* f = s.fa.F[I][J];
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk) {
+                    const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
+                    const int c0 = J * SUB + gid, c1 = c0 + 8;
+                    const uint32_t a0 = tf32_bits(dM[i0 * PC + c0]), a1 = tf32_bits(dM[i0 * PC + c1]);
+                    const uint32_t a2 = tf32_bits(dM[i1 * PC + c0]), a3 = tf32_bits(dM[i1 * PC + c1]);
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        const int c = ch * 64 + nt * 8 + gid;
+                        const float fc = f[c];
+                        mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(base[i0 * PS + c] * fc),
+                                        tf32_bits(base[i1 * PS + c] * fc));
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = J * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+                adk[nt][e] += s.ep[row * PS + col] * acc[nt][e];
+                adg[nt][e] -= __uint_as_float(tf32_bits(s.kp[row * PS + col])) * acc[nt][e];
+            }
+    }
+    // (c) elementwise terms of Q^*Gamma, K^*Gamma, Kbar
+    const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB);
+    const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB);
+    const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT);
+    float pk[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int row = rb * SUB + gid + hh * 8, col = ch * 64 + nt * 8 + tig * 2;
+            const float2 dQ2 = *reinterpret_cast<const float2*>(gdQ + row * D + col);
+            const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
+            const float2 dKt2 = *reinterpret_cast<const float2*>(gdKt + row * D + col);
+            const float dQv[2] = {dQ2.x, dQ2.y}, dKbv[2] = {dKb2.x, dKb2.y}, dKtv[2] = {dKt2.x, dKt2.y};
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = hh * 2 + e2, cc = col + e2, I = row >> 4;
+                const float pb = s.fa.Pb[I][cc], sf = s.fa.Sf[I][cc];
+                const float gam = s.em[row * PS + cc] * pb;
+                const float qb = s.qe[row * PS + cc] * pb, kt = s.ke[row * PS + cc] * pb;
+                const float el = s.ep[row * PS + cc] * sf, kb = s.kp[row * PS + cc] * sf;
+                adq[nt][e] += dQv[e2] * gam;
+                adk[nt][e] += dKtv[e2] * gam + dKbv[e2] * el;
+                adg[nt][e] += dQv[e2] * qb + dKtv[e2] * kt;
+                pk[nt][e] = dKbv[e2] * kb;
+            }
+        }
+    __syncthreads();   // all reads of qe, ke, kp, em done
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+            s.qe[row * PS + col] = adq[nt][e];
+            s.ke[row * PS + col] = adk[nt][e];
+            s.kp[row * PS + col] = adg[nt][e];
+            s.em[row * PS + col] = pk[nt][e];
+        }
+    __syncthreads();
+
+    // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps)
+    for (int r = warp; r < L; r += 8) {
+        const int c0 = lane * 4;
+        const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+            const uint16_t* src = which == 0 ? q : k;
+            const float* dx = which == 0 ? s.qe : s.ke;
+            const float inv = which == 0 ? s.inq[r] : s.ink[r];
+            const uint2 w = *reinterpret_cast<const uint2*>(src + base);
+            const float xv[4] = {bf2f((uint16_t)(w.x & 0xffffu)) * inv, bf2f((uint16_t)(w.x >> 16)) * inv,
+                                 bf2f((uint16_t)(w.y & 0xffffu)) * inv, bf2f((uint16_t)(w.y >> 16)) * inv};
+            float dot = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) dot += xv[e] * dx[r * PS + c0 + e];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+            uint16_t out[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) out[e] = f2bf((dx[r * PS + c0 + e] - xv[e] * dot) * inv);
+            uint16_t* dst = which == 0 ? dq : dk;
+            *reinterpret_cast<uint2*>(dst + base) =
+                make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 16), (uint32_t)out[2] | ((uint32_t)out[3] << 16));
+        }
+    }
+    // dg: reverse cumulative sum over rows, gate chain, parameter partials (thread per key channel)
+    float* part = reinterpret_cast<float*>(ws + lay.part) + tile * (D + 4);
+    if (tid < D) {
+        const int c = tid;
+        float run = 0.0f;
+        for (int r = 0; r < L; ++r) {      // exclusive prefix of dKbar*Kbar
+            const float p = s.em[r * PS + c];
+            s.em[r * PS + c] = run;
+            run += p;
+        }
+        const float dgam = reinterpret_cast<const float*>(bg + BgOff::DGAM)[c] * s.fa.gl[c];
+        const float dtc = dt_bias[h * D + c];
+        float rev = 0.0f, ddt = 0.0f, dA = 0.0f;
+        for (int r = L - 1; r >= 0; --r) {
+            rev += s.kp[r * PS + c];
+            const float dgt = rev + s.em[r * PS + c] + dgam;
+            const float x = bf2f(g_raw[((size_t)(t0 + r) * H + h) * D + c]) + dtc;
+            const float sg = sigmoidf(a_h * x);
+            const float du = dgt * lb * sg * (1.0f - sg);
+            const float dgr = du * a_h;
+            dg_raw[((size_t)(t0 + r) * H + h) * D + c] = f2bf(dgr);
+            ddt += dgr;
+            dA += dgr * x;
+        }
+        part[c] = ddt;
+        s.red[c] = dA;
+    }
+    if (tid < L) {
+        const float b = s.beta[tid];
+        const float db = reinterpret_cast<const float*>(wy + WyOff::DBETA)[tid];
+        dbeta_raw[(size_t)(t0 + tid) * H + h] = f2bf(db * b * (1.0f - b));
+    }
+    __syncthreads();
+    for (int off = D / 2; off > 0; off >>= 1) {
+        if (tid < off) s.red[tid] += s.red[tid + off];
+        __syncthreads();
+    }
+    if (tid == 0) part[D] = s.red[0];
+}
+
+// Deterministic sum of the per-chunk parameter partials, chunk order, per head.
+__global__ void __launch_bounds__(128)
+    kda_param_reduce_kernel(int H, float* __restrict__ dA_log, float* __restrict__ ddt_bias,
+                            uint8_t* __restrict__ ws, Layout lay) {
+    const int h = blockIdx.x, c = threadIdx.x;
+    if (read_status(ws) != 0) return;
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const float* part = reinterpret_cast<const float*>(ws + lay.part);
+    float acc = 0.0f, accA = 0.0f;
+    for (int64_t ch = 0; ch < lay.nc_max; ++ch) {
+        if (chunks[ch].L <= 0) continue;
+        const float* p = part + ((size_t)ch * H + h) * (D + 4);
+        acc += p[c];
+        if (c == 0) accA += p[D];
+    }
+    ddt_bias[h * D + c] = acc;
+    if (c == 0) dA_log[h] = accA;
+}
+
+}  // namespace kda

@@ -1,0 +1,188 @@
+// Backward state scan: one CTA per (sequence, head), chunks in reverse order.
+// The fp32 state adjoint dS (V x K) lives in tensor memory. Per chunk, given
+// dS_L (adjoint of the chunk's final state):
+//   dUt^T = scale dO^T Aqk + dS_L (K^*e^{G_L-G})^T             (tcgen05, M=128 N=64)
+//   dS_0  = dS_L diag(exp(G_L)) + scale dO^T (Q^*Gamma) - dUt^T W
+// which is the reverse mode of the chunk form
+//   Ut = U - W S0^T,  O = scale[(Q^*Gamma) S0^T + Aqk Ut],
+//   S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
+// dS_L of every chunk (tf32, as the MMAs use it) and dUt are stored in the
+// workspace for the per-chunk backward kernels; dh0 = dS at the sequence start.
+#include "kda_internal.cuh"
+#include "umma.cuh"
+
+namespace kda {
+
+namespace {
+struct BScanSmem {
+    uint8_t DS[kTileDD];     // dS_L operand [128 v][128 k]
+    uint8_t WT[kTileCK];     // W^T    [128 k][64 c]   \ bulk group Y
+    uint8_t QBT[kTileCK];    // QB^T   [128 k][64 i]   /
+    uint8_t KB[kTileCK];     // KB     [64 c][128 k]   \ bulk group X
+    uint8_t AQKT[kTileCC];   // Aqk^T  [64 j][64 i]    /
+    uint8_t DOT[kTileCK];    // scale*dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
+    float gam[D];
+    uint64_t barX, barY, barM1, barM2;
+    uint32_t tmem;
+};
+}  // namespace
+
+size_t bwd_scan_smem_bytes() { return sizeof(BScanSmem) + 1024; }
+
+__global__ void __launch_bounds__(128, 1)
+    kda_bwd_scan_kernel(const uint16_t* __restrict__ dO, const float* __restrict__ dhT, float* __restrict__ dh0,
+                        int H, float scale, uint8_t* __restrict__ ws, Layout lay) {
+    extern __shared__ uint8_t smem_raw[];
+    BScanSmem& s = *reinterpret_cast<BScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (read_status(ws) != 0) return;
+    const int h = blockIdx.x;
+    const int n = reinterpret_cast<const int*>(ws + lay.seq_order)[blockIdx.y];
+    const int cf = reinterpret_cast<const int*>(ws + lay.seq_first)[n];
+    const int cl = reinterpret_cast<const int*>(ws + lay.seq_first)[n + 1];
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int v = tid;
+    const size_t sidx = ((size_t)n * H + h) * D * D;
+
+    if (warp == 0) {
+        tmem_alloc(&s.tmem, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&s.barX, 1); mbar_init(&s.barY, 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s.tmem;
+    const uint32_t tS = tm, tU = tm + 128;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    for (int c0 = 0; c0 < D; c0 += 32) {
+        float r[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = dhT ? dhT[sidx + (size_t)v * D + c0 + j] : 0.0f;
+        tmem_st32(tS + lane_base + c0, r);
+    }
+
+    auto img_of = [&](int chunk) { return ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES; };
+    auto issue_X = [&](int chunk) {
+        mbar_arrive_expect_tx(&s.barX, (uint32_t)(kTileCK + kTileCC));
+        bulk_g2s(s.KB, img_of(chunk) + ImgOff::KB, (uint32_t)(kTileCK + kTileCC), &s.barX);
+    };
+    auto issue_Y = [&](int chunk) {
+        mbar_arrive_expect_tx(&s.barY, (uint32_t)(2 * kTileCK));
+        bulk_g2s(s.WT, img_of(chunk) + ImgOff::WT, (uint32_t)(2 * kTileCK), &s.barY);
+    };
+    int x_issued = 0, y_issued = 0, x_done = 0, y_done = 0;
+    if (tid == 0 && cf < cl) { issue_X(cl - 1); issue_Y(cl - 1); x_issued = y_issued = 1; }
+
+    bool ok = true;
+    const uint32_t idN64 = idesc_tf32(128, 64, 0, 0);
+    const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
+    for (int chunk = cl - 1; chunk >= cf && ok; --chunk) {
+        const uint32_t par = (uint32_t)((cl - 1 - chunk) & 1);
+        const ChunkInfo ci = chunks[chunk];
+        const size_t tile = (size_t)chunk * H + h;
+        s.gam[v] = reinterpret_cast<const float*>(img_of(chunk) + ImgOff::GAML)[v];
+        // scale * dO^T into the operand tile (row v, columns i)
+        float dov[C];
+#pragma unroll
+        for (int i = 0; i < C; ++i)
+            dov[i] = i < ci.L ? tf32_round(scale * bf2f(dO[((size_t)(ci.t0 + i) * H + h) * D + v])) : 0.0f;
+        if (tid == 0) bulk_wait_read_all();   // previous dS checkpoint copy done reading DS
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < C; i += 4)
+            *reinterpret_cast<float4*>(s.DOT + panel_off(v, i, D)) = make_float4(dov[i], dov[i + 1], dov[i + 2], dov[i + 3]);
+        // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float r[32];
+            tmem_ld32(tS + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) =
+                    make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]), tf32_round(r[j + 3]));
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
+            tmem_st32(tS + lane_base + c0, r);
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            bulk_s2g(ws + lay.ds + tile * kTileDD, s.DS, (uint32_t)kTileDD);
+            bulk_commit();
+            const bool gx = mbar_wait(&s.barX, par), gy = gx && mbar_wait(&s.barY, par);
+            x_done += gx; y_done += gy;
+            if (!gx || !gy) ok = false;
+            if (ok) {
+                const uint32_t aD = smem_u32(s.DOT), aS = smem_u32(s.DS);
+                // dUt^T = (scale dO^T) Aqk + dS_L KB^T
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32(tU, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.AQKT), C, ks), idN64, ks > 0);
+                for (int ks = 0; ks < D / 8; ++ks)
+                    umma_tf32(tU, desc_kmajor(aS, D, ks), desc_kmajor(smem_u32(s.KB), C, ks), idN64, 1);
+                // dS += (scale dO^T) QB
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32(tS, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.QBT), D, ks), idN128, 1);
+                umma_commit(&s.barM1);
+            }
+        }
+        ok = mbar_wait(&s.barM1, par) && ok;
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && chunk - 1 >= cf) { issue_X(chunk - 1); ++x_issued; }
+
+        // -dUt^T into the operand tile (reusing DOT); dUt -> workspace [c][v] panels
+        uint8_t* gdU = ws + lay.dut + tile * kTileCK;
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            float r[32];
+            tmem_ld32(tU + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = tf32_round(r[j]);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(s.DOT + panel_off(v, c0 + j, D)) =
+                    make_float4(-r[j], -r[j + 1], -r[j + 2], -r[j + 3]);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(c0 + j, v, C)) = r[j];
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        if (tid == 0) {
+            for (int ks = 0; ks < C / 8; ++ks)
+                umma_tf32(tS, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.WT), D, ks), idN128, 1);
+            umma_commit(&s.barM2);
+        }
+        ok = mbar_wait(&s.barM2, par) && ok;
+        ok = __syncthreads_and(ok);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && chunk - 1 >= cf) { issue_Y(chunk - 1); ++y_issued; }
+    }
+    if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
+    if (ok && dh0) {
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float r[32];
+            tmem_ld32(tS + lane_base + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dh0[sidx + (size_t)v * D + c0 + j] = r[j];
+        }
+    }
+    if (tid == 0) {
+        for (; x_done < x_issued; ++x_done) mbar_wait(&s.barX, (uint32_t)(x_done & 1));
+        for (; y_done < y_issued; ++y_done) mbar_wait(&s.barY, (uint32_t)(y_done & 1));
+        bulk_wait_all();
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 256);
+}
+
+}  // namespace kda

@@ -1,0 +1,161 @@
+// Backward, state-side products of each chunk: one CTA per (chunk, head), all
+// chunks in parallel. From the checkpoints S0 (forward) and dS_L (backward
+// scan), and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over
+// the key channel k):
+//   dQbar = scale dO S0            [c][k]
+//   dW    = -dUt S0                [c][k]
+//   dKbar = Ut dS_L                [c][k]
+//   dAqk  = scale dO Ut^T          [i][j], kept for j <= i
+//   dgam  = sum_v dS_L[v,k] S0[v,k]  (adjoint of exp(G_L) through the decayed state,
+//                                    before the factor exp(G_L))
+// These are the reverse mode of Ut = U - W S0^T, O = scale[(Q^*Gamma) S0^T + Aqk Ut],
+// S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
+#include "kda_internal.cuh"
+#include "umma.cuh"
+
+namespace kda {
+
+namespace {
+struct BStateSmem {
+    uint8_t S0T[kTileDD];    // S0^T   [128 k][128 v]
+    uint8_t DST[kTileDD];    // dS_L^T [128 k][128 v]
+    uint8_t STK[kTileDD];    // rows 0..63: scale*dO [c][v]; rows 64..127: dUt [c][v]
+    uint8_t UT[kTileCK];     // Ut [64 c][128 v]
+    uint64_t bar, barM;
+    uint32_t tmem;
+};
+}  // namespace
+
+size_t bwd_state_smem_bytes() { return sizeof(BStateSmem) + 1024; }
+
+__global__ void __launch_bounds__(128, 1)
+    kda_bwd_state_kernel(const uint16_t* __restrict__ dO, int H, float scale, uint8_t* __restrict__ ws, Layout lay) {
+    extern __shared__ uint8_t smem_raw[];
+    BStateSmem& s = *reinterpret_cast<BStateSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    if (read_status(ws) != 0) return;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
+    if (ci.L <= 0) return;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const size_t tile = (size_t)chunk * H + h;
+    const uint8_t* gS0 = ws + lay.s0 + tile * kTileDD;
+    const uint8_t* gDS = ws + lay.ds + tile * kTileDD;
+    const uint8_t* gUt = ws + lay.ut + tile * kTileCK;
+    const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
+
+    if (warp == 0) {
+        tmem_alloc(&s.tmem, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&s.bar, 1); mbar_init(&s.barM, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    // bulk loads: Ut [64][128] (R = 64) and dUt into rows 64..127 of the stack (R = 128), panel by panel
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s.bar, (uint32_t)(2 * kTileCK));
+        bulk_g2s(s.UT, gUt, (uint32_t)kTileCK, &s.bar);
+        for (int p = 0; p < 4; ++p)
+            bulk_g2s(s.STK + p * (D * 128) + 64 * 128, gdU + p * (C * 128), C * 128, &s.bar);
+    }
+    // transposed checkpoints: thread v reads row v of S0 / dS_L, writes column v
+    {
+        const int v = tid;
+        for (int c0 = 0; c0 < D; c0 += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(gS0 + panel_off(v, c0, D));
+            const float4 b = *reinterpret_cast<const float4*>(gDS + panel_off(v, c0, D));
+            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 0, v, D)) = a.x;
+            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 1, v, D)) = a.y;
+            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 2, v, D)) = a.z;
+            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 3, v, D)) = a.w;
+            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 0, v, D)) = b.x;
+            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 1, v, D)) = b.y;
+            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 2, v, D)) = b.z;
+            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 3, v, D)) = b.w;
+        }
+        // scale * dO rows 0..63 of the stack
+        for (int c = 0; c < C; ++c) {
+            const float x = c < ci.L ? tf32_round(scale * bf2f(dO[((size_t)(ci.t0 + c) * H + h) * D + v])) : 0.0f;
+            *reinterpret_cast<float*>(s.STK + panel_off(c, v, D)) = x;
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = s.tmem;
+    bool ok = true;
+    if (tid == 0) {
+        ok = mbar_wait(&s.bar, 0);
+        if (ok) {
+            const uint32_t aS = smem_u32(s.S0T), aD = smem_u32(s.DST), aK = smem_u32(s.STK), bU = smem_u32(s.UT);
+            const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
+            // [dQbar | dUt S0]^T = S0^T [scale dO ; dUt]^T     -> cols 0..127
+            for (int ks = 0; ks < D / 8; ++ks)
+                umma_tf32(tm + 0, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, ks > 0);
+            // dKbar^T = dS_L^T Ut^T                            -> cols 128..191
+            for (int ks = 0; ks < D / 8; ++ks)
+                umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
+            // dS_L^T S0 (diagonal used)                         -> cols 256..383
+            for (int ks = 0; ks < D / 8; ++ks)
+                umma_tf32(tm + 256, desc_kmajor(aD, D, ks), desc_kmajor(aS, D, ks), id128, ks > 0);
+            // [scale dO ; dUt] Ut^T (rows 0..63 used)          -> cols 384..447
+            for (int ks = 0; ks < D / 8; ++ks)
+                umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
+            umma_commit(&s.barM);
+        }
+    }
+    ok = mbar_wait(&s.barM, 0) && ok;
+    ok = __syncthreads_and(ok);
+    tc_fence_after();
+    if (ok) {
+        const int kq = tid;   // lane = key channel k (or row i for dAqk)
+        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+        uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
+        float* gdQ = reinterpret_cast<float*>(bg + BgOff::DQB);
+        float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
+        float* gdK = reinterpret_cast<float*>(bg + BgOff::DKB);
+        float* gdA = reinterpret_cast<float*>(bg + BgOff::DAQK);
+        float* gdG = reinterpret_cast<float*>(bg + BgOff::DGAM);
+        for (int c0 = 0; c0 < C; c0 += 32) {
+            float r[32];
+            tmem_ld32(tm + lb + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gdQ[(c0 + j) * D + kq] = r[j];
+            tmem_ld32(tm + lb + 64 + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gdW[(c0 + j) * D + kq] = -r[j];
+            tmem_ld32(tm + lb + 128 + c0, r);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) gdK[(c0 + j) * D + kq] = r[j];
+        }
+        {
+            float r[32];
+            tmem_ld32(tm + lb + 256 + warp * 32, r);
+            float dg = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) dg = (j == (tid & 31)) ? r[j] : dg;
+            gdG[kq] = dg;
+        }
+        if (warp < 2) {
+            const int i = tid;
+            for (int c0 = 0; c0 < C; c0 += 32) {
+                float r[32];
+                tmem_ld32(tm + lb + 384 + c0, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? r[j] : 0.0f;
+            }
+        } else {
+            // warps 2, 3 must still take part in the .sync.aligned loads of their own lanes? No:
+            // tcgen05.ld is per warp; warps 2, 3 simply skip the dAqk rows (lanes 64..127 unused).
+        }
+    } else {
+        raise_status(ws, KDA_ERR_TIMEOUT);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tm, 512);
+}
+
+}  // namespace kda

@@ -1,0 +1,218 @@
+// Backward through the UT transform of each chunk: one CTA per (chunk, head),
+// all chunks in parallel. With W = T (K^*Gamma), U = T V, T = X diag(beta),
+// X = (I + A)^{-1}, A = diag(beta) B, and the adjoints dW (state-products
+// kernel) and dU = dUt (backward scan):
+//   dT    = dW (K^*Gamma)^T + dU V^T
+//   dKt   = T^T dW        (adjoint of K^*Gamma)
+//   dV    = T^T dU        (final dv)
+//   dbeta_j  = sum_i dT_ij X_ij + sum_l dA_jl B_jl
+//   dA    = -strict_lower(X^T dT T^T),   dB = diag(beta) dA
+// tf32 mma.sync on 16-row tiles; dKt, dB and dbeta go to the workspace.
+#include "kda_internal.cuh"
+#include "kda_prep.cuh"
+#include "mma_sync.cuh"
+#include "umma.cuh"
+
+namespace kda {
+
+namespace {
+struct WySmem {
+    float kt[C * PS];    // k^, then K^*Gamma
+    float v[C * PS];
+    float dW[C * PS];    // dW, then M = dT T^T (stride PC)
+    float dU[C * PS];    // alpha scratch, then dU
+    float X[C * PC];
+    float B[C * PC];
+    float T[C * PC];
+    float dT[C * PC];    // dT, then dA
+    Factors fa;
+    float beta[C];
+    float dbeta[C];
+};
+}  // namespace
+
+size_t bwd_wy_smem_bytes() { return sizeof(WySmem); }
+
+__global__ void __launch_bounds__(256, 1)
+    kda_bwd_wy_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                      const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
+                      const float* __restrict__ A_log, const float* __restrict__ dt_bias, int H, float lb,
+                      uint16_t* __restrict__ dv, uint8_t* __restrict__ ws, Layout lay) {
+    extern __shared__ uint8_t smem_raw[];
+    WySmem& s = *reinterpret_cast<WySmem*>(smem_raw);
+    if (read_status(ws) != 0) return;
+    const int chunk = blockIdx.x, h = blockIdx.y;
+    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
+    if (ci.L <= 0) return;
+    const int L = ci.L;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gid = lane >> 2, tig = lane & 3;
+    const size_t tile = (size_t)chunk * H + h;
+    const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
+    const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
+    const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
+    uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
+    const float a_h = __expf(A_log[h]);
+
+    prep_rows(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dU, s.beta,
+              nullptr, nullptr);
+    __syncthreads();
+    block_products(s.dU, nullptr, s.kt, nullptr, nullptr, &s.fa);
+    __syncthreads();
+    block_factors(&s.fa);
+    __syncthreads();
+    for (int idx = tid; idx < C * D; idx += blockDim.x) {
+        const int r = idx >> 7, c = idx & 127;
+        s.kt[r * PS + c] *= s.fa.Pb[r >> 4][c];
+        s.dW[r * PS + c] = reinterpret_cast<const float*>(bg + BgOff::DW)[idx];
+        s.dU[r * PS + c] = *reinterpret_cast<const float*>(gdU + panel_off(r, c, C));
+    }
+    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+        const int r = idx >> 6, c = idx & 63;
+        const float x = reinterpret_cast<const float*>(img + ImgOff::XM)[idx];
+        s.X[r * PC + c] = x;
+        s.B[r * PC + c] = reinterpret_cast<const float*>(img + ImgOff::BM)[idx];
+        s.T[r * PC + c] = x * s.beta[c];
+    }
+    __syncthreads();
+
+    // dT = dW Kt^T + dU V^T   (rows 16rb, columns 32ch: 4 n-tiles)
+    {
+        const int rb = warp & 3, ch = warp >> 2;
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const int r0 = rb * SUB + gid, r1 = r0 + 8;
+        for (int ks = 0; ks < D / 8; ++ks) {
+            const int k0 = ks * 8 + tig, k1 = k0 + 4;
+            const uint32_t w0 = tf32_bits(s.dW[r0 * PS + k0]), w1 = tf32_bits(s.dW[r1 * PS + k0]);
+            const uint32_t w2 = tf32_bits(s.dW[r0 * PS + k1]), w3 = tf32_bits(s.dW[r1 * PS + k1]);
+            const uint32_t u0 = tf32_bits(s.dU[r0 * PS + k0]), u1 = tf32_bits(s.dU[r1 * PS + k0]);
+            const uint32_t u2 = tf32_bits(s.dU[r0 * PS + k1]), u3 = tf32_bits(s.dU[r1 * PS + k1]);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int j = ch * 32 + nt * 8 + gid;
+                mma_tf32_16x8x8(acc[nt], w0, w1, w2, w3, tf32_bits(s.kt[j * PS + k0]), tf32_bits(s.kt[j * PS + k1]));
+                mma_tf32_16x8x8(acc[nt], u0, u1, u2, u3, tf32_bits(s.v[j * PS + k0]), tf32_bits(s.v[j * PS + k1]));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                s.dT[row * PC + col] = acc[nt][e];
+            }
+    }
+    // dKt = T^T dW, dV = T^T dU   (rows j in 16jb, columns 64ch: 8 n-tiles); T[i][j] = 0 for i < j
+    {
+        const int jb = warp & 3, ch = warp >> 2;
+        float ak[8][4], av[8][4];
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) { ak[nt][e] = 0.0f; av[nt][e] = 0.0f; }
+        const int j0 = jb * SUB + gid, j1 = j0 + 8;
+        for (int ks = 2 * jb; ks < C / 8; ++ks) {
+            const int i0 = ks * 8 + tig, i1 = i0 + 4;
+            const uint32_t a0 = tf32_bits(s.T[i0 * PC + j0]), a1 = tf32_bits(s.T[i0 * PC + j1]);
+            const uint32_t a2 = tf32_bits(s.T[i1 * PC + j0]), a3 = tf32_bits(s.T[i1 * PC + j1]);
+#pragma unroll
+            for (int nt = 0; nt < 8; ++nt) {
+                const int c = ch * 64 + nt * 8 + gid;
+                mma_tf32_16x8x8(ak[nt], a0, a1, a2, a3, tf32_bits(s.dW[i0 * PS + c]), tf32_bits(s.dW[i1 * PS + c]));
+                mma_tf32_16x8x8(av[nt], a0, a1, a2, a3, tf32_bits(s.dU[i0 * PS + c]), tf32_bits(s.dU[i1 * PS + c]));
+            }
+        }
+        float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = jb * SUB + gid + hh * 8, col = ch * 64 + nt * 8 + tig * 2;
+                *reinterpret_cast<float2*>(gdK + row * D + col) = make_float2(ak[nt][hh * 2], ak[nt][hh * 2 + 1]);
+                if (row < L) {
+                    const uint32_t pk = (uint32_t)f2bf(av[nt][hh * 2]) | ((uint32_t)f2bf(av[nt][hh * 2 + 1]) << 16);
+                    *reinterpret_cast<uint32_t*>(dv + ((size_t)(ci.t0 + row) * H + h) * D + col) = pk;
+                }
+            }
+    }
+    __syncthreads();
+    // dbeta from T = X diag(beta); M = dT T^T into the dW buffer
+    if (tid < C) {
+        float acc = 0.0f;
+        for (int i = tid; i < C; ++i) acc += s.dT[i * PC + tid] * s.X[i * PC + tid];
+        s.dbeta[tid] = acc;
+    }
+    float* M = s.dW;
+    {
+        const int rb = warp & 3, ch = warp >> 2;
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const int r0 = rb * SUB + gid, r1 = r0 + 8;
+        for (int ks = 0; ks < C / 8; ++ks) {
+            const int m0 = ks * 8 + tig, m1 = m0 + 4;
+            const uint32_t a0 = tf32_bits(s.dT[r0 * PC + m0]), a1 = tf32_bits(s.dT[r1 * PC + m0]);
+            const uint32_t a2 = tf32_bits(s.dT[r0 * PC + m1]), a3 = tf32_bits(s.dT[r1 * PC + m1]);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int j = ch * 32 + nt * 8 + gid;
+                mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(s.T[j * PC + m0]), tf32_bits(s.T[j * PC + m1]));
+            }
+        }
+        __syncthreads();   // everyone is done reading dW before M overwrites it
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                M[row * PC + col] = acc[nt][e];
+            }
+    }
+    __syncthreads();
+    // dA = -strict_lower(X^T M) into the dT buffer; X[m][i] = 0 for m < i
+    {
+        const int ib = warp & 3, ch = warp >> 2;
+        float acc[4][4];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+        const int i0 = ib * SUB + gid, i1 = i0 + 8;
+        for (int ks = 2 * ib; ks < C / 8; ++ks) {
+            const int m0 = ks * 8 + tig, m1 = m0 + 4;
+            const uint32_t a0 = tf32_bits(s.X[m0 * PC + i0]), a1 = tf32_bits(s.X[m0 * PC + i1]);
+            const uint32_t a2 = tf32_bits(s.X[m1 * PC + i0]), a3 = tf32_bits(s.X[m1 * PC + i1]);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const int j = ch * 32 + nt * 8 + gid;
+                mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(M[m0 * PC + j]), tf32_bits(M[m1 * PC + j]));
+            }
+        }
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int row = ib * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                s.dT[row * PC + col] = col < row ? -acc[nt][e] : 0.0f;
+            }
+    }
+    __syncthreads();
+    float* gdB = reinterpret_cast<float*>(wy + WyOff::DB);
+    for (int idx = tid; idx < C * C; idx += blockDim.x) {
+        const int r = idx >> 6, c = idx & 63;
+        gdB[idx] = s.beta[r] * s.dT[r * PC + c];
+    }
+    if (tid < C) {
+        float acc = s.dbeta[tid];
+        for (int j = 0; j < tid; ++j) acc += s.dT[tid * PC + j] * s.B[tid * PC + j];
+        reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] = acc;
+    }
+}
+
+}  // namespace kda

@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(128, 1)
 extern "C" int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, const float* B,
                                       float* D, void* stream) {
     if (N < 16 || N > 256 || (N % 16) || Kd < 8 || Kd > 128 || (Kd % 32)) return KDA_ERR_SHAPE;
+    if (a_mn || b_mn) return KDA_ERR_UNSUPPORTED;   // kind::tf32 takes K-major operands only
     if (!A || !B || !D) return KDA_ERR_NULL;
     const size_t smem = (size_t)(128 + N) * Kd * 4 + 1024;
     cudaError_t e = cudaFuncSetAttribute(kda::umma_selftest_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

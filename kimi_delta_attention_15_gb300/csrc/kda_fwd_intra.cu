@@ -17,28 +17,25 @@
 #include "kda_internal.cuh"
 #include "mma_sync.cuh"
 #include "umma.cuh"
+#include "kda_prep.cuh"
 
 namespace kda {
 
 namespace {
 
-constexpr int P = 132;   // padded row stride (floats) of [64][128] tiles
-constexpr int PA = 68;   // padded row stride of [64][64] tiles
+constexpr int P = PS;
+constexpr int PA = PC;
 
 struct IntraSmem {
-    float qe[C * P];      // q^ * E-   (E- = decay from the row's block start, inclusive)
+    float qe[C * P];      // q^ * E-
     float ke[C * P];      // k^ * E-
-    float kp[C * P];      // k^ * E+   (E+ = decay to the row's block end, exclusive)
+    float kp[C * P];      // alpha, then k^ * E+
     float v[C * P];
-    float A[C * PA];      // beta-scaled strictly lower A, then scratch
+    float A[C * PA];      // beta-scaled strictly lower A
     float Aqk[C * PA];
     float X[C * PA];      // (I + A)^{-1}
     float T[C * PA];      // X diag(beta)
-    float F[NSUB][NSUB][D];  // row factors f_IJ (I >= J)
-    float Pb[NSUB][D];    // decay from chunk start to the start of block I
-    float Sf[NSUB][D];    // decay from the end of block I to the chunk end
-    float Db[NSUB][D];    // decay across block I
-    float gl[D];          // exp(G_L)
+    Factors fa;
     float beta[C];
 };
 
@@ -60,70 +57,13 @@ __global__ void __launch_bounds__(256, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const float a_h = __expf(A_log[h]);
+    const size_t tile = (size_t)chunk * H + h;
+    uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
 
-    // ---- load rows, L2 norms, gate, beta
-    for (int r = warp; r < C; r += 8) {
-        float qv[4] = {0, 0, 0, 0}, kv[4] = {0, 0, 0, 0}, vv[4] = {0, 0, 0, 0}, al[4] = {1, 1, 1, 1};
-        const int c0 = lane * 4;
-        if (r < L) {
-            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-            const uint2 q2 = *reinterpret_cast<const uint2*>(q + base);
-            const uint2 k2 = *reinterpret_cast<const uint2*>(k + base);
-            const uint2 v2 = *reinterpret_cast<const uint2*>(v + base);
-            const uint2 g2 = *reinterpret_cast<const uint2*>(g_raw + base);
-            const uint32_t qw[2] = {q2.x, q2.y}, kw[2] = {k2.x, k2.y}, vw[2] = {v2.x, v2.y}, gw[2] = {g2.x, g2.y};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int sh = (e & 1) * 16;
-                qv[e] = bf2f((uint16_t)(qw[e >> 1] >> sh));
-                kv[e] = bf2f((uint16_t)(kw[e >> 1] >> sh));
-                vv[e] = bf2f((uint16_t)(vw[e >> 1] >> sh));
-                const float gr = bf2f((uint16_t)(gw[e >> 1] >> sh));
-                const float z = a_h * (gr + dt_bias[h * D + c0 + e]);
-                al[e] = __expf(lb * sigmoidf(z));
-            }
-        }
-        float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-        float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        const float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            s.qe[r * P + c0 + e] = qv[e] * iq;
-            s.ke[r * P + c0 + e] = kv[e] * ik;
-            s.kp[r * P + c0 + e] = al[e];
-            s.v[r * P + c0 + e] = vv[e];
-        }
-        if (lane == 0) s.beta[r] = r < L ? sigmoidf(bf2f(beta_raw[(size_t)(t0 + r) * H + h])) : 0.0f;
-    }
+    prep_rows(q, k, v, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, s.v, s.kp, s.beta, nullptr,
+              nullptr);
     __syncthreads();
-
-    // ---- decays inside each 16-row block, per key channel
-    for (int task = tid; task < NSUB * D; task += blockDim.x) {
-        const int c = task & (D - 1), I = task >> 7;
-        float al[SUB], em[SUB], ep[SUB];
-#pragma unroll
-        for (int i = 0; i < SUB; ++i) al[i] = s.kp[(I * SUB + i) * P + c];
-        float pre = 1.0f;
-#pragma unroll
-        for (int i = 0; i < SUB; ++i) { pre *= al[i]; em[i] = pre; }
-        float suf = 1.0f;
-#pragma unroll
-        for (int i = SUB - 1; i >= 0; --i) { ep[i] = suf; suf *= al[i]; }
-        s.Db[I][c] = pre;
-#pragma unroll
-        for (int i = 0; i < SUB; ++i) {
-            const int r = I * SUB + i;
-            const float kh = s.ke[r * P + c], qh = s.qe[r * P + c];
-            s.ke[r * P + c] = kh * em[i];
-            s.qe[r * P + c] = qh * em[i];
-            s.kp[r * P + c] = kh * ep[i];
-        }
-    }
+    block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);
     // zero the blocks above the diagonal of A, Aqk, X
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int r = idx >> 6, cc = idx & 63;
@@ -134,26 +74,16 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     __syncthreads();
-    if (tid < D) {
-        const int c = tid;
-        const float d0 = s.Db[0][c], d1 = s.Db[1][c], d2 = s.Db[2][c], d3 = s.Db[3][c];
-        s.Pb[0][c] = 1.0f; s.Pb[1][c] = d0; s.Pb[2][c] = d0 * d1; s.Pb[3][c] = d0 * d1 * d2;
-        s.gl[c] = d0 * d1 * d2 * d3;
-        s.Sf[3][c] = 1.0f; s.Sf[2][c] = d3; s.Sf[1][c] = d2 * d3; s.Sf[0][c] = d1 * d2 * d3;
-        s.F[0][0][c] = 1.0f / d0; s.F[1][1][c] = 1.0f / d1; s.F[2][2][c] = 1.0f / d2; s.F[3][3][c] = 1.0f / d3;
-        s.F[1][0][c] = 1.0f; s.F[2][1][c] = 1.0f; s.F[3][2][c] = 1.0f;
-        s.F[2][0][c] = d1; s.F[3][1][c] = d2; s.F[3][0][c] = d1 * d2;
-    }
+    block_factors(&s.fa);
     __syncthreads();
 
     // ---- pairwise decayed products, 16x16 blocks (I >= J), tf32 mma.sync
     for (int task = warp; task < 20; task += 8) {
         const int m = task / 10;
-        int rem = task % 10, I = 0;
-        while (rem > I) { rem -= I + 1; ++I; }
-        const int J = rem;
+        int I, J;
+        tri_pair(task % 10, I, J);
         const float* base = m == 0 ? s.ke : s.qe;
-        const float* f = s.F[I][J];
+        const float* f = s.fa.F[I][J];
         float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
         const int r0 = I * SUB + gid, r1 = r0 + 8;
 #pragma unroll 4
@@ -175,8 +105,13 @@ __global__ void __launch_bounds__(256, 1)
                 const int row = I * SUB + gid + (e >> 1) * 8;
                 const int col = J * SUB + nt * 8 + tig * 2 + (e & 1);
                 const float val = acc[nt][e];
-                if (m == 0) s.A[row * PA + col] = col < row ? val * s.beta[row] : 0.0f;
-                else s.Aqk[row * PA + col] = col <= row ? val : 0.0f;
+                if (m == 0) {
+                    const float b = col < row ? val : 0.0f;
+                    s.A[row * PA + col] = b * s.beta[row];
+                    reinterpret_cast<float*>(img + ImgOff::BM)[row * C + col] = b;
+                } else {
+                    s.Aqk[row * PA + col] = col <= row ? val : 0.0f;
+                }
             }
     }
     __syncthreads();
@@ -212,16 +147,16 @@ __global__ void __launch_bounds__(256, 1)
             __syncthreads();
         }
     }
-    // T = X diag(beta)
+    // T = X diag(beta); X and the zero upper blocks of B to the workspace
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int r = idx >> 6, cc = idx & 63;
         s.T[r * PA + cc] = s.X[r * PA + cc] * s.beta[cc];
+        reinterpret_cast<float*>(img + ImgOff::XM)[idx] = s.X[r * PA + cc];
+        if ((cc >> 4) > (r >> 4)) reinterpret_cast<float*>(img + ImgOff::BM)[idx] = 0.0f;
     }
     __syncthreads();
 
     // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 64ch..)
-    const size_t tile = (size_t)chunk * H + h;
-    uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
     {
         const int rb = warp & 3, ch = warp >> 2;
         float aw[8][4], au[8][4];
@@ -234,7 +169,7 @@ __global__ void __launch_bounds__(256, 1)
             const int j0 = ks * 8 + tig, j1 = j0 + 4;
             const uint32_t a0 = tf32_bits(s.T[ra * PA + j0]), a1 = tf32_bits(s.T[rbb * PA + j0]);
             const uint32_t a2 = tf32_bits(s.T[ra * PA + j1]), a3 = tf32_bits(s.T[rbb * PA + j1]);
-            const float* pb = s.Pb[j0 >> 4];
+            const float* pb = s.fa.Pb[j0 >> 4];
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int c = ch * 64 + nt * 8 + gid;
@@ -261,15 +196,15 @@ __global__ void __launch_bounds__(256, 1)
     // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G), Aqk, and their transposes
     for (int idx = tid; idx < C * D; idx += blockDim.x) {
         const int r = idx >> 7, c = idx & 127;          // [64][128] row-major walk
-        const float qb = tf32_round(s.qe[r * P + c] * s.Pb[r >> 4][c]);
-        const float kb = tf32_round(s.kp[r * P + c] * s.Sf[r >> 4][c]);
+        const float qb = tf32_round(s.qe[r * P + c] * s.fa.Pb[r >> 4][c]);
+        const float kb = tf32_round(s.kp[r * P + c] * s.fa.Sf[r >> 4][c]);
         *reinterpret_cast<float*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
         *reinterpret_cast<float*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
     }
     for (int idx = tid; idx < C * D; idx += blockDim.x) {
         const int kk = idx >> 6, c = idx & 63;           // [128][64] row-major walk
-        const float qb = tf32_round(s.qe[c * P + kk] * s.Pb[c >> 4][kk]);
-        const float kb = tf32_round(s.kp[c * P + kk] * s.Sf[c >> 4][kk]);
+        const float qb = tf32_round(s.qe[c * P + kk] * s.fa.Pb[c >> 4][kk]);
+        const float kb = tf32_round(s.kp[c * P + kk] * s.fa.Sf[c >> 4][kk]);
         *reinterpret_cast<float*>(img + ImgOff::QBT + panel_off(kk, c, D)) = qb;
         *reinterpret_cast<float*>(img + ImgOff::KBT + panel_off(kk, c, D)) = kb;
     }
@@ -278,7 +213,7 @@ __global__ void __launch_bounds__(256, 1)
         *reinterpret_cast<float*>(img + ImgOff::AQK + panel_off(r, c, C)) = tf32_round(s.Aqk[r * PA + c]);
         *reinterpret_cast<float*>(img + ImgOff::AQKT + panel_off(r, c, C)) = tf32_round(s.Aqk[c * PA + r]);
     }
-    if (tid < D) reinterpret_cast<float*>(img + ImgOff::GAML)[tid] = s.gl[tid];
+    if (tid < D) reinterpret_cast<float*>(img + ImgOff::GAML)[tid] = s.fa.gl[tid];
 }
 
 size_t fwd_intra_smem_bytes() { return sizeof(IntraSmem); }

@@ -35,6 +35,9 @@ constexpr size_t kTileDD = (size_t)D * D * 4;     // [128][128] fp32
 //     QBT  [128][64]  panels R=128   (Q^ * Gamma)^T
 //     KB   [64][128]  panels R=64    K^ * exp(G_L - G)
 //     AQKT [64][64]   panels R=64    Aqk^T
+//   read by the backward chunk kernels:
+//     XM   [64][64]   row-major fp32 X = (I + A)^{-1}
+//     BM   [64][64]   row-major fp32 B_ij = sum_c k^_ic k^_jc e^{G_ic - G_jc} (j < i), A = diag(beta) B
 struct ImgOff {
     static constexpr size_t W = 0;
     static constexpr size_t QB = W + kTileCK;
@@ -48,7 +51,9 @@ struct ImgOff {
     static constexpr size_t KB = QBT + kTileCK;
     static constexpr size_t AQKT = KB + kTileCK;
     static constexpr size_t BWD_BULK = AQKT + kTileCC - WT;  // bytes bulk-loaded by the backward scan
-    static constexpr size_t BYTES = AQKT + kTileCC;
+    static constexpr size_t XM = AQKT + kTileCC;
+    static constexpr size_t BM = XM + kTileCC;
+    static constexpr size_t BYTES = BM + kTileCC;
 };
 
 // Backward state-product outputs per tile (row-major fp32).
@@ -59,6 +64,14 @@ struct BgOff {
     static constexpr size_t DAQK = DKB + kTileCK;    // dAqk  [64][64] (scale included)
     static constexpr size_t DGAM = DAQK + kTileCC;   // sum_v dS_L * S0 [128]
     static constexpr size_t BYTES = ((DGAM + D * 4) + 1023) & ~size_t(1023);
+};
+
+// Backward WY-kernel outputs per tile (row-major fp32).
+struct WyOff {
+    static constexpr size_t DKT = 0;                 // d(K^ * Gamma) [64][128]
+    static constexpr size_t DB = DKT + kTileCK;      // dB = diag(beta) dA [64][64]
+    static constexpr size_t DBETA = DB + kTileCC;    // dbeta [64]
+    static constexpr size_t BYTES = ((DBETA + C * 4) + 1023) & ~size_t(1023);
 };
 
 struct ChunkInfo {
@@ -72,7 +85,7 @@ struct Layout {
     int64_t nc_max;      // chunk slots
     int64_t H;
     size_t status, chunks, seq_first, seq_order;
-    size_t img, s0, ut, ds, dut, bg, part;
+    size_t img, s0, ut, ds, dut, bg, wy, part;
     size_t total;
 };
 
@@ -98,6 +111,7 @@ __host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, i
     l.ds = o;          o += (size_t)tiles * kTileDD;
     l.dut = o;         o += (size_t)tiles * kTileCK;
     l.bg = o;          o += (size_t)tiles * BgOff::BYTES;
+    l.wy = o;          o += (size_t)tiles * WyOff::BYTES;
     l.part = o;        o = align_up(o + (size_t)tiles * (D + 4) * 4, 1024);
     l.total = o;
     return l;

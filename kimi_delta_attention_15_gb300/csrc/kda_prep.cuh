@@ -1,0 +1,135 @@
+// Per-chunk preprocessing shared by the forward and backward chunk kernels,
+// so every kernel recomputes bitwise the same values:
+//   q^ = q / sqrt(|q|^2 + 1e-6), k^ likewise          (flashinfer contract)
+//   beta = sigmoid(beta_raw)
+//   alpha_c = exp(lb * sigmoid(exp(A_log) (g_raw_c + dt_bias_c)))   per key channel
+// and, per 16-row sub-block I and key channel c, products of alpha:
+//   E-_i = prod_{s_I <= j <= i} alpha_j   (decay from the block start, inclusive)
+//   E+_i = prod_{i < j <= e_I} alpha_j    (decay to the block end, exclusive)
+//   D_I  = prod over the block;  Pb_I = prod_{I' < I} D_I'  (= Gamma at the block start)
+//   Sf_I = prod_{I' > I} D_I';  gl = prod_I D_I = exp(G_L)
+//   f_IJ = prod_{J < I' < I} D_I' (I > J),  1 / D_I (I = J)
+// so that e^{G_i - G_j} = (E-_i f_IJ) (E+_j) for i in block I >= J, j in block J,
+// with both factors in [e^{-80}, e^{80}] when lb >= -5. Rows at or past the
+// chunk length L are zero with alpha = 1 (no decay) and beta = 0.
+#pragma once
+#include "kda_internal.cuh"
+
+namespace kda {
+
+constexpr int PS = 132;   // padded row stride (floats) of [64][128] smem tiles
+constexpr int PC = 68;    // padded row stride of [64][64] smem tiles
+
+struct Factors {
+    float F[NSUB][NSUB][D];
+    float Pb[NSUB][D];
+    float Sf[NSUB][D];
+    float Db[NSUB][D];
+    float gl[D];
+};
+
+// Loads rows of one chunk (warp per row, lane per 4 channels). Any output
+// pointer may be null. xq/xk receive q^, k^; xv receives v; xa receives alpha;
+// beta[r], inq[r], ink[r] receive beta and 1/sqrt(|x|^2 + eps).
+__device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
+                                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
+                                          const uint16_t* __restrict__ beta_raw, const float* __restrict__ dt_bias,
+                                          float a_h, float lb, int t0, int L, int H, int h, float* xq, float* xk,
+                                          float* xv, float* xa, float* beta, float* inq, float* ink) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+    const int c0 = lane * 4;
+    for (int r = warp; r < C; r += nw) {
+        float qv[4] = {0, 0, 0, 0}, kv[4] = {0, 0, 0, 0}, vv[4] = {0, 0, 0, 0}, al[4] = {1, 1, 1, 1};
+        if (r < L) {
+            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+            auto ld4 = [&](const uint16_t* p, float* out) {
+                const uint2 w = *reinterpret_cast<const uint2*>(p + base);
+                out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
+                out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
+            };
+            if (xq || inq) ld4(q, qv);
+            if (xk || ink) ld4(k, kv);
+            if (xv) ld4(v, vv);
+            if (xa) {
+                float gr[4];
+                ld4(g_raw, gr);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dt_bias[h * D + c0 + e])));
+            }
+        }
+        float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+        float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sq += __shfl_xor_sync(0xffffffffu, sq, o);
+            sk += __shfl_xor_sync(0xffffffffu, sk, o);
+        }
+        const float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if (xq) xq[r * PS + c0 + e] = qv[e] * iq;
+            if (xk) xk[r * PS + c0 + e] = kv[e] * ik;
+            if (xv) xv[r * PS + c0 + e] = vv[e];
+            if (xa) xa[r * PS + c0 + e] = al[e];
+        }
+        if (lane == 0) {
+            if (beta) beta[r] = r < L ? sigmoidf(bf2f(beta_raw[(size_t)(t0 + r) * H + h])) : 0.0f;
+            if (inq) inq[r] = iq;
+            if (ink) ink[r] = ik;
+        }
+    }
+}
+
+// Block products. On entry `ap` holds alpha, `xq`/`xk` hold q^/k^ (either may
+// be null). On exit: ap = k^ * E+ (needs xk), xq = q^ * E-, xk = k^ * E-;
+// em/ep (nullable) receive E-/E+; fa->Db receives D_I.
+__device__ __forceinline__ void block_products(float* ap, float* xq, float* xk, float* em_out, float* ep_out,
+                                               Factors* fa) {
+    for (int task = threadIdx.x; task < NSUB * D; task += blockDim.x) {
+        const int c = task & (D - 1), I = task >> 7;
+        float al[SUB], em[SUB], ep[SUB];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) al[i] = ap[(I * SUB + i) * PS + c];
+        float pre = 1.0f;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) { pre *= al[i]; em[i] = pre; }
+        float suf = 1.0f;
+#pragma unroll
+        for (int i = SUB - 1; i >= 0; --i) { ep[i] = suf; suf *= al[i]; }
+        fa->Db[I][c] = pre;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+            const int r = (I * SUB + i) * PS + c;
+            if (xk) {
+                const float kh = xk[r];
+                xk[r] = kh * em[i];
+                ap[r] = kh * ep[i];
+            }
+            if (xq) xq[r] = xq[r] * em[i];
+            if (em_out) em_out[r] = em[i];
+            if (ep_out) ep_out[r] = ep[i];
+        }
+    }
+}
+
+// Per-channel block factors from fa->Db (threads 0..127). Call after a barrier.
+__device__ __forceinline__ void block_factors(Factors* fa) {
+    const int c = threadIdx.x;
+    if (c >= D) return;
+    const float d0 = fa->Db[0][c], d1 = fa->Db[1][c], d2 = fa->Db[2][c], d3 = fa->Db[3][c];
+    fa->Pb[0][c] = 1.0f; fa->Pb[1][c] = d0; fa->Pb[2][c] = d0 * d1; fa->Pb[3][c] = d0 * d1 * d2;
+    fa->gl[c] = d0 * d1 * d2 * d3;
+    fa->Sf[3][c] = 1.0f; fa->Sf[2][c] = d3; fa->Sf[1][c] = d2 * d3; fa->Sf[0][c] = d1 * d2 * d3;
+    fa->F[0][0][c] = 1.0f / d0; fa->F[1][1][c] = 1.0f / d1; fa->F[2][2][c] = 1.0f / d2; fa->F[3][3][c] = 1.0f / d3;
+    fa->F[1][0][c] = 1.0f; fa->F[2][1][c] = 1.0f; fa->F[3][2][c] = 1.0f;
+    fa->F[2][0][c] = d1; fa->F[3][1][c] = d2; fa->F[3][0][c] = d1 * d2;
+}
+
+// Decode the t-th lower-triangular block pair (I >= J) of the 4x4 sub-block grid.
+__device__ __forceinline__ void tri_pair(int t, int& I, int& J) {
+    I = 0;
+    while (t > I) { t -= I + 1; ++I; }
+    J = t;
+}
+
+}  // namespace kda

@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True):
         lib.kda_get_device_status.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_set_profile_events.argtypes = [P, ctypes.c_int]
+        lib.kda_set_profile_events.restype = ctypes.c_int
         lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
         lib.kda_diag_umma_selftest.restype = ctypes.c_int
         _lib = lib
@@ -164,3 +166,28 @@ def umma_selftest(A, B, a_mn: int, b_mn: int):
     code = lib.kda_diag_umma_selftest(a_mn, b_mn, N, Kd, _ptr(A), _ptr(B), _ptr(D), _stream_handle())
     _check(code, "kda_diag_umma_selftest")
     return D
+
+
+KERNEL_SLOTS = {
+    "fwd_table": (0, 1), "fwd_intra": (1, 2), "fwd_scan": (2, 3),
+    "bwd_scan": (4, 5), "bwd_state": (5, 6), "bwd_wy": (6, 7), "bwd_pair": (7, 8), "bwd_reduce": (8, 9),
+}
+
+
+class KernelTimer:
+    """Per-kernel CUDA events recorded by the library around its launches
+    (kda_set_profile_events). Use as a context manager around one call pair."""
+
+    def __init__(self):
+        self.events = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+        self._arr = (ctypes.c_void_p * 10)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
+
+    def __enter__(self):
+        load().kda_set_profile_events(self._arr, 10)
+        return self
+
+    def __exit__(self, *exc):
+        load().kda_set_profile_events(None, 0)
+
+    def times_ms(self):
+        return {k: self.events[a].elapsed_time(self.events[b]) for k, (a, b) in KERNEL_SLOTS.items()}

@@ -1,0 +1,74 @@
+"""The C ABI library (no GPU needed): it loads, exports every function that
+include/kda.h declares, and rejects bad arguments on the host before any
+CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from kimi_delta_attention_15_gb300 import build, ops
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "kda.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ops.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert "kda_fwd" in names and "kda_bwd" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_workspace_size(lib):
+    s = ops.make_shape(8192, 96, 1)
+    n = ops.workspace_size(s)
+    assert n > 0 and n % 1024 == 0
+    bad = ops.make_shape(8192, 96, 1)
+    bad.K = 64
+    assert ops.workspace_size(bad) == 0
+    bad = ops.make_shape(100, 2, 1, lower_bound=-6.0)
+    assert ops.workspace_size(bad) == 0
+
+
+def _call_fwd(lib, shape, ptr=16, ws_bytes=1 << 40, cu=None, ws=1024):
+    p = ctypes.c_void_p(ptr)
+    return lib.kda_fwd(ctypes.byref(shape), p, p, p, p, p, p, p, None, cu, p, None, ctypes.c_void_p(ws),
+                       ws_bytes, None)
+
+
+def test_host_validation_codes(lib):
+    s = ops.make_shape(64, 2, 1)
+    assert _call_fwd(lib, s, ptr=0) == 1                     # NULL
+    assert _call_fwd(lib, s, ptr=24) == 2                    # misaligned
+    assert _call_fwd(lib, s, ws_bytes=16) == 5               # workspace too small
+    assert _call_fwd(lib, s, ws=0) == 5                      # no workspace
+    assert _call_fwd(lib, s, ws=1032) == 2                   # misaligned workspace
+    u = ops.make_shape(64, 2, 1); u.V = 256
+    assert _call_fwd(lib, u) == 4                            # unsupported V
+    u = ops.make_shape(64, 2, 1, lower_bound=0.0)
+    assert _call_fwd(lib, u) == 4                            # lb must be < 0
+    u = ops.make_shape(64, 2, 1, scale=float("nan"))
+    assert _call_fwd(lib, u) == 4
+    u = ops.make_shape(64, 0, 1)
+    assert _call_fwd(lib, u) == 3                            # H = 0
+    u = ops.make_shape(64, 2, 3)                             # packed with B = 1, N = 3 needs offsets
+    assert _call_fwd(lib, u) == 3
+    assert lib.kda_status_string(6) == b"KDA_ERR_OFFSETS"
+
+
+def test_selftest_rejects_bad_shapes(lib):
+    p = ctypes.c_void_p(16)
+    assert lib.kda_diag_umma_selftest(0, 0, 300, 64, p, p, p, None) == 3
+    assert lib.kda_diag_umma_selftest(1, 0, 64, 64, p, p, p, None) == 4
