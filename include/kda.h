@@ -127,6 +127,10 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
  * not thread-safe; pass NULL to switch it off. Returns KDA_OK. */
 int kda_set_profile_events(void* const* events, int count);
 
+/* Text of the last CUDA error an entry point of the calling thread turned
+ * into KDA_ERR_CUDA ("" if none). Static per-thread buffer. */
+const char* kda_last_error(void);
+
 /* Human-readable name of a status code (static string). */
 const char* kda_status_string(kda_status s);
 

@@ -1,6 +1,7 @@
 // C ABI entry points (include/kda.h): argument validation, workspace layout,
 // the chunk table built on the device from cu_seqlens, and kernel launches.
 #include <cmath>
+#include <cstdio>
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -13,9 +14,10 @@ size_t bwd_wy_smem_bytes();
 size_t bwd_pair_smem_bytes();
 
 __global__ void kda_fwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
-                                     const uint16_t*, const float*, const float*, int, float, uint8_t*, Layout);
+                                     const uint16_t*, const float*, const float*, int, float, float, uint8_t*,
+                                     Layout);
 __global__ void kda_fwd_scan_kernel(const float*, uint16_t*, float*, int, float, uint8_t*, Layout);
-__global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, float, uint8_t*, Layout);
+__global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, uint8_t*, Layout);
 __global__ void kda_bwd_state_kernel(const uint16_t*, int, float, uint8_t*, Layout);
 __global__ void kda_bwd_wy_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*, const float*,
                                   const float*, int, float, uint16_t*, uint8_t*, Layout);
@@ -106,6 +108,14 @@ using namespace kda;
 
 namespace {
 
+// Last CUDA error seen by an entry point of this thread (kda_last_error).
+thread_local char g_last_error[256] = "";
+kda_status cuda_status(cudaError_t e, const char* where) {
+    if (e == cudaSuccess) return KDA_OK;
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%d)", where, cudaGetErrorString(e), (int)e);
+    return KDA_ERR_CUDA;
+}
+
 // Optional per-kernel timing events (kda_set_profile_events).
 const cudaEvent_t* g_prof = nullptr;
 int g_prof_n = 0;
@@ -134,9 +144,8 @@ Layout layout_of(const kda_shape* sh, bool packed) { return make_layout(sh->B, s
 
 template <typename K>
 kda_status set_smem(K kernel, size_t bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) == cudaSuccess
-               ? KDA_OK
-               : KDA_ERR_CUDA;
+    return cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
+                       "cudaFuncSetAttribute");
 }
 
 kda_status common_checks(const kda_shape* shape, const int64_t* cu, void* ws, size_t ws_bytes, Layout* lay) {
@@ -186,13 +195,13 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
         kda_fwd_intra_kernel<<<dim3((unsigned)lay.nc_max, (unsigned)H), 256, fwd_intra_smem_bytes(), s>>>(
-            q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, ws, lay);
+            q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, shape->scale, ws, lay);
     prof(2, s);
     if (shape->N > 0)
         kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, fwd_scan_smem_bytes(), s>>>(
             h0, o, hT, H, shape->scale, ws, lay);
     prof(3, s);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return cuda_status(cudaGetLastError(), "kda_fwd launch");
 }
 
 extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
@@ -224,7 +233,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     prof(4, s);
     if (shape->N > 0)
         kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, bwd_scan_smem_bytes(), s>>>(
-            do_, dhT, dh0, H, scale, ws, lay);
+            do_, dhT, dh0, H, ws, lay);
     prof(5, s);
     if (lay.nc_max > 0)
         kda_bwd_state_kernel<<<tiles, 128, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws, lay);
@@ -239,8 +248,10 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     prof(8, s);
     kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);
     prof(9, s);
-    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+    return cuda_status(cudaGetLastError(), "kda_bwd launch");
 }
+
+extern "C" const char* kda_last_error(void) { return g_last_error; }
 
 extern "C" int kda_set_profile_events(void* const* events, int count) {
     g_prof = reinterpret_cast<const cudaEvent_t*>(events);
@@ -251,9 +262,11 @@ extern "C" int kda_set_profile_events(void* const* events, int count) {
 extern "C" kda_status kda_get_device_status(const void* workspace, void* stream) {
     if (!workspace) return KDA_ERR_NULL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    kda_status st = cuda_status(cudaStreamSynchronize(s), "cudaStreamSynchronize");
+    if (st != KDA_OK) return st;
     int word = 0;
-    if (cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return KDA_ERR_CUDA;
+    st = cuda_status(cudaMemcpy(&word, workspace, sizeof(int), cudaMemcpyDeviceToHost), "cudaMemcpy");
+    if (st != KDA_OK) return st;
     return static_cast<kda_status>(word);
 }
 

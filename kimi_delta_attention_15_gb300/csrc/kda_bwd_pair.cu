@@ -242,8 +242,7 @@ __global__ void __launch_bounds__(256, 1)
             rev += s.kp[r * PS + c];
             const float dgt = rev + s.em[r * PS + c] + dgam;
             const float x = bf2f(g_raw[((size_t)(t0 + r) * H + h) * D + c]) + dtc;
-            const float sg = sigmoidf(a_h * x);
-            const float du = dgt * lb * sg * (1.0f - sg);
+            const float du = dgt * lb * dsigmoidf(a_h * x);
             const float dgr = du * a_h;
             dg_raw[((size_t)(t0 + r) * H + h) * D + c] = f2bf(dgr);
             ddt += dgr;
@@ -253,9 +252,8 @@ __global__ void __launch_bounds__(256, 1)
         s.red[c] = dA;
     }
     if (tid < L) {
-        const float b = s.beta[tid];
         const float db = reinterpret_cast<const float*>(wy + WyOff::DBETA)[tid];
-        dbeta_raw[(size_t)(t0 + tid) * H + h] = f2bf(db * b * (1.0f - b));
+        dbeta_raw[(size_t)(t0 + tid) * H + h] = f2bf(db * dsigmoidf(bf2f(beta_raw[(size_t)(t0 + tid) * H + h])));
     }
     __syncthreads();
     for (int off = D / 2; off > 0; off >>= 1) {

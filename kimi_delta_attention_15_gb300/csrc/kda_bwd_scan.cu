@@ -20,7 +20,7 @@ struct BScanSmem {
     uint8_t QBT[kTileCK];    // QB^T   [128 k][64 i]   /
     uint8_t KB[kTileCK];     // KB     [64 c][128 k]   \ bulk group X
     uint8_t AQKT[kTileCC];   // Aqk^T  [64 j][64 i]    /
-    uint8_t DOT[kTileCK];    // scale*dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
+    uint8_t DOT[kTileCK];    // dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
     float gam[D];
     uint64_t barX, barY, barM1, barM2;
     uint32_t tmem;
@@ -31,7 +31,7 @@ size_t bwd_scan_smem_bytes() { return sizeof(BScanSmem) + 1024; }
 
 __global__ void __launch_bounds__(128, 1)
     kda_bwd_scan_kernel(const uint16_t* __restrict__ dO, const float* __restrict__ dhT, float* __restrict__ dh0,
-                        int H, float scale, uint8_t* __restrict__ ws, Layout lay) {
+                        int H, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
     BScanSmem& s = *reinterpret_cast<BScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     if (read_status(ws) != 0) return;
@@ -86,11 +86,11 @@ __global__ void __launch_bounds__(128, 1)
         const ChunkInfo ci = chunks[chunk];
         const size_t tile = (size_t)chunk * H + h;
         s.gam[v] = reinterpret_cast<const float*>(img_of(chunk) + ImgOff::GAML)[v];
-        // scale * dO^T into the operand tile (row v, columns i)
+        // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
+        // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
         float dov[C];
 #pragma unroll
-        for (int i = 0; i < C; ++i)
-            dov[i] = i < ci.L ? tf32_round(scale * bf2f(dO[((size_t)(ci.t0 + i) * H + h) * D + v])) : 0.0f;
+        for (int i = 0; i < C; ++i) dov[i] = i < ci.L ? bf2f(dO[((size_t)(ci.t0 + i) * H + h) * D + v]) : 0.0f;
         if (tid == 0) bulk_wait_read_all();   // previous dS checkpoint copy done reading DS
         __syncthreads();
 #pragma unroll
@@ -120,12 +120,12 @@ __global__ void __launch_bounds__(128, 1)
             if (!gx || !gy) ok = false;
             if (ok) {
                 const uint32_t aD = smem_u32(s.DOT), aS = smem_u32(s.DS);
-                // dUt^T = (scale dO^T) Aqk + dS_L KB^T
+                // dUt^T = dO^T (scale Aqk) + dS_L KB^T
                 for (int ks = 0; ks < C / 8; ++ks)
                     umma_tf32(tU, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.AQKT), C, ks), idN64, ks > 0);
                 for (int ks = 0; ks < D / 8; ++ks)
                     umma_tf32(tU, desc_kmajor(aS, D, ks), desc_kmajor(smem_u32(s.KB), C, ks), idN64, 1);
-                // dS += (scale dO^T) QB
+                // dS += dO^T (scale QB)
                 for (int ks = 0; ks < C / 8; ++ks)
                     umma_tf32(tS, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.QBT), D, ks), idN128, 1);
                 umma_commit(&s.barM1);

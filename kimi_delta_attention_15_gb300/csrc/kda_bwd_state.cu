@@ -19,7 +19,7 @@ namespace {
 struct BStateSmem {
     uint8_t S0T[kTileDD];    // S0^T   [128 k][128 v]
     uint8_t DST[kTileDD];    // dS_L^T [128 k][128 v]
-    uint8_t STK[kTileDD];    // rows 0..63: scale*dO [c][v]; rows 64..127: dUt [c][v]
+    uint8_t STK[kTileDD];    // rows 0..63: dO [c][v]; rows 64..127: dUt [c][v]
     uint8_t UT[kTileCK];     // Ut [64 c][128 v]
     uint64_t bar, barM;
     uint32_t tmem;
@@ -74,9 +74,9 @@ __global__ void __launch_bounds__(128, 1)
             *reinterpret_cast<float*>(s.DST + panel_off(c0 + 2, v, D)) = b.z;
             *reinterpret_cast<float*>(s.DST + panel_off(c0 + 3, v, D)) = b.w;
         }
-        // scale * dO rows 0..63 of the stack
+        // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
         for (int c = 0; c < C; ++c) {
-            const float x = c < ci.L ? tf32_round(scale * bf2f(dO[((size_t)(ci.t0 + c) * H + h) * D + v])) : 0.0f;
+            const float x = c < ci.L ? bf2f(dO[((size_t)(ci.t0 + c) * H + h) * D + v]) : 0.0f;
             *reinterpret_cast<float*>(s.STK + panel_off(c, v, D)) = x;
         }
     }
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(128, 1)
         if (ok) {
             const uint32_t aS = smem_u32(s.S0T), aD = smem_u32(s.DST), aK = smem_u32(s.STK), bU = smem_u32(s.UT);
             const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
-            // [dQbar | dUt S0]^T = S0^T [scale dO ; dUt]^T     -> cols 0..127
+            // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T  -> cols 0..127
             for (int ks = 0; ks < D / 8; ++ks)
                 umma_tf32(tm + 0, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, ks > 0);
             // dKbar^T = dS_L^T Ut^T                            -> cols 128..191
@@ -100,7 +100,7 @@ __global__ void __launch_bounds__(128, 1)
             // dS_L^T S0 (diagonal used)                         -> cols 256..383
             for (int ks = 0; ks < D / 8; ++ks)
                 umma_tf32(tm + 256, desc_kmajor(aD, D, ks), desc_kmajor(aS, D, ks), id128, ks > 0);
-            // [scale dO ; dUt] Ut^T (rows 0..63 used)          -> cols 384..447
+            // [dO ; dUt] Ut^T (rows 0..63 used, x scale)      -> cols 384..447
             for (int ks = 0; ks < D / 8; ++ks)
                 umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
             umma_commit(&s.barM);
@@ -122,7 +122,7 @@ __global__ void __launch_bounds__(128, 1)
             float r[32];
             tmem_ld32(tm + lb + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) gdQ[(c0 + j) * D + kq] = r[j];
+            for (int j = 0; j < 32; ++j) gdQ[(c0 + j) * D + kq] = scale * r[j];
             tmem_ld32(tm + lb + 64 + c0, r);
 #pragma unroll
             for (int j = 0; j < 32; ++j) gdW[(c0 + j) * D + kq] = -r[j];
@@ -144,11 +144,8 @@ __global__ void __launch_bounds__(128, 1)
                 float r[32];
                 tmem_ld32(tm + lb + 384 + c0, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? r[j] : 0.0f;
+                for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? scale * r[j] : 0.0f;
             }
-        } else {
-            // warps 2, 3 must still take part in the .sync.aligned loads of their own lanes? No:
-            // tcgen05.ld is per warp; warps 2, 3 simply skip the dAqk rows (lanes 64..127 unused).
         }
     } else {
         raise_status(ws, KDA_ERR_TIMEOUT);

@@ -45,8 +45,8 @@ __global__ void __launch_bounds__(256, 1)
     kda_fwd_intra_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
                          const uint16_t* __restrict__ beta_raw, const float* __restrict__ A_log,
-                         const float* __restrict__ dt_bias, int H, float lb, uint8_t* __restrict__ ws,
-                         Layout lay) {
+                         const float* __restrict__ dt_bias, int H, float lb, float scale,
+                         uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
     IntraSmem& s = *reinterpret_cast<IntraSmem*>(smem_raw);
     if (read_status(ws) != 0) return;
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(256, 1)
     }
     for (int idx = tid; idx < C * D; idx += blockDim.x) {
         const int kk = idx >> 6, c = idx & 63;           // [128][64] row-major walk
-        const float qb = tf32_round(s.qe[c * P + kk] * s.fa.Pb[c >> 4][kk]);
+        const float qb = tf32_round(scale * (s.qe[c * P + kk] * s.fa.Pb[c >> 4][kk]));
         const float kb = tf32_round(s.kp[c * P + kk] * s.fa.Sf[c >> 4][kk]);
         *reinterpret_cast<float*>(img + ImgOff::QBT + panel_off(kk, c, D)) = qb;
         *reinterpret_cast<float*>(img + ImgOff::KBT + panel_off(kk, c, D)) = kb;
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(256, 1)
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int r = idx >> 6, c = idx & 63;
         *reinterpret_cast<float*>(img + ImgOff::AQK + panel_off(r, c, C)) = tf32_round(s.Aqk[r * PA + c]);
-        *reinterpret_cast<float*>(img + ImgOff::AQKT + panel_off(r, c, C)) = tf32_round(s.Aqk[c * PA + r]);
+        *reinterpret_cast<float*>(img + ImgOff::AQKT + panel_off(r, c, C)) = tf32_round(scale * s.Aqk[c * PA + r]);
     }
     if (tid < D) reinterpret_cast<float*>(img + ImgOff::GAML)[tid] = s.fa.gl[tid];
 }

@@ -32,9 +32,9 @@ constexpr size_t kTileDD = (size_t)D * D * 4;     // [128][128] fp32
 //     GAML [128]      fp32           exp(G_L)
 //   read by the backward scan:
 //     WT   [128][64]  panels R=128   W^T
-//     QBT  [128][64]  panels R=128   (Q^ * Gamma)^T
+//     QBT  [128][64]  panels R=128   scale * (Q^ * Gamma)^T
 //     KB   [64][128]  panels R=64    K^ * exp(G_L - G)
-//     AQKT [64][64]   panels R=64    Aqk^T
+//     AQKT [64][64]   panels R=64    scale * Aqk^T
 //   read by the backward chunk kernels:
 //     XM   [64][64]   row-major fp32 X = (I + A)^{-1}
 //     BM   [64][64]   row-major fp32 B_ij = sum_c k^_ic k^_jc e^{G_ic - G_jc} (j < i), A = diag(beta) B
@@ -133,5 +133,13 @@ __device__ __forceinline__ uint16_t f2bf(float x) {
 
 // sigmoid via the CUDA exponential and an IEEE division
 __device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+// sigmoid(x) * (1 - sigmoid(x)) = u / (1 + u)^2 with u = exp(-|x|): no
+// cancellation in 1 - sigmoid(x) when the sigmoid saturates.
+__device__ __forceinline__ float dsigmoidf(float x) {
+    const float u = __expf(-fabsf(x));
+    const float d = 1.0f + u;
+    return u / (d * d);
+}
 
 }  // namespace kda

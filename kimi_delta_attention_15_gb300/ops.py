@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True):
         lib.kda_get_device_status.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_last_error.argtypes = []
+        lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_set_profile_events.argtypes = [P, ctypes.c_int]
         lib.kda_set_profile_events.restype = ctypes.c_int
         lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
@@ -95,7 +97,10 @@ def workspace_size(shape: Shape) -> int:
 
 def _check(code, where):
     if code != KDA_OK:
-        raise KdaError(code, where)
+        detail = ""
+        if code == 8:
+            detail = " (" + load().kda_last_error().decode(errors="replace") + ")"
+        raise KdaError(code, where + detail)
 
 
 def _shape_of(q, cu_seqlens, B, scale, lower_bound):
@@ -180,6 +185,9 @@ class KernelTimer:
 
     def __init__(self):
         self.events = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+        for e in self.events:     # torch creates the CUDA event on first record
+            e.record()
+        torch.cuda.synchronize()
         self._arr = (ctypes.c_void_p * 10)(*[ctypes.c_void_p(e.cuda_event) for e in self.events])
 
     def __enter__(self):
