@@ -48,6 +48,16 @@ KERNEL_MODEL = {
 }
 
 
+def _workload(args):
+    from kimi_delta_attention_15_gb300 import inputs as I
+    if not args.workload:
+        return I.WORKLOADS[I.HEADLINE]
+    for w in I.WORKLOADS + I.EXTRA_WORKLOADS:
+        if w.name == args.workload:
+            return w
+    raise SystemExit(f"unknown workload {args.workload}")
+
+
 def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -156,7 +166,7 @@ def run_reference(args, ws, rank):
         return
     from kimi_delta_attention_15_gb300 import inputs as I
     import oracle
-    w = I.WORKLOADS[I.HEADLINE]
+    w = _workload(args)
     inp = I.make_inputs(w)
     cores = oracle.default_threads()
     heads = max(1, min(w.H, cores))
@@ -188,25 +198,26 @@ def run_gb300(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist = _init_dist(ws, "nccl")
-    w = I.WORKLOADS[I.HEADLINE]
+    w = _workload(args)
     inp = I.make_inputs(w)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    shape = ops.make_shape(w.T, w.H, 1)
+    cu = d["cu_seqlens"] if w.packed else None
+    shape = ops.make_shape(w.T, w.H, w.N)
     wsp = ops.alloc_workspace(shape, dev)
     o = torch.empty_like(d["v"])
-    hT = torch.empty(1, w.H, 128, 128, device=dev)
+    hT = torch.empty(w.N, w.H, 128, 128, device=dev)
     grads = dict(dq=torch.empty_like(d["q"]), dk=torch.empty_like(d["k"]), dv=torch.empty_like(d["v"]),
                  dg_raw=torch.empty_like(d["g_raw"]), dbeta_raw=torch.empty_like(d["beta_raw"]),
                  dA_log=torch.empty_like(d["A_log"]), ddt_bias=torch.empty_like(d["dt_bias"]),
-                 dh0=torch.empty(1, w.H, 128, 128, device=dev))
+                 dh0=torch.empty(w.N, w.H, 128, 128, device=dev))
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def step():
-        ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], workspace=wsp,
-                o=o, hT=hT)
+        ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], h0=d["h0"],
+                cu_seqlens=cu, workspace=wsp, o=o, hT=hT)
         ops.bwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], d["do"], wsp,
-                grads=grads)
+                cu_seqlens=cu, dhT=d["dhT"], grads=grads)
 
     for _ in range(args.warmup):
         step()
@@ -246,7 +257,7 @@ def run_gb300(args, ws, rank, local):
     # dominant kernel and its roofline
     kms = {k: v / args.steps for k, v in per_kernel.items()}
     dom = max(KERNEL_MODEL, key=lambda k: kms[k])
-    tiles = 128 * w.H
+    tiles = sum((L + 63) // 64 for L in w.lengths) * w.H
     bytes_tile, flops_tile = KERNEL_MODEL[dom]
     t_s = kms[dom] * 1e-3
     gbs = bytes_tile * tiles / t_s / 1e9
@@ -270,7 +281,7 @@ def run_gb300(args, ws, rank, local):
 
     # end to end through the public API with pinned host buffers
     if not args.no_e2e:
-        line["e2e"] = e2e(args, inp, dev)
+        line["e2e"] = e2e(args, inp, dev, w)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         cores = oracle.default_threads()
@@ -284,16 +295,16 @@ def run_gb300(args, ws, rank, local):
         dist.destroy_process_group()
 
 
-def e2e(args, inp, dev):
+def e2e(args, inp, dev, w):
     """Same metric with host buffers: H2D of every input from pinned memory,
     kda_fwd + kda_bwd, D2H of the output and every gradient, all timed."""
     import torch
-    from kimi_delta_attention_15_gb300 import ops, inputs as I
-    w = I.WORKLOADS[I.HEADLINE]
+    from kimi_delta_attention_15_gb300 import ops
     names = ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "do")
     host = {k: inp[k].pin_memory() for k in names}
     dv = {k: torch.empty_like(host[k], device=dev) for k in names}
-    shape = ops.make_shape(w.T, w.H, 1)
+    cu = inp["cu_seqlens"].to(dev) if w.packed else None
+    shape = ops.make_shape(w.T, w.H, w.N)
     wsp = ops.alloc_workspace(shape, dev)
     out_host = {"o": torch.empty_like(host["v"]).pin_memory()}
     for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias"):
@@ -306,9 +317,9 @@ def e2e(args, inp, dev):
         for k in names:
             dv[k].copy_(host[k], non_blocking=True)
         o, _, _ = ops.fwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"],
-                          workspace=wsp, want_hT=False)
+                          cu_seqlens=cu, workspace=wsp, want_hT=False)
         g = ops.bwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"], dv["do"],
-                    wsp, want_dh0=False)
+                    wsp, cu_seqlens=cu, want_dh0=False)
         out_host["o"].copy_(o, non_blocking=True)
         for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias"):
             out_host["d" + k].copy_(g["d" + k], non_blocking=True)
@@ -333,6 +344,8 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--workload", default=None,
+                    help="name of a workload in kimi_delta_attention_15_gb300.inputs (default: the T=8192, H=96 one)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
