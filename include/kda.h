@@ -127,6 +127,40 @@ kda_status kda_get_device_status(const void* workspace, void* stream);
  * not thread-safe; pass NULL to switch it off. Returns KDA_OK. */
 int kda_set_profile_events(void* const* events, int count);
 
+/* Bytes of the scratch array compiled into the library for
+ * kda_fwd_static_scratch (64 MiB). */
+#define KDA_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* kda_fwd for callers that cannot allocate device memory. The pages have no
+ * counterpart of this entry point; it exists for the library's users.
+ *
+ * Some callers may not call cudaMalloc or any allocator: code running inside
+ * another runtime's plugin or custom-op interface, where the host program owns
+ * every device allocation, and serving loops that must not allocate, because
+ * an allocation can synchronise the device and stall other work. This entry
+ * point takes the same arguments as kda_fwd without the workspace: it uses a
+ * scratch array of KDA_STATIC_SCRATCH_BYTES compiled into the library, which
+ * every GPU that loads the library's code holds until the process exits.
+ * It calls no allocating routine.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) and caches it; make that first call before any
+ *    stream capture on that device.
+ *  - All calls on a device share the one array and it keeps the last call's
+ *    contents (what must start at zero is cleared by each call). Calls whose
+ *    work overlaps on the GPU (other streams, other host threads) race on it:
+ *    serialise them.
+ *  - Shapes whose kda_workspace_size() exceeds KDA_STATIC_SCRATCH_BYTES (about
+ *    100 (chunk of 64 tokens, head) tiles, e.g. T = 1024 with H = 4) return
+ *    KDA_ERR_WORKSPACE, and kda_last_error() states both sizes.
+ *  - Forward only: the intermediates it keeps are not available to kda_bwd.
+ * Other errors are those of kda_fwd. */
+kda_status kda_fwd_static_scratch(const kda_shape* shape,
+                                  const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                                  const kda_bf16* g_raw, const kda_bf16* beta_raw,
+                                  const float* A_log, const float* dt_bias,
+                                  const float* h0, const int64_t* cu_seqlens,
+                                  kda_bf16* o, float* hT, void* stream);
+
 /* Text of the last CUDA error an entry point of the calling thread turned
  * into KDA_ERR_CUDA ("" if none). Static per-thread buffer. */
 const char* kda_last_error(void);

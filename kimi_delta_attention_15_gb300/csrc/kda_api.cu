@@ -102,6 +102,9 @@ __global__ void __launch_bounds__(1024)
 
 __global__ void kda_clear_status_kernel(uint8_t* ws) { *reinterpret_cast<int*>(ws) = 0; }
 
+// Lets the other translation units of the library set the text kda_last_error returns.
+void set_last_error_text(const char* msg);
+
 }  // namespace kda
 
 using namespace kda;
@@ -252,6 +255,10 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
 }
 
 extern "C" const char* kda_last_error(void) { return g_last_error; }
+
+namespace kda {
+void set_last_error_text(const char* msg) { snprintf(g_last_error, sizeof(g_last_error), "%s", msg); }
+}  // namespace kda
 
 extern "C" int kda_set_profile_events(void* const* events, int count) {
     g_prof = reinterpret_cast<const cudaEvent_t*>(events);

@@ -67,6 +67,8 @@ def load(build_if_missing: bool = True):
         lib.kda_get_device_status.restype = ctypes.c_int
         lib.kda_status_string.argtypes = [ctypes.c_int]
         lib.kda_status_string.restype = ctypes.c_char_p
+        lib.kda_fwd_static_scratch.argtypes = [ctypes.POINTER(Shape)] + [P] * 11 + [P]
+        lib.kda_fwd_static_scratch.restype = ctypes.c_int
         lib.kda_last_error.argtypes = []
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_set_profile_events.argtypes = [P, ctypes.c_int]
@@ -135,6 +137,30 @@ def fwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B
                        _ptr(workspace), workspace.numel(), _stream_handle(stream))
     _check(code, "kda_fwd")
     return o, hT, workspace
+
+
+STATIC_SCRATCH_BYTES = 64 * 1024 * 1024
+
+
+def fwd_static_scratch(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B: int = 1,
+                       scale: float = SCALE, lower_bound: float = LOWER_BOUND, o=None, hT=None,
+                       want_hT: bool = True, stream=None):
+    """kda_fwd_static_scratch: the forward without a workspace argument, for
+    callers that cannot allocate device memory (the scratch is a fixed array
+    inside the library). Returns (o, hT)."""
+    lib = load()
+    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    if o is None:
+        o = torch.empty_like(v)
+    if hT is None and want_hT:
+        hT = torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32, device=q.device)
+    code = lib.kda_fwd_static_scratch(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
+                                      _ptr(beta_raw), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens),
+                                      _ptr(o), _ptr(hT), _stream_handle(stream))
+    if code == 5:
+        raise KdaError(code, "kda_fwd_static_scratch (" + lib.kda_last_error().decode(errors="replace") + ")")
+    _check(code, "kda_fwd_static_scratch")
+    return o, hT
 
 
 def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seqlens=None,
