@@ -6,8 +6,9 @@
 //     with dB (WY kernel) and dAqk (state-products kernel), for column block J:
 //     a = dM[:,J] Kt_J,  b = dM[:,J]^T Xt_J   (Xt_J = x^ e^{G-G_eJ}, Kt_J = k^_J e^{G_eJ-G_J})
 //     dx += e^{G-G_eJ} a,  dk_J += e^{G_eJ-G_J} b,  dG += Xt_J a,  dG_J -= Kt_J b
-//     (both dG terms use the same tf32-rounded operands as the products, so the
-//      pairs inside [t, L) cancel in the reverse cumulative sum as they must);
+//     (split-tf32 products, about fp32 accurate, and both dG terms multiply by
+//      the same fp32 operand values, so the pairs inside [t, L) cancel in the
+//      reverse cumulative sum as they must);
 //   dq^ += dQbar Gamma, dk^ += dKt Gamma + dKbar e^{G_L-G},
 //   dG  += dQbar Q^Gamma + dKt K^Gamma - dKbar Kbar,
 //   dG_L = sum_i dKbar_i Kbar_i + dgam exp(G_L).
@@ -60,13 +61,12 @@ __global__ void __launch_bounds__(256, 1)
     const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
     const float a_h = __expf(A_log[h]);
 
+    tile_to_smem_async(s.dB, PC, reinterpret_cast<const float*>(wy + WyOff::DB), C, C);
+    tile_to_smem_async(s.dA, PC, reinterpret_cast<const float*>(bg + BgOff::DAQK), C, C);
+    cp_async_commit();
     prep_rows(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp, s.beta,
               s.inq, s.ink);
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int r = idx >> 6, c = idx & 63;
-        s.dB[r * PC + c] = reinterpret_cast<const float*>(wy + WyOff::DB)[idx];
-        s.dA[r * PC + c] = reinterpret_cast<const float*>(bg + BgOff::DAQK)[idx];
-    }
+    cp_async_wait_all();
     __syncthreads();
     block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);
     __syncthreads();
@@ -97,13 +97,11 @@ __global__ void __launch_bounds__(256, 1)
                 for (int kk = 0; kk < 2; ++kk) {
                     const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
                     const int r0 = I * SUB + gid, r1 = r0 + 8;
-                    const uint32_t a0 = tf32_bits(dM[r0 * PC + j0]), a1 = tf32_bits(dM[r1 * PC + j0]);
-                    const uint32_t a2 = tf32_bits(dM[r0 * PC + j1]), a3 = tf32_bits(dM[r1 * PC + j1]);
+                    const Frag4 af = frag4(dM[r0 * PC + j0], dM[r1 * PC + j0], dM[r0 * PC + j1], dM[r1 * PC + j1]);
 #pragma unroll
                     for (int nt = 0; nt < 8; ++nt) {
                         const int c = ch * 64 + nt * 8 + gid;
-                        mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(s.kp[j0 * PS + c]),
-                                        tf32_bits(s.kp[j1 * PS + c]));
+                        mma3(acc[nt], af, frag2(s.kp[j0 * PS + c], s.kp[j1 * PS + c]));
                     }
                 }
                 const float* f = s.fa.F[I][J];
@@ -114,7 +112,7 @@ __global__ void __launch_bounds__(256, 1)
                         const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
                         const float fc = f[col];
                         const float R = s.em[row * PS + col] * fc;
-                        const float Xt = __uint_as_float(tf32_bits(base[row * PS + col] * fc));
+                        const float Xt = base[row * PS + col] * fc;
                         if (m == 0) adk[nt][e] += R * acc[nt][e];
                         else adq[nt][e] += R * acc[nt][e];
                         adg[nt][e] += Xt * acc[nt][e];
@@ -139,14 +137,12 @@ __global__ void __launch_bounds__(256, 1)
                 for (int kk = 0; kk < 2; ++kk) {
                     const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
                     const int c0 = J * SUB + gid, c1 = c0 + 8;
-                    const uint32_t a0 = tf32_bits(dM[i0 * PC + c0]), a1 = tf32_bits(dM[i0 * PC + c1]);
-                    const uint32_t a2 = tf32_bits(dM[i1 * PC + c0]), a3 = tf32_bits(dM[i1 * PC + c1]);
+                    const Frag4 af = frag4(dM[i0 * PC + c0], dM[i0 * PC + c1], dM[i1 * PC + c0], dM[i1 * PC + c1]);
 #pragma unroll
                     for (int nt = 0; nt < 8; ++nt) {
                         const int c = ch * 64 + nt * 8 + gid;
                         const float fc = f[c];
-                        mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(base[i0 * PS + c] * fc),
-                                        tf32_bits(base[i1 * PS + c] * fc));
+                        mma3(acc[nt], af, frag2(base[i0 * PS + c] * fc, base[i1 * PS + c] * fc));
                     }
                 }
             }
@@ -157,7 +153,7 @@ __global__ void __launch_bounds__(256, 1)
             for (int e = 0; e < 4; ++e) {
                 const int row = J * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
                 adk[nt][e] += s.ep[row * PS + col] * acc[nt][e];
-                adg[nt][e] -= __uint_as_float(tf32_bits(s.kp[row * PS + col])) * acc[nt][e];
+                adg[nt][e] -= s.kp[row * PS + col] * acc[nt][e];
             }
     }
     // (c) elementwise terms of Q^*Gamma, K^*Gamma, Kbar
@@ -237,11 +233,16 @@ __global__ void __launch_bounds__(256, 1)
         }
         const float dgam = reinterpret_cast<const float*>(bg + BgOff::DGAM)[c] * s.fa.gl[c];
         const float dtc = dt_bias[h * D + c];
+        float xr[C];
+#pragma unroll
+        for (int r = 0; r < C; ++r) xr[r] = r < L ? bf2f(g_raw[((size_t)(t0 + r) * H + h) * D + c]) + dtc : 0.0f;
         float rev = 0.0f, ddt = 0.0f, dA = 0.0f;
-        for (int r = L - 1; r >= 0; --r) {
+#pragma unroll
+        for (int r = C - 1; r >= 0; --r) {
+            if (r >= L) continue;
             rev += s.kp[r * PS + c];
             const float dgt = rev + s.em[r * PS + c] + dgam;
-            const float x = bf2f(g_raw[((size_t)(t0 + r) * H + h) * D + c]) + dtc;
+            const float x = xr[r];
             const float du = dgt * lb * dsigmoidf(a_h * x);
             const float dgr = du * a_h;
             dg_raw[((size_t)(t0 + r) * H + h) * D + c] = f2bf(dgr);

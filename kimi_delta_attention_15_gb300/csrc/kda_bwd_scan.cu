@@ -6,7 +6,7 @@
 // which is the reverse mode of the chunk form
 //   Ut = U - W S0^T,  O = scale[(Q^*Gamma) S0^T + Aqk Ut],
 //   S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
-// dS_L of every chunk (tf32, as the MMAs use it) and dUt are stored in the
+// dS_L of every chunk (tf32, as the MMAs use it) and dUt (fp32) are stored in the
 // workspace for the per-chunk backward kernels; dh0 = dS at the sequence start.
 #include "kda_internal.cuh"
 #include "umma.cuh"
@@ -16,9 +16,9 @@ namespace kda {
 namespace {
 struct BScanSmem {
     uint8_t DS[kTileDD];     // dS_L operand [128 v][128 k]
-    uint8_t WT[kTileCK];     // W^T    [128 k][64 c]   \ bulk group Y
-    uint8_t QBT[kTileCK];    // QB^T   [128 k][64 i]   /
-    uint8_t KB[kTileCK];     // KB     [64 c][128 k]   \ bulk group X
+    uint8_t WT[kTileCK];     // W^T    [128 k][64 c]     bulk group Y (second MMA group)
+    uint8_t QBT[kTileCK];    // QB^T   [128 k][64 i]   \ bulk group X (first MMA group)
+    uint8_t KB[kTileCK];     // KB     [64 c][128 k]   |
     uint8_t AQKT[kTileCC];   // Aqk^T  [64 j][64 i]    /
     uint8_t DOT[kTileCK];    // dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
     float gam[D];
@@ -68,12 +68,12 @@ __global__ void __launch_bounds__(128, 1)
 
     auto img_of = [&](int chunk) { return ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES; };
     auto issue_X = [&](int chunk) {
-        mbar_arrive_expect_tx(&s.barX, (uint32_t)(kTileCK + kTileCC));
-        bulk_g2s(s.KB, img_of(chunk) + ImgOff::KB, (uint32_t)(kTileCK + kTileCC), &s.barX);
+        mbar_arrive_expect_tx(&s.barX, (uint32_t)(2 * kTileCK + kTileCC));
+        bulk_g2s(s.QBT, img_of(chunk) + ImgOff::QBT, (uint32_t)(2 * kTileCK + kTileCC), &s.barX);
     };
     auto issue_Y = [&](int chunk) {
-        mbar_arrive_expect_tx(&s.barY, (uint32_t)(2 * kTileCK));
-        bulk_g2s(s.WT, img_of(chunk) + ImgOff::WT, (uint32_t)(2 * kTileCK), &s.barY);
+        mbar_arrive_expect_tx(&s.barY, (uint32_t)kTileCK);
+        bulk_g2s(s.WT, img_of(chunk) + ImgOff::WT, (uint32_t)kTileCK, &s.barY);
     };
     int x_issued = 0, y_issued = 0, x_done = 0, y_done = 0;
     if (tid == 0 && cf < cl) { issue_X(cl - 1); issue_Y(cl - 1); x_issued = y_issued = 1; }
@@ -81,21 +81,37 @@ __global__ void __launch_bounds__(128, 1)
     bool ok = true;
     const uint32_t idN64 = idesc_tf32(128, 64, 0, 0);
     const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
+    // dO, exp(G_L) and the chunk record are fetched one chunk ahead
+    uint32_t don[C / 2];
+    auto fetch_dO = [&](const ChunkInfo& c2) {
+#pragma unroll
+        for (int i = 0; i < C; i += 2) {
+            const uint32_t lo = i < c2.L ? dO[((size_t)(c2.t0 + i) * H + h) * D + v] : 0u;
+            const uint32_t hi = i + 1 < c2.L ? dO[((size_t)(c2.t0 + i + 1) * H + h) * D + v] : 0u;
+            don[i >> 1] = lo | (hi << 16);
+        }
+    };
+    ChunkInfo ci_next = cf < cl ? chunks[cl - 1] : ChunkInfo{0, 0, 0, 0};
+    float gam_next = cf < cl ? reinterpret_cast<const float*>(img_of(cl - 1) + ImgOff::GAML)[v] : 0.0f;
+    if (cf < cl) fetch_dO(ci_next);
     for (int chunk = cl - 1; chunk >= cf && ok; --chunk) {
         const uint32_t par = (uint32_t)((cl - 1 - chunk) & 1);
-        const ChunkInfo ci = chunks[chunk];
         const size_t tile = (size_t)chunk * H + h;
-        s.gam[v] = reinterpret_cast<const float*>(img_of(chunk) + ImgOff::GAML)[v];
-        // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
-        // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
-        float dov[C];
-#pragma unroll
-        for (int i = 0; i < C; ++i) dov[i] = i < ci.L ? bf2f(dO[((size_t)(ci.t0 + i) * H + h) * D + v]) : 0.0f;
+        s.gam[v] = gam_next;
         if (tid == 0) bulk_wait_read_all();   // previous dS checkpoint copy done reading DS
         __syncthreads();
+        // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
+        // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
 #pragma unroll
         for (int i = 0; i < C; i += 4)
-            *reinterpret_cast<float4*>(s.DOT + panel_off(v, i, D)) = make_float4(dov[i], dov[i + 1], dov[i + 2], dov[i + 3]);
+            *reinterpret_cast<float4*>(s.DOT + panel_off(v, i, D)) =
+                make_float4(bf2f((uint16_t)(don[i >> 1] & 0xffffu)), bf2f((uint16_t)(don[i >> 1] >> 16)),
+                            bf2f((uint16_t)(don[(i >> 1) + 1] & 0xffffu)), bf2f((uint16_t)(don[(i >> 1) + 1] >> 16)));
+        if (chunk - 1 >= cf) {
+            ci_next = chunks[chunk - 1];
+            gam_next = reinterpret_cast<const float*>(img_of(chunk - 1) + ImgOff::GAML)[v];
+            fetch_dO(ci_next);
+        }
         // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
         for (int c0 = 0; c0 < D; c0 += 32) {
             float r[32];
@@ -137,19 +153,17 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
         if (tid == 0 && chunk - 1 >= cf) { issue_X(chunk - 1); ++x_issued; }
 
-        // -dUt^T into the operand tile (reusing DOT); dUt -> workspace [c][v] panels
+        // -dUt^T into the operand tile (reusing DOT); dUt (fp32) -> workspace [c][v] panels
         uint8_t* gdU = ws + lay.dut + tile * kTileCK;
         for (int c0 = 0; c0 < C; c0 += 32) {
             float r[32];
             tmem_ld32(tU + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = tf32_round(r[j]);
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(c0 + j, v, C)) = r[j];
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(s.DOT + panel_off(v, c0 + j, D)) =
-                    make_float4(-r[j], -r[j + 1], -r[j + 2], -r[j + 3]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(c0 + j, v, C)) = r[j];
+                    make_float4(-tf32_round(r[j]), -tf32_round(r[j + 1]), -tf32_round(r[j + 2]), -tf32_round(r[j + 3]));
         }
         fence_async_smem();
         tc_fence_before();

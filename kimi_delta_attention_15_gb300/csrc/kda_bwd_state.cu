@@ -52,61 +52,112 @@ __global__ void __launch_bounds__(128, 1)
         fence_mbar_init();
     }
     __syncthreads();
-    // bulk loads: Ut [64][128] (R = 64) and dUt into rows 64..127 of the stack (R = 128), panel by panel
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s.bar, (uint32_t)(2 * kTileCK));
-        bulk_g2s(s.UT, gUt, (uint32_t)kTileCK, &s.bar);
-        for (int p = 0; p < 4; ++p)
-            bulk_g2s(s.STK + p * (D * 128) + 64 * 128, gdU + p * (C * 128), C * 128, &s.bar);
-    }
+    // Ut and dUt (fp32) are used split into tf32 high and low parts, in two
+    // passes over the same buffers: pass 1 with the high parts, pass 2 adds
+    // the products with the low parts (S0, dS_L and dO are exact in tf32).
+    auto load_u = [&](uint32_t) {
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&s.bar, (uint32_t)(2 * kTileCK));
+            bulk_g2s(s.UT, gUt, (uint32_t)kTileCK, &s.bar);
+            for (int p = 0; p < 4; ++p)
+                bulk_g2s(s.STK + p * (D * 128) + 64 * 128, gdU + p * (C * 128), C * 128, &s.bar);
+        }
+    };
+    // to high (lo = false) or low (lo = true) tf32 parts, in place
+    auto split_u = [&](bool lo) {
+        for (int i = tid; i < C * D; i += blockDim.x) {
+            float* a = reinterpret_cast<float*>(s.UT) + i;
+            const int r = i >> 7, c = i & 127;   // any bijection over the 64 x 128 elements
+            float* b = reinterpret_cast<float*>(s.STK + panel_off(64 + r, c, D));
+            const float x = *a, y = *b;
+            *a = lo ? tf32_round(x - tf32_round(x)) : tf32_round(x);
+            *b = lo ? tf32_round(y - tf32_round(y)) : tf32_round(y);
+        }
+    };
+    load_u(0);
     // transposed checkpoints: thread v reads row v of S0 / dS_L, writes column v
     {
         const int v = tid;
-        for (int c0 = 0; c0 < D; c0 += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(gS0 + panel_off(v, c0, D));
-            const float4 b = *reinterpret_cast<const float4*>(gDS + panel_off(v, c0, D));
-            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 0, v, D)) = a.x;
-            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 1, v, D)) = a.y;
-            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 2, v, D)) = a.z;
-            *reinterpret_cast<float*>(s.S0T + panel_off(c0 + 3, v, D)) = a.w;
-            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 0, v, D)) = b.x;
-            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 1, v, D)) = b.y;
-            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 2, v, D)) = b.z;
-            *reinterpret_cast<float*>(s.DST + panel_off(c0 + 3, v, D)) = b.w;
+        uint16_t dov[C];
+#pragma unroll
+        for (int c = 0; c < C; ++c) dov[c] = c < ci.L ? dO[((size_t)(ci.t0 + c) * H + h) * D + v] : (uint16_t)0;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float4 a[8], b[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                a[j] = *reinterpret_cast<const float4*>(gS0 + panel_off(v, c0 + 4 * j, D));
+                b[j] = *reinterpret_cast<const float4*>(gDS + panel_off(v, c0 + 4 * j, D));
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int cc = c0 + 4 * j;
+                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 0, v, D)) = a[j].x;
+                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 1, v, D)) = a[j].y;
+                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 2, v, D)) = a[j].z;
+                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 3, v, D)) = a[j].w;
+                *reinterpret_cast<float*>(s.DST + panel_off(cc + 0, v, D)) = b[j].x;
+                *reinterpret_cast<float*>(s.DST + panel_off(cc + 1, v, D)) = b[j].y;
+                *reinterpret_cast<float*>(s.DST + panel_off(cc + 2, v, D)) = b[j].z;
+                *reinterpret_cast<float*>(s.DST + panel_off(cc + 3, v, D)) = b[j].w;
+            }
         }
         // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
+#pragma unroll
         for (int c = 0; c < C; ++c) {
-            const float x = c < ci.L ? bf2f(dO[((size_t)(ci.t0 + c) * H + h) * D + v]) : 0.0f;
+            const float x = bf2f(dov[c]);
             *reinterpret_cast<float*>(s.STK + panel_off(c, v, D)) = x;
         }
     }
+    const uint32_t tm = s.tmem;
+    bool ok = mbar_wait(&s.bar, 0);
+    ok = __syncthreads_and(ok);
+    if (ok) split_u(false);
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tm = s.tmem;
-    bool ok = true;
-    if (tid == 0) {
-        ok = mbar_wait(&s.bar, 0);
-        if (ok) {
-            const uint32_t aS = smem_u32(s.S0T), aD = smem_u32(s.DST), aK = smem_u32(s.STK), bU = smem_u32(s.UT);
-            const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
-            // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T  -> cols 0..127
-            for (int ks = 0; ks < D / 8; ++ks)
-                umma_tf32(tm + 0, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, ks > 0);
-            // dKbar^T = dS_L^T Ut^T                            -> cols 128..191
-            for (int ks = 0; ks < D / 8; ++ks)
-                umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
-            // dS_L^T S0 (diagonal used)                         -> cols 256..383
-            for (int ks = 0; ks < D / 8; ++ks)
-                umma_tf32(tm + 256, desc_kmajor(aD, D, ks), desc_kmajor(aS, D, ks), id128, ks > 0);
-            // [dO ; dUt] Ut^T (rows 0..63 used, x scale)      -> cols 384..447
-            for (int ks = 0; ks < D / 8; ++ks)
-                umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
-            umma_commit(&s.barM);
-        }
+    const uint32_t aS = smem_u32(s.S0T), aD = smem_u32(s.DST), aK = smem_u32(s.STK), bU = smem_u32(s.UT);
+    const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
+    if (tid == 0 && ok) {
+        // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T  -> cols 0..127
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 0, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, ks > 0);
+        // dKbar^T = dS_L^T Ut^T                            -> cols 128..191
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
+        // dS_L^T S0 (diagonal used)                         -> cols 256..383
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 256, desc_kmajor(aD, D, ks), desc_kmajor(aS, D, ks), id128, ks > 0);
+        // [dO ; dUt] Ut^T (rows 0..63 used, x scale)      -> cols 384..447
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
+        umma_commit(&s.barM);
     }
-    ok = mbar_wait(&s.barM, 0) && ok;
+    ok = (ok && mbar_wait(&s.barM, 0));
+    ok = __syncthreads_and(ok);
+    // pass 2: the low parts of Ut and dUt
+    if (ok) {
+        tc_fence_after();
+        load_u(1);
+        ok = mbar_wait(&s.bar, 1);
+        ok = __syncthreads_and(ok);
+    }
+    if (ok) split_u(true);
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0 && ok) {
+        // (dUt_lo S0)^T                                     -> cols 64..127
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 64, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks, 64), id64, 1);
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, 1);
+        for (int ks = 0; ks < D / 8; ++ks)
+            umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, 1);
+        umma_commit(&s.barM);
+    }
+    ok = (ok && mbar_wait(&s.barM, 1));
     ok = __syncthreads_and(ok);
     tc_fence_after();
     if (ok) {

@@ -7,7 +7,8 @@
 //   dV    = T^T dU        (final dv)
 //   dbeta_j  = sum_i dT_ij X_ij + sum_l dA_jl B_jl
 //   dA    = -strict_lower(X^T dT T^T),   dB = diag(beta) dA
-// tf32 mma.sync on 16-row tiles; dKt, dB and dbeta go to the workspace.
+// Split-tf32 mma.sync on 16-row tiles (the gate gradient needs the extra
+// precision); dKt, dB and dbeta go to the workspace.
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -19,8 +20,8 @@ namespace {
 struct WySmem {
     float kt[C * PS];    // k^, then K^*Gamma
     float v[C * PS];
-    float dW[C * PS];    // dW, then M = dT T^T (stride PC)
-    float dU[C * PS];    // alpha scratch, then dU
+    float dW[C * PS];    // alpha scratch, then dW, then M = dT T^T (stride PC)
+    float dU[C * PS];
     float X[C * PC];
     float B[C * PC];
     float T[C * PC];
@@ -54,25 +55,29 @@ __global__ void __launch_bounds__(256, 1)
     uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
     const float a_h = __expf(A_log[h]);
 
-    prep_rows(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dU, s.beta,
+    // dU, X, B arrive asynchronously while the rows are prepared
+    panels_to_smem_async(s.dU, PS, gdU);
+    tile_to_smem_async(s.X, PC, reinterpret_cast<const float*>(img + ImgOff::XM), C, C);
+    tile_to_smem_async(s.B, PC, reinterpret_cast<const float*>(img + ImgOff::BM), C, C);
+    cp_async_commit();
+    prep_rows(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dW, s.beta,
               nullptr, nullptr);
     __syncthreads();
-    block_products(s.dU, nullptr, s.kt, nullptr, nullptr, &s.fa);
+    block_products(s.dW, nullptr, s.kt, nullptr, nullptr, &s.fa);
     __syncthreads();
     block_factors(&s.fa);
-    __syncthreads();
+    __syncthreads();   // alpha scratch (dW) is free
+    tile_to_smem_async(s.dW, PS, reinterpret_cast<const float*>(bg + BgOff::DW), C, D);
+    cp_async_commit();
     for (int idx = tid; idx < C * D; idx += blockDim.x) {
         const int r = idx >> 7, c = idx & 127;
         s.kt[r * PS + c] *= s.fa.Pb[r >> 4][c];
-        s.dW[r * PS + c] = reinterpret_cast<const float*>(bg + BgOff::DW)[idx];
-        s.dU[r * PS + c] = *reinterpret_cast<const float*>(gdU + panel_off(r, c, C));
     }
+    cp_async_wait_all();
+    __syncthreads();
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int r = idx >> 6, c = idx & 63;
-        const float x = reinterpret_cast<const float*>(img + ImgOff::XM)[idx];
-        s.X[r * PC + c] = x;
-        s.B[r * PC + c] = reinterpret_cast<const float*>(img + ImgOff::BM)[idx];
-        s.T[r * PC + c] = x * s.beta[c];
+        s.T[r * PC + c] = s.X[r * PC + c] * s.beta[c];
     }
     __syncthreads();
 
@@ -87,15 +92,13 @@ __global__ void __launch_bounds__(256, 1)
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < D / 8; ++ks) {
             const int k0 = ks * 8 + tig, k1 = k0 + 4;
-            const uint32_t w0 = tf32_bits(s.dW[r0 * PS + k0]), w1 = tf32_bits(s.dW[r1 * PS + k0]);
-            const uint32_t w2 = tf32_bits(s.dW[r0 * PS + k1]), w3 = tf32_bits(s.dW[r1 * PS + k1]);
-            const uint32_t u0 = tf32_bits(s.dU[r0 * PS + k0]), u1 = tf32_bits(s.dU[r1 * PS + k0]);
-            const uint32_t u2 = tf32_bits(s.dU[r0 * PS + k1]), u3 = tf32_bits(s.dU[r1 * PS + k1]);
+            const Frag4 wf = frag4(s.dW[r0 * PS + k0], s.dW[r1 * PS + k0], s.dW[r0 * PS + k1], s.dW[r1 * PS + k1]);
+            const Frag4 uf = frag4(s.dU[r0 * PS + k0], s.dU[r1 * PS + k0], s.dU[r0 * PS + k1], s.dU[r1 * PS + k1]);
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int j = ch * 32 + nt * 8 + gid;
-                mma_tf32_16x8x8(acc[nt], w0, w1, w2, w3, tf32_bits(s.kt[j * PS + k0]), tf32_bits(s.kt[j * PS + k1]));
-                mma_tf32_16x8x8(acc[nt], u0, u1, u2, u3, tf32_bits(s.v[j * PS + k0]), tf32_bits(s.v[j * PS + k1]));
+                mma3(acc[nt], wf, frag2(s.kt[j * PS + k0], s.kt[j * PS + k1]));
+                mma2a(acc[nt], uf, tf32_bits(s.v[j * PS + k0]), tf32_bits(s.v[j * PS + k1]));   // v: bf16, exact
             }
         }
 #pragma unroll
@@ -117,13 +120,12 @@ __global__ void __launch_bounds__(256, 1)
         const int j0 = jb * SUB + gid, j1 = j0 + 8;
         for (int ks = 2 * jb; ks < C / 8; ++ks) {
             const int i0 = ks * 8 + tig, i1 = i0 + 4;
-            const uint32_t a0 = tf32_bits(s.T[i0 * PC + j0]), a1 = tf32_bits(s.T[i0 * PC + j1]);
-            const uint32_t a2 = tf32_bits(s.T[i1 * PC + j0]), a3 = tf32_bits(s.T[i1 * PC + j1]);
+            const Frag4 tf = frag4(s.T[i0 * PC + j0], s.T[i0 * PC + j1], s.T[i1 * PC + j0], s.T[i1 * PC + j1]);
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int c = ch * 64 + nt * 8 + gid;
-                mma_tf32_16x8x8(ak[nt], a0, a1, a2, a3, tf32_bits(s.dW[i0 * PS + c]), tf32_bits(s.dW[i1 * PS + c]));
-                mma_tf32_16x8x8(av[nt], a0, a1, a2, a3, tf32_bits(s.dU[i0 * PS + c]), tf32_bits(s.dU[i1 * PS + c]));
+                mma3(ak[nt], tf, frag2(s.dW[i0 * PS + c], s.dW[i1 * PS + c]));
+                mma3(av[nt], tf, frag2(s.dU[i0 * PS + c], s.dU[i1 * PS + c]));
             }
         }
         float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT);
@@ -157,12 +159,11 @@ __global__ void __launch_bounds__(256, 1)
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < C / 8; ++ks) {
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
-            const uint32_t a0 = tf32_bits(s.dT[r0 * PC + m0]), a1 = tf32_bits(s.dT[r1 * PC + m0]);
-            const uint32_t a2 = tf32_bits(s.dT[r0 * PC + m1]), a3 = tf32_bits(s.dT[r1 * PC + m1]);
+            const Frag4 af = frag4(s.dT[r0 * PC + m0], s.dT[r1 * PC + m0], s.dT[r0 * PC + m1], s.dT[r1 * PC + m1]);
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int j = ch * 32 + nt * 8 + gid;
-                mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(s.T[j * PC + m0]), tf32_bits(s.T[j * PC + m1]));
+                mma3(acc[nt], af, frag2(s.T[j * PC + m0], s.T[j * PC + m1]));
             }
         }
         __syncthreads();   // everyone is done reading dW before M overwrites it
@@ -186,12 +187,11 @@ __global__ void __launch_bounds__(256, 1)
         const int i0 = ib * SUB + gid, i1 = i0 + 8;
         for (int ks = 2 * ib; ks < C / 8; ++ks) {
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
-            const uint32_t a0 = tf32_bits(s.X[m0 * PC + i0]), a1 = tf32_bits(s.X[m0 * PC + i1]);
-            const uint32_t a2 = tf32_bits(s.X[m1 * PC + i0]), a3 = tf32_bits(s.X[m1 * PC + i1]);
+            const Frag4 xf = frag4(s.X[m0 * PC + i0], s.X[m0 * PC + i1], s.X[m1 * PC + i0], s.X[m1 * PC + i1]);
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int j = ch * 32 + nt * 8 + gid;
-                mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(M[m0 * PC + j]), tf32_bits(M[m1 * PC + j]));
+                mma3(acc[nt], xf, frag2(M[m0 * PC + j], M[m1 * PC + j]));
             }
         }
 #pragma unroll

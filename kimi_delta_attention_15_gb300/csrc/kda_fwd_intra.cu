@@ -8,6 +8,8 @@
 //   T = (I + A)^{-1} diag(beta) by blocked forward substitution,
 //   W = T (K^ * Gamma), U = T V,
 // and stores the images the two state scans consume (kda_internal.cuh).
+// The pairwise products and W, U use split-tf32 operands (mma_sync.cuh): the
+// gate gradient of the backward needs them to about 1e-6 relative.
 //
 // The chunk form is the exact "16-sub-chunk + WY" prefill of the
 // kda-neuron-kernels log, with a 64-token chunk. Decay factors between rows i
@@ -90,12 +92,12 @@ __global__ void __launch_bounds__(256, 1)
         for (int ks = 0; ks < D / 8; ++ks) {
             const int k0 = ks * 8 + tig, k1 = k0 + 4;
             const float f0 = f[k0], f1 = f[k1];
-            const uint32_t a0 = tf32_bits(base[r0 * P + k0] * f0), a1 = tf32_bits(base[r1 * P + k0] * f0);
-            const uint32_t a2 = tf32_bits(base[r0 * P + k1] * f1), a3 = tf32_bits(base[r1 * P + k1] * f1);
+            const Frag4 af = frag4(base[r0 * P + k0] * f0, base[r1 * P + k0] * f0, base[r0 * P + k1] * f1,
+                                   base[r1 * P + k1] * f1);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = J * SUB + nt * 8 + gid;
-                mma_tf32_16x8x8(acc[nt], a0, a1, a2, a3, tf32_bits(s.kp[j * P + k0]), tf32_bits(s.kp[j * P + k1]));
+                mma3(acc[nt], af, frag2(s.kp[j * P + k0], s.kp[j * P + k1]));
             }
         }
 #pragma unroll
@@ -167,15 +169,14 @@ __global__ void __launch_bounds__(256, 1)
         const int ra = rb * SUB + gid, rbb = ra + 8;
         for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
             const int j0 = ks * 8 + tig, j1 = j0 + 4;
-            const uint32_t a0 = tf32_bits(s.T[ra * PA + j0]), a1 = tf32_bits(s.T[rbb * PA + j0]);
-            const uint32_t a2 = tf32_bits(s.T[ra * PA + j1]), a3 = tf32_bits(s.T[rbb * PA + j1]);
+            const Frag4 tf = frag4(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
             const float* pb = s.fa.Pb[j0 >> 4];
 #pragma unroll
             for (int nt = 0; nt < 8; ++nt) {
                 const int c = ch * 64 + nt * 8 + gid;
-                mma_tf32_16x8x8(aw[nt], a0, a1, a2, a3, tf32_bits(s.ke[j0 * P + c] * pb[c]),
-                                tf32_bits(s.ke[j1 * P + c] * pb[c]));
-                mma_tf32_16x8x8(au[nt], a0, a1, a2, a3, tf32_bits(s.v[j0 * P + c]), tf32_bits(s.v[j1 * P + c]));
+                mma3(aw[nt], tf, frag2(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
+                // v is bf16 data, exact in tf32
+                mma2a(au[nt], tf, tf32_bits(s.v[j0 * P + c]), tf32_bits(s.v[j1 * P + c]));
             }
         }
         float* gU = reinterpret_cast<float*>(img + ImgOff::U);

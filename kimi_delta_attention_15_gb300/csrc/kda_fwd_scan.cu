@@ -9,7 +9,7 @@
 // (chunk form of S_t = S_{t-1} diag(e^{g_t}) (I - b k^ k^T) + b v k^T,
 //  o_t = scale S_t q^_t; flashinfer "kda_backward" contract). S0 of every
 // chunk, rounded to tf32 as the MMAs use it, is checkpointed to the
-// workspace for the backward, together with Ut.
+// workspace for the backward, together with Ut (fp32).
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
@@ -86,13 +86,22 @@ __global__ void __launch_bounds__(128, 1)
     bool ok = true;
     const uint32_t idS0W = idesc_tf32(128, 64, 0, 0);
     const uint32_t idS = idesc_tf32(128, 128, 0, 0);
+    // per-chunk scalars are fetched one chunk ahead
+    ChunkInfo ci_next = cf < cl ? chunks[cf] : ChunkInfo{0, 0, 0, 0};
+    float gam_next = cf < cl ? reinterpret_cast<const float*>(ws + lay.img + ((size_t)cf * H + h) * ImgOff::BYTES +
+                                                              ImgOff::GAML)[v]
+                             : 0.0f;
     for (int chunk = cf; chunk < cl && ok; ++chunk) {
         const uint32_t par = (uint32_t)((chunk - cf) & 1);
-        const ChunkInfo ci = chunks[chunk];
+        const ChunkInfo ci = ci_next;
         const size_t tile = (size_t)chunk * H + h;
         const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
         const float* gU = reinterpret_cast<const float*>(img + ImgOff::U);
-        s.gam[v] = reinterpret_cast<const float*>(img + ImgOff::GAML)[v];
+        s.gam[v] = gam_next;
+        if (chunk + 1 < cl) {
+            ci_next = chunks[chunk + 1];
+            gam_next = reinterpret_cast<const float*>(img + (size_t)H * ImgOff::BYTES + ImgOff::GAML)[v];  // chunk + 1
+        }
         if (tid == 0) bulk_wait_read_all();   // previous checkpoint copy finished reading S0
         __syncthreads();
 
@@ -139,19 +148,19 @@ __global__ void __launch_bounds__(128, 1)
         tc_fence_after();
         if (tid == 0 && chunk + 1 < cl) { issue_A(chunk + 1); ++a_issued; }
 
-        // Ut^T = U^T - S0 W^T  -> tf32 operand [v][c]; Ut -> workspace [c][v] panels
+        // Ut^T = U^T - S0 W^T  -> tf32 operand [v][c]; Ut (fp32) -> workspace [c][v] panels
         uint8_t* gUt = ws + lay.ut + tile * kTileCK;
         for (int c0 = 0; c0 < C; c0 += 32) {
             float r[32];
             tmem_ld32(tUT + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = tf32_round(u[c0 + j] - r[j]);
+            for (int j = 0; j < 32; ++j) r[j] = u[c0 + j] - r[j];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gUt + panel_off(c0 + j, v, C)) = r[j];
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
                 *reinterpret_cast<float4*>(s.UT + panel_off(v, c0 + j, D)) =
-                    make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gUt + panel_off(c0 + j, v, C)) = r[j];
+                    make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]), tf32_round(r[j + 3]));
         }
         fence_async_smem();
         tc_fence_before();

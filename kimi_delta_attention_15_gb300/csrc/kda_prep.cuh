@@ -14,6 +14,7 @@
 // chunk length L are zero with alpha = 1 (no decay) and beta = 0.
 #pragma once
 #include "kda_internal.cuh"
+#include "umma.cuh"
 
 namespace kda {
 
@@ -38,44 +39,62 @@ __device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const 
                                           float* xv, float* xa, float* beta, float* inq, float* ink) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
     const int c0 = lane * 4;
-    for (int r = warp; r < C; r += nw) {
-        float qv[4] = {0, 0, 0, 0}, kv[4] = {0, 0, 0, 0}, vv[4] = {0, 0, 0, 0}, al[4] = {1, 1, 1, 1};
-        if (r < L) {
-            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-            auto ld4 = [&](const uint16_t* p, float* out) {
-                const uint2 w = *reinterpret_cast<const uint2*>(p + base);
+    const bool wq = xq || inq, wk = xk || ink;
+    float dtv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dtv[e] = xa ? dt_bias[h * D + c0 + e] : 0.0f;
+    constexpr int RB = 4;   // rows per batch of loads
+    for (int rb0 = warp; rb0 < C; rb0 += nw * RB) {
+        uint2 wqv[RB], wkv[RB], wvv[RB], wgv[RB];
+        float brv[RB];
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = rb0 + b * nw;
+            wqv[b] = wkv[b] = wvv[b] = wgv[b] = make_uint2(0u, 0u);
+            brv[b] = 0.0f;
+            if (r < L) {
+                if (beta && lane == 0) brv[b] = bf2f(beta_raw[(size_t)(t0 + r) * H + h]);
+                const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+                if (wq) wqv[b] = *reinterpret_cast<const uint2*>(q + base);
+                if (wk) wkv[b] = *reinterpret_cast<const uint2*>(k + base);
+                if (xv) wvv[b] = *reinterpret_cast<const uint2*>(v + base);
+                if (xa) wgv[b] = *reinterpret_cast<const uint2*>(g_raw + base);
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = rb0 + b * nw;
+            if (r >= C) break;
+            auto un = [](uint2 w, float* out) {
                 out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
                 out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
             };
-            if (xq || inq) ld4(q, qv);
-            if (xk || ink) ld4(k, kv);
-            if (xv) ld4(v, vv);
-            if (xa) {
-                float gr[4];
-                ld4(g_raw, gr);
+            float qv[4], kv[4], vv[4], gr[4], al[4] = {1, 1, 1, 1};
+            un(wqv[b], qv); un(wkv[b], kv); un(wvv[b], vv); un(wgv[b], gr);
+            if (xa && r < L) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dt_bias[h * D + c0 + e])));
+                for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dtv[e])));
             }
-        }
-        float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-        float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            sq += __shfl_xor_sync(0xffffffffu, sq, o);
-            sk += __shfl_xor_sync(0xffffffffu, sk, o);
-        }
-        const float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
+            for (int o = 16; o > 0; o >>= 1) {
+                sq += __shfl_xor_sync(0xffffffffu, sq, o);
+                sk += __shfl_xor_sync(0xffffffffu, sk, o);
+            }
+            const float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            if (xq) xq[r * PS + c0 + e] = qv[e] * iq;
-            if (xk) xk[r * PS + c0 + e] = kv[e] * ik;
-            if (xv) xv[r * PS + c0 + e] = vv[e];
-            if (xa) xa[r * PS + c0 + e] = al[e];
-        }
-        if (lane == 0) {
-            if (beta) beta[r] = r < L ? sigmoidf(bf2f(beta_raw[(size_t)(t0 + r) * H + h])) : 0.0f;
-            if (inq) inq[r] = iq;
-            if (ink) ink[r] = ik;
+            for (int e = 0; e < 4; ++e) {
+                if (xq) xq[r * PS + c0 + e] = qv[e] * iq;
+                if (xk) xk[r * PS + c0 + e] = kv[e] * ik;
+                if (xv) xv[r * PS + c0 + e] = vv[e];
+                if (xa) xa[r * PS + c0 + e] = al[e];
+            }
+            if (lane == 0) {
+                if (beta) beta[r] = r < L ? sigmoidf(brv[b]) : 0.0f;
+                if (inq) inq[r] = iq;
+                if (ink) ink[r] = ik;
+            }
         }
     }
 }
@@ -132,4 +151,23 @@ __device__ __forceinline__ void tri_pair(int t, int& I, int& J) {
     J = t;
 }
 
+}  // namespace kda
+
+namespace kda {
+// Asynchronous copy of a row-major fp32 [rows][cols] global tile into a padded
+// shared tile (row stride `ld` floats); cols a multiple of 4.
+__device__ __forceinline__ void tile_to_smem_async(float* dst, int ld, const float* src, int rows, int cols) {
+    const int chunks = cols >> 2;
+    for (int i = threadIdx.x; i < rows * chunks; i += blockDim.x) {
+        const int r = i / chunks, j = i - r * chunks;
+        cp_async16(dst + r * ld + 4 * j, src + r * cols + 4 * j);
+    }
+}
+// The same from a [64][128] panel image (umma.cuh layout, R = 64 rows).
+__device__ __forceinline__ void panels_to_smem_async(float* dst, int ld, const uint8_t* src) {
+    for (int i = threadIdx.x; i < C * 32; i += blockDim.x) {
+        const int r = i >> 5, j = i & 31;   // 16-byte chunk j of row r
+        cp_async16(dst + r * ld + 4 * j, src + (j >> 3) * C * 128 + r * 128 + ((((j & 7) ^ (r & 7))) << 4));
+    }
+}
 }  // namespace kda

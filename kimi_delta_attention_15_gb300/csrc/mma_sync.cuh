@@ -26,3 +26,40 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], uint32_t a0, uint
 }
 
 }  // namespace kda
+
+namespace kda {
+
+// Split-tf32 ("3xTF32") products: x = hi + lo with hi = tf32(x), lo = tf32(x - hi),
+// and a*b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps about 21 bits of the
+// fp32 operands instead of 10. Used where the gate gradient needs more than tf32.
+struct Frag4 { uint32_t hi[4], lo[4]; };
+struct Frag2 { uint32_t hi[2], lo[2]; };
+
+__device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
+    hi = tf32_bits(x);
+    lo = tf32_bits(x - __uint_as_float(hi));
+}
+__device__ __forceinline__ Frag4 frag4(float a0, float a1, float a2, float a3) {
+    Frag4 f;
+    split_tf32(a0, f.hi[0], f.lo[0]); split_tf32(a1, f.hi[1], f.lo[1]);
+    split_tf32(a2, f.hi[2], f.lo[2]); split_tf32(a3, f.hi[3], f.lo[3]);
+    return f;
+}
+__device__ __forceinline__ Frag2 frag2(float b0, float b1) {
+    Frag2 f;
+    split_tf32(b0, f.hi[0], f.lo[0]); split_tf32(b1, f.hi[1], f.lo[1]);
+    return f;
+}
+// c += a * b, both operands split
+__device__ __forceinline__ void mma3(float (&c)[4], const Frag4& a, const Frag2& b) {
+    mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b.hi[0], b.hi[1]);
+    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.lo[0], b.lo[1]);
+    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.hi[0], b.hi[1]);
+}
+// c += a * b, b exact in tf32 (e.g. bf16 data)
+__device__ __forceinline__ void mma2a(float (&c)[4], const Frag4& a, uint32_t b0, uint32_t b1) {
+    mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b0, b1);
+    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b0, b1);
+}
+
+}  // namespace kda
