@@ -196,61 +196,87 @@ __global__ void __launch_bounds__(256, 1)
         }
     __syncthreads();
 
-    // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps)
-    for (int r = warp; r < L; r += 8) {
+    // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); all rows of a warp loaded at once
+    {
         const int c0 = lane * 4;
-        const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+        uint2 wq[C / 8], wk[C / 8];
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-            const uint16_t* src = which == 0 ? q : k;
-            const float* dx = which == 0 ? s.qe : s.ke;
-            const float inv = which == 0 ? s.inq[r] : s.ink[r];
-            const uint2 w = *reinterpret_cast<const uint2*>(src + base);
-            const float xv[4] = {bf2f((uint16_t)(w.x & 0xffffu)) * inv, bf2f((uint16_t)(w.x >> 16)) * inv,
-                                 bf2f((uint16_t)(w.y & 0xffffu)) * inv, bf2f((uint16_t)(w.y >> 16)) * inv};
-            float dot = 0.0f;
+        for (int b = 0; b < C / 8; ++b) {
+            const int r = warp + 8 * b;
+            wq[b] = wk[b] = make_uint2(0u, 0u);
+            if (r < L) {
+                const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+                wq[b] = *reinterpret_cast<const uint2*>(q + base);
+                wk[b] = *reinterpret_cast<const uint2*>(k + base);
+            }
+        }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) dot += xv[e] * dx[r * PS + c0 + e];
+        for (int b = 0; b < C / 8; ++b) {
+            const int r = warp + 8 * b;
+            if (r >= L) break;
+            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-            uint16_t out[4];
+            for (int which = 0; which < 2; ++which) {
+                const uint2 w = which == 0 ? wq[b] : wk[b];
+                const float* dx = which == 0 ? s.qe : s.ke;
+                const float inv = which == 0 ? s.inq[r] : s.ink[r];
+                const float xv[4] = {bf2f((uint16_t)(w.x & 0xffffu)) * inv, bf2f((uint16_t)(w.x >> 16)) * inv,
+                                     bf2f((uint16_t)(w.y & 0xffffu)) * inv, bf2f((uint16_t)(w.y >> 16)) * inv};
+                float dot = 0.0f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) out[e] = f2bf((dx[r * PS + c0 + e] - xv[e] * dot) * inv);
-            uint16_t* dst = which == 0 ? dq : dk;
-            *reinterpret_cast<uint2*>(dst + base) =
-                make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 16), (uint32_t)out[2] | ((uint32_t)out[3] << 16));
+                for (int e = 0; e < 4; ++e) dot += xv[e] * dx[r * PS + c0 + e];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+                uint16_t out[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) out[e] = f2bf((dx[r * PS + c0 + e] - xv[e] * dot) * inv);
+                uint16_t* dst = which == 0 ? dq : dk;
+                *reinterpret_cast<uint2*>(dst + base) = make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 16),
+                                                                   (uint32_t)out[2] | ((uint32_t)out[3] << 16));
+            }
         }
     }
-    // dg: reverse cumulative sum over rows, gate chain, parameter partials (thread per key channel)
+    // dg: sums over rows per key channel (threads 0..127), written back as dg_t
+    //   dg_t = sum_{i>=t} dG'_i + sum_{i<t} dKbar_i Kbar_i + dgam exp(G_L)
     float* part = reinterpret_cast<float*>(ws + lay.part) + tile * (D + 4);
     if (tid < D) {
         const int c = tid;
+        const float dgam = reinterpret_cast<const float*>(bg + BgOff::DGAM)[c] * s.fa.gl[c];
         float run = 0.0f;
-        for (int r = 0; r < L; ++r) {      // exclusive prefix of dKbar*Kbar
+        for (int r = 0; r < L; ++r) {
             const float p = s.em[r * PS + c];
             s.em[r * PS + c] = run;
             run += p;
         }
-        const float dgam = reinterpret_cast<const float*>(bg + BgOff::DGAM)[c] * s.fa.gl[c];
-        const float dtc = dt_bias[h * D + c];
-        float xr[C];
-#pragma unroll
-        for (int r = 0; r < C; ++r) xr[r] = r < L ? bf2f(g_raw[((size_t)(t0 + r) * H + h) * D + c]) + dtc : 0.0f;
-        float rev = 0.0f, ddt = 0.0f, dA = 0.0f;
-#pragma unroll
-        for (int r = C - 1; r >= 0; --r) {
-            if (r >= L) continue;
+        float rev = 0.0f;
+        for (int r = L - 1; r >= 0; --r) {
             rev += s.kp[r * PS + c];
-            const float dgt = rev + s.em[r * PS + c] + dgam;
-            const float x = xr[r];
-            const float du = dgt * lb * dsigmoidf(a_h * x);
-            const float dgr = du * a_h;
-            dg_raw[((size_t)(t0 + r) * H + h) * D + c] = f2bf(dgr);
+            s.kp[r * PS + c] = rev + s.em[r * PS + c] + dgam;
+        }
+    }
+    __syncthreads();
+    // gate chain, every thread: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
+    {
+        const int c = tid & (D - 1), r0 = tid >> 7;
+        const float dtc = dt_bias[h * D + c];
+        float ddt = 0.0f, dA = 0.0f;
+#pragma unroll 4
+        for (int r = r0; r < L; r += 2) {
+            const size_t gi = ((size_t)(t0 + r) * H + h) * D + c;
+            const float x = bf2f(g_raw[gi]) + dtc;
+            const float dgr = s.kp[r * PS + c] * lb * dsigmoidf(a_h * x) * a_h;
+            dg_raw[gi] = f2bf(dgr);
             ddt += dgr;
             dA += dgr * x;
         }
-        part[c] = ddt;
-        s.red[c] = dA;
+        // two threads per channel: rows of even / odd index; combined in a fixed order
+        s.em[r0 * PS + c] = ddt;
+        s.ep[r0 * PS + c] = dA;
+    }
+    __syncthreads();
+    if (tid < D) {
+        part[tid] = s.em[tid] + s.em[PS + tid];
+        s.red[tid] = s.ep[tid] + s.ep[PS + tid];
     }
     if (tid < L) {
         const float db = reinterpret_cast<const float*>(wy + WyOff::DBETA)[tid];

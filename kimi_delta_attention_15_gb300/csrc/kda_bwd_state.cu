@@ -28,7 +28,7 @@ struct BStateSmem {
 
 size_t bwd_state_smem_bytes() { return sizeof(BStateSmem) + 1024; }
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     kda_bwd_state_kernel(const uint16_t* __restrict__ dO, int H, float scale, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
     BStateSmem& s = *reinterpret_cast<BStateSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -75,13 +75,17 @@ __global__ void __launch_bounds__(128, 1)
         }
     };
     load_u(0);
-    // transposed checkpoints: thread v reads row v of S0 / dS_L, writes column v
+    // transposed checkpoints: threads (v, half) read half of row v of S0 / dS_L, write column v
     {
-        const int v = tid;
-        uint16_t dov[C];
+        const int v = tid & (D - 1), half = tid >> 7;
+        uint16_t dov[C / 2];
 #pragma unroll
-        for (int c = 0; c < C; ++c) dov[c] = c < ci.L ? dO[((size_t)(ci.t0 + c) * H + h) * D + v] : (uint16_t)0;
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int i = 0; i < C / 2; ++i) {
+            const int c = half * (C / 2) + i;
+            dov[i] = c < ci.L ? dO[((size_t)(ci.t0 + c) * H + h) * D + v] : (uint16_t)0;
+        }
+#pragma unroll
+        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
             float4 a[8], b[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -103,10 +107,8 @@ __global__ void __launch_bounds__(128, 1)
         }
         // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
 #pragma unroll
-        for (int c = 0; c < C; ++c) {
-            const float x = bf2f(dov[c]);
-            *reinterpret_cast<float*>(s.STK + panel_off(c, v, D)) = x;
-        }
+        for (int i = 0; i < C / 2; ++i)
+            *reinterpret_cast<float*>(s.STK + panel_off(half * (C / 2) + i, v, D)) = bf2f(dov[i]);
     }
     const uint32_t tm = s.tmem;
     bool ok = mbar_wait(&s.bar, 0);
@@ -161,15 +163,17 @@ __global__ void __launch_bounds__(128, 1)
     ok = __syncthreads_and(ok);
     tc_fence_after();
     if (ok) {
-        const int kq = tid;   // lane = key channel k (or row i for dAqk)
-        const uint32_t lb = (uint32_t)(warp * 32) << 16;
+        // warp w reads TMEM lanes 32 (w % 4) .. +31; warps w and w + 4 split the columns
+        const int kq = (warp & 3) * 32 + (tid & 31);   // lane = key channel k (or row i for dAqk)
+        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
+        const int c0 = (warp >> 2) * 32;
         uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
         float* gdQ = reinterpret_cast<float*>(bg + BgOff::DQB);
         float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
         float* gdK = reinterpret_cast<float*>(bg + BgOff::DKB);
         float* gdA = reinterpret_cast<float*>(bg + BgOff::DAQK);
         float* gdG = reinterpret_cast<float*>(bg + BgOff::DGAM);
-        for (int c0 = 0; c0 < C; c0 += 32) {
+        {
             float r[32];
             tmem_ld32(tm + lb + c0, r);
 #pragma unroll
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) gdK[(c0 + j) * D + kq] = r[j];
         }
-        {
+        if (warp < 4) {
             float r[32];
             tmem_ld32(tm + lb + 256 + warp * 32, r);
             float dg = 0.0f;
@@ -189,14 +193,12 @@ __global__ void __launch_bounds__(128, 1)
             for (int j = 0; j < 32; ++j) dg = (j == (tid & 31)) ? r[j] : dg;
             gdG[kq] = dg;
         }
-        if (warp < 2) {
-            const int i = tid;
-            for (int c0 = 0; c0 < C; c0 += 32) {
-                float r[32];
-                tmem_ld32(tm + lb + 384 + c0, r);
+        if ((warp & 3) < 2) {
+            const int i = kq;
+            float r[32];
+            tmem_ld32(tm + lb + 384 + c0, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? scale * r[j] : 0.0f;
-            }
+            for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? scale * r[j] : 0.0f;
         }
     } else {
         raise_status(ws, KDA_ERR_TIMEOUT);

@@ -131,15 +131,16 @@ __device__ __forceinline__ uint16_t f2bf(float x) {
     return *reinterpret_cast<uint16_t*>(&b);
 }
 
-// sigmoid via the CUDA exponential and an IEEE division
-__device__ __forceinline__ float sigmoidf(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// sigmoid via the CUDA exponential and the fast division (denominator >= 1;
+// an infinite denominator gives the correct limit 0)
+__device__ __forceinline__ float sigmoidf(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
 // sigmoid(x) * (1 - sigmoid(x)) = u / (1 + u)^2 with u = exp(-|x|): no
 // cancellation in 1 - sigmoid(x) when the sigmoid saturates.
 __device__ __forceinline__ float dsigmoidf(float x) {
     const float u = __expf(-fabsf(x));
     const float d = 1.0f + u;
-    return u / (d * d);
+    return __fdividef(u, d * d);
 }
 
 }  // namespace kda

@@ -43,7 +43,7 @@ __device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const 
     float dtv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) dtv[e] = xa ? dt_bias[h * D + c0 + e] : 0.0f;
-    constexpr int RB = 4;   // rows per batch of loads
+    constexpr int RB = C / 8;   // rows per batch of loads (all rows of a warp at 8 warps)
     for (int rb0 = warp; rb0 < C; rb0 += nw * RB) {
         uint2 wqv[RB], wkv[RB], wvv[RB], wgv[RB];
         float brv[RB];
