@@ -180,6 +180,14 @@ const char* kda_status_string(kda_status s);
 int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, const float* B,
                            float* D, void* stream);
 
+/* Diagnostics: launches one CTA that waits on an mbarrier nothing completes,
+ * gives up after limit_ns (1 .. 1e9 ns), and sets KDA_ERR_TIMEOUT in the
+ * status word of `workspace` (its first 4 bytes, device memory) exactly as a
+ * timed-out wait inside kda_fwd / kda_bwd would. Read it with
+ * kda_get_device_status(). Used by the tests of the failure path; the
+ * context stays usable afterwards. */
+int kda_diag_wait_timeout(unsigned long long limit_ns, void* workspace, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

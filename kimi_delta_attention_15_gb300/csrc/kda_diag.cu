@@ -81,7 +81,29 @@ __global__ void __launch_bounds__(128, 1)
     if (warp == 0) tmem_dealloc(tm, 256);
 }
 
+// Waits on an mbarrier that nothing will ever complete, with a limit of
+// limit_ns, then reports KDA_ERR_TIMEOUT in the status word at `status_word`
+// the same way the KDA kernels do. Exercises the timeout path without hanging.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, uint8_t* status_word) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    bool ok = mbar_wait(&bar, 0, limit_ns);   // nobody arrives
+    ok = __syncthreads_and(ok);
+    if (!ok && threadIdx.x == 0) raise_status(status_word, KDA_ERR_TIMEOUT);
+}
+
 }  // namespace kda
+
+extern "C" int kda_diag_wait_timeout(unsigned long long limit_ns, void* workspace, void* stream) {
+    if (!workspace) return KDA_ERR_NULL;
+    if (limit_ns == 0 || limit_ns > 1000000000ull) return KDA_ERR_UNSUPPORTED;
+    kda::wait_timeout_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(limit_ns, static_cast<uint8_t*>(workspace));
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 
 extern "C" int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, const float* B,
                                       float* D, void* stream) {

@@ -73,6 +73,8 @@ def load(build_if_missing: bool = True):
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_set_profile_events.argtypes = [P, ctypes.c_int]
         lib.kda_set_profile_events.restype = ctypes.c_int
+        lib.kda_diag_wait_timeout.argtypes = [ctypes.c_ulonglong, P, P]
+        lib.kda_diag_wait_timeout.restype = ctypes.c_int
         lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
         lib.kda_diag_umma_selftest.restype = ctypes.c_int
         _lib = lib
@@ -187,6 +189,11 @@ def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seq
 
 def device_status(workspace, stream=None) -> int:
     return int(load().kda_get_device_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def wait_timeout(workspace, limit_ns: int = 20_000_000):
+    """Diagnostic: a kernel whose wait runs out sets KDA_ERR_TIMEOUT in `workspace`."""
+    _check(load().kda_diag_wait_timeout(limit_ns, _ptr(workspace), _stream_handle()), "kda_diag_wait_timeout")
 
 
 def umma_selftest(A, B, a_mn: int, b_mn: int):
