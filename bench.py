@@ -47,6 +47,26 @@ KERNEL_MODEL = {
     "bwd_pair": (225.0 * KB, 2.62e6),
 }
 
+# DRAM traffic per tile (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture
+# on T=4096 H=32, 2,048 tiles; profiles/kernels_fixed_T4096_H32.md). Valid only for the
+# kernel sources it was measured on: `sources` is a hash of csrc/, checked at run time.
+MEASURED_TRAFFIC = {
+    "sources": "beb975906222fd6e",
+    "per_tile": {"fwd_intra": 332168, "fwd_scan": 244300, "bwd_scan": 211651, "bwd_state": 311142,
+                 "bwd_wy": 200034, "bwd_pair": 222258},
+}
+
+
+def _sources_hash():
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "kimi_delta_attention_15_gb300", "csrc", "*"))):
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
 
 def _workload(args):
     from kimi_delta_attention_15_gb300 import inputs as I
@@ -267,7 +287,11 @@ def run_gb300(args, ws, rank, local):
     roof = ({"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": hbm_frac}
             if bound == "hbm" else
             {"bound": "tensor", "achieved": tfl, "peak": bf16, "unit": "TFLOP/s", "frac": tc_frac})
-    roof.update({"kernel": dom, "traffic": None, "peak_source": peak_src,
+    traffic = None
+    if _sources_hash() == MEASURED_TRAFFIC["sources"] and dom in MEASURED_TRAFFIC["per_tile"]:
+        traffic = MEASURED_TRAFFIC["per_tile"][dom] * tiles   # bytes per launch, scaled by tiles
+    roof.update({"kernel": dom, "traffic": traffic, "algorithmic_bytes": bytes_tile * tiles,
+                 "peak_source": peak_src,
                  "kernel_ms": {k: round(v, 4) for k, v in kms.items()}})
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
