@@ -145,6 +145,16 @@ kda_status check_shape(const kda_shape* sh, bool packed) {
 
 Layout layout_of(const kda_shape* sh, bool packed) { return make_layout(sh->B, sh->T, sh->H, sh->N, packed); }
 
+// Grid of a persistent per-tile kernel: one CTA per SM (each holds ~220 KB of
+// shared memory), never more CTAs than tiles.
+unsigned persistent_grid(int64_t tiles) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        sms <= 0)
+        sms = 148;
+    return (unsigned)(tiles < sms ? (tiles > 0 ? tiles : 1) : sms);
+}
+
 template <typename K>
 kda_status set_smem(K kernel, size_t bytes) {
     return cuda_status(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes),
@@ -197,7 +207,7 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
-        kda_fwd_intra_kernel<<<dim3((unsigned)lay.nc_max, (unsigned)H), 256, fwd_intra_smem_bytes(), s>>>(
+        kda_fwd_intra_kernel<<<persistent_grid(lay.nc_max * H), 256, fwd_intra_smem_bytes(), s>>>(
             q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, shape->scale, ws, lay);
     prof(2, s);
     if (shape->N > 0)
@@ -242,7 +252,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
         kda_bwd_state_kernel<<<tiles, 256, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws, lay);
     prof(6, s);
     if (lay.nc_max > 0)
-        kda_bwd_wy_kernel<<<tiles, 256, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,
+        kda_bwd_wy_kernel<<<persistent_grid(lay.nc_max * H), 256, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,
                                                                    ws, lay);
     prof(7, s);
     if (lay.nc_max > 0)

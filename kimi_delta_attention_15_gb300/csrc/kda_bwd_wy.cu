@@ -1,5 +1,5 @@
-// Backward through the UT transform of each chunk: one CTA per (chunk, head),
-// all chunks in parallel. With W = T (K^*Gamma), U = T V, T = X diag(beta),
+// Backward through the UT transform of each chunk: persistent CTAs (one per
+// SM) over all (chunk, head) tiles. With W = T (K^*Gamma), U = T V, T = X diag(beta),
 // X = (I + A)^{-1}, A = diag(beta) B, and the adjoints dW (state-products
 // kernel) and dU = dUt (backward scan):
 //   dT    = dW (K^*Gamma)^T + dU V^T
@@ -42,26 +42,47 @@ __global__ void __launch_bounds__(256, 1)
     extern __shared__ uint8_t smem_raw[];
     WySmem& s = *reinterpret_cast<WySmem*>(smem_raw);
     if (read_status(ws) != 0) return;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
-    if (ci.L <= 0) return;
-    const int L = ci.L;
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int ntiles = (int)lay.nc_max * H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const size_t tile = (size_t)chunk * H + h;
+    // Persistent over tiles (tile = chunk * H + h); the next tile's rows are
+    // loaded into registers while the current one computes.
+    RowRegs rr;
+    // chunk records are read two tiles ahead so the row loads never wait on them
+    const int step = (int)gridDim.x;
+    auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
+    ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
+    auto fetch = [&](int t) {   // t: the tile whose record is ci_next
+        if (ci_next.L > 0) prep_load(rr, nullptr, k, v, g_raw, beta_raw, ci_next.t0, ci_next.L, H, t % H, A_log, dt_bias);
+    };
+    if ((int)blockIdx.x < ntiles) fetch(blockIdx.x);
+    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
+    const ChunkInfo ci = ci_next;
+    const int h = tile_i % H;
+    const int nxt = tile_i + step;
+    ci_next = ci_next2;                        // record of tile nxt
+    ci_next2 = chunk_of(nxt + step);
+    if (ci.L <= 0) {
+        if (nxt < ntiles) fetch(nxt);
+        continue;
+    }
+    const int L = ci.L;
+    const size_t tile = (size_t)tile_i;
     const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
     uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
-    const float a_h = __expf(A_log[h]);
+    const float a_h = __expf(rr.alog);
 
     // dU, X, B arrive asynchronously while the rows are prepared
     panels_to_smem_async(s.dU, PS, gdU);
     tile_to_smem_async(s.X, PC, reinterpret_cast<const float*>(img + ImgOff::XM), C, C);
     tile_to_smem_async(s.B, PC, reinterpret_cast<const float*>(img + ImgOff::BM), C, C);
     cp_async_commit();
-    prep_rows(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dW, s.beta,
-              nullptr, nullptr);
+    prep_compute(rr, nullptr, a_h, lb, L, h, nullptr, s.kt, s.v, s.dW, s.beta, nullptr, nullptr);
+    __syncthreads();
+    if (nxt < ntiles) fetch(nxt);
     __syncthreads();
     block_products(s.dW, nullptr, s.kt, nullptr, nullptr, &s.fa);
     __syncthreads();
@@ -212,6 +233,8 @@ __global__ void __launch_bounds__(256, 1)
         float acc = s.dbeta[tid];
         for (int j = 0; j < tid; ++j) acc += s.dT[tid * PC + j] * s.B[tid * PC + j];
         reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] = acc;
+    }
+    __syncthreads();   // shared tiles are rewritten by the next tile
     }
 }
 

@@ -1,5 +1,5 @@
-// Forward intra-chunk kernel: one CTA per (chunk, head), all chunks in
-// parallel. For the chunk's L <= 64 tokens it computes
+// Forward intra-chunk kernel: persistent CTAs (one per SM) over all
+// (chunk, head) tiles, in parallel. For the chunk's L <= 64 tokens it computes
 //   q^, k^ (L2 norm, eps 1e-6), beta = sigmoid(beta_raw),
 //   alpha = exp(g), g = lb * sigmoid(exp(A_log) (g_raw + dt_bias))   per key channel,
 //   the decays between rows from products of alpha inside 16-row sub-blocks,
@@ -52,19 +52,39 @@ __global__ void __launch_bounds__(256, 1)
     extern __shared__ uint8_t smem_raw[];
     IntraSmem& s = *reinterpret_cast<IntraSmem*>(smem_raw);
     if (read_status(ws) != 0) return;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
-    if (ci.L <= 0) return;
-    const int t0 = ci.t0, L = ci.L;
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int ntiles = (int)lay.nc_max * H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const float a_h = __expf(A_log[h]);
-    const size_t tile = (size_t)chunk * H + h;
+    // Persistent: this CTA takes tiles blockIdx.x, + gridDim.x, ... (tile = chunk * H + h).
+    // The rows of the next tile are loaded into registers while the current one computes.
+    RowRegs rr;
+    // chunk records are read two tiles ahead so the row loads never wait on them
+    const int step = (int)gridDim.x;
+    auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
+    ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
+    auto fetch = [&](int t) {   // t: the tile whose record is ci_next
+        if (ci_next.L > 0) prep_load(rr, q, k, v, g_raw, beta_raw, ci_next.t0, ci_next.L, H, t % H, A_log, dt_bias);
+    };
+    if ((int)blockIdx.x < ntiles) fetch(blockIdx.x);
+    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
+    const ChunkInfo ci = ci_next;
+    const int h = tile_i % H;
+    const int nxt = tile_i + step;
+    ci_next = ci_next2;                        // record of tile nxt
+    ci_next2 = chunk_of(nxt + step);
+    if (ci.L <= 0) {
+        if (nxt < ntiles) fetch(nxt);
+        continue;
+    }
+    const int L = ci.L;
+    const float a_h = __expf(rr.alog);
+    const size_t tile = (size_t)tile_i;
     uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
 
-    prep_rows(q, k, v, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, s.v, s.kp, s.beta, nullptr,
-              nullptr);
+    prep_compute(rr, nullptr, a_h, lb, L, h, s.qe, s.ke, s.v, s.kp, s.beta, nullptr, nullptr);
     __syncthreads();
+    if (nxt < ntiles) fetch(nxt);
     block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);
     // zero the blocks above the diagonal of A, Aqk, X
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
@@ -87,19 +107,27 @@ __global__ void __launch_bounds__(256, 1)
         const float* base = m == 0 ? s.ke : s.qe;
         const float* f = s.fa.F[I][J];
         float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+        float acc2[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};   // second chain: odd k-steps
         const int r0 = I * SUB + gid, r1 = r0 + 8;
-#pragma unroll 4
-        for (int ks = 0; ks < D / 8; ++ks) {
-            const int k0 = ks * 8 + tig, k1 = k0 + 4;
-            const float f0 = f[k0], f1 = f[k1];
-            const Frag4 af = frag4(base[r0 * P + k0] * f0, base[r1 * P + k0] * f0, base[r0 * P + k1] * f1,
-                                   base[r1 * P + k1] * f1);
+#pragma unroll 2
+        for (int ks = 0; ks < D / 8; ks += 2) {
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int j = J * SUB + nt * 8 + gid;
-                mma3(acc[nt], af, frag2(s.kp[j * P + k0], s.kp[j * P + k1]));
+            for (int u = 0; u < 2; ++u) {
+                const int k0 = (ks + u) * 8 + tig, k1 = k0 + 4;
+                const float f0 = f[k0], f1 = f[k1];
+                const Frag4 af = frag4(base[r0 * P + k0] * f0, base[r1 * P + k0] * f0, base[r0 * P + k1] * f1,
+                                       base[r1 * P + k1] * f1);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int j = J * SUB + nt * 8 + gid;
+                    mma3(u == 0 ? acc[nt] : acc2[nt], af, frag2(s.kp[j * P + k0], s.kp[j * P + k1]));
+                }
             }
         }
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -132,29 +160,59 @@ __global__ void __launch_bounds__(256, 1)
         }
     }
     __syncthreads();
-    // off-diagonal blocks, by distance from the diagonal:
+    // off-diagonal blocks, by distance d from the diagonal (the tasks of a level
+    // run on separate warps; split-tf32 products keep fp32-level accuracy):
     //   X_IJ = -X_II * sum_{J <= K' < I} A_IK' X_K'J
-    float* Y = s.T;   // scratch [16][16]
     for (int d = 1; d < NSUB; ++d) {
-        for (int J = 0; J + d < NSUB; ++J) {
-            const int I = J + d;
-            const int r = tid >> 4, cc = tid & 15;
-            float y = 0.0f;
-            for (int m2 = J * SUB; m2 < I * SUB; ++m2) y += s.A[(I * SUB + r) * PA + m2] * s.X[m2 * PA + J * SUB + cc];
-            Y[r * SUB + cc] = y;
-            __syncthreads();
-            float acc = 0.0f;
-            for (int m2 = 0; m2 <= r; ++m2) acc += s.X[(I * SUB + r) * PA + I * SUB + m2] * Y[m2 * SUB + cc];
-            s.X[(I * SUB + r) * PA + J * SUB + cc] = -acc;
-            __syncthreads();
+        if (warp < NSUB - d) {
+            const int J = warp, I = J + d;
+            float* Y = s.T + warp * SUB * PA;   // per-warp [16][16] scratch (T is not yet in use)
+            float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+            const int r0 = I * SUB + gid, r1 = r0 + 8;
+            for (int ks = 2 * J; ks < 2 * I; ++ks) {
+                const int m0 = ks * 8 + tig, m1 = m0 + 4;
+                const Frag4 af = frag4(s.A[r0 * PA + m0], s.A[r1 * PA + m0], s.A[r0 * PA + m1], s.A[r1 * PA + m1]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int cc = J * SUB + nt * 8 + gid;
+                    mma3(acc[nt], af, frag2(s.X[m0 * PA + cc], s.X[m1 * PA + cc]));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) Y[(gid + (e >> 1) * 8) * PA + nt * 8 + tig * 2 + (e & 1)] = acc[nt][e];
+            __syncwarp();
+            float xr[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+                const int m0 = ks * 8 + tig, m1 = m0 + 4;
+                const Frag4 af = frag4(s.X[r0 * PA + I * SUB + m0], s.X[r1 * PA + I * SUB + m0],
+                                       s.X[r0 * PA + I * SUB + m1], s.X[r1 * PA + I * SUB + m1]);
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int cc = nt * 8 + gid;
+                    mma3(xr[nt], af, frag2(Y[m0 * PA + cc], Y[m1 * PA + cc]));
+                }
+            }
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    s.X[(I * SUB + gid + (e >> 1) * 8) * PA + J * SUB + nt * 8 + tig * 2 + (e & 1)] = -xr[nt][e];
         }
+        __syncthreads();
     }
     // T = X diag(beta); X and the zero upper blocks of B to the workspace
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
         const int r = idx >> 6, cc = idx & 63;
         s.T[r * PA + cc] = s.X[r * PA + cc] * s.beta[cc];
-        reinterpret_cast<float*>(img + ImgOff::XM)[idx] = s.X[r * PA + cc];
-        if ((cc >> 4) > (r >> 4)) reinterpret_cast<float*>(img + ImgOff::BM)[idx] = 0.0f;
+    }
+    for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
+        const int r = idx >> 4, cc = (idx & 15) * 4;
+        *reinterpret_cast<float4*>(img + ImgOff::XM + (r * C + cc) * 4) = *reinterpret_cast<const float4*>(&s.X[r * PA + cc]);
+        if ((cc >> 4) > (r >> 4))
+            *reinterpret_cast<float4*>(img + ImgOff::BM + (r * C + cc) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
     __syncthreads();
 
@@ -195,26 +253,45 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G), Aqk, and their transposes
-    for (int idx = tid; idx < C * D; idx += blockDim.x) {
-        const int r = idx >> 7, c = idx & 127;          // [64][128] row-major walk
-        const float qb = tf32_round(s.qe[r * P + c] * s.fa.Pb[r >> 4][c]);
-        const float kb = tf32_round(s.kp[r * P + c] * s.fa.Sf[r >> 4][c]);
-        *reinterpret_cast<float*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
-        *reinterpret_cast<float*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
+    //      (16-byte stores: a 16-byte chunk of a panel row is 4 consecutive columns)
+    for (int idx = tid; idx < C * D / 4; idx += blockDim.x) {
+        const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
+        const float* pb = s.fa.Pb[r >> 4];
+        const float* sf = s.fa.Sf[r >> 4];
+        float4 qb, kb;
+        qb.x = tf32_round(s.qe[r * P + c] * pb[c]);         kb.x = tf32_round(s.kp[r * P + c] * sf[c]);
+        qb.y = tf32_round(s.qe[r * P + c + 1] * pb[c + 1]); kb.y = tf32_round(s.kp[r * P + c + 1] * sf[c + 1]);
+        qb.z = tf32_round(s.qe[r * P + c + 2] * pb[c + 2]); kb.z = tf32_round(s.kp[r * P + c + 2] * sf[c + 2]);
+        qb.w = tf32_round(s.qe[r * P + c + 3] * pb[c + 3]); kb.w = tf32_round(s.kp[r * P + c + 3] * sf[c + 3]);
+        *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
+        *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
     }
-    for (int idx = tid; idx < C * D; idx += blockDim.x) {
-        const int kk = idx >> 6, c = idx & 63;           // [128][64] row-major walk
-        const float qb = tf32_round(scale * (s.qe[c * P + kk] * s.fa.Pb[c >> 4][kk]));
-        const float kb = tf32_round(s.kp[c * P + kk] * s.fa.Sf[c >> 4][kk]);
-        *reinterpret_cast<float*>(img + ImgOff::QBT + panel_off(kk, c, D)) = qb;
-        *reinterpret_cast<float*>(img + ImgOff::KBT + panel_off(kk, c, D)) = kb;
+    for (int idx = tid; idx < C * D / 4; idx += blockDim.x) {
+        const int kk = idx >> 4, c = (idx & 15) * 4;         // [128][64], 4 columns (rows of the source) per thread
+        float4 qb, kb;
+        float* qp = &qb.x;
+        float* kp = &kb.x;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            qp[e] = tf32_round(scale * (s.qe[(c + e) * P + kk] * s.fa.Pb[(c + e) >> 4][kk]));
+            kp[e] = tf32_round(s.kp[(c + e) * P + kk] * s.fa.Sf[(c + e) >> 4][kk]);
+        }
+        *reinterpret_cast<float4*>(img + ImgOff::QBT + panel_off(kk, c, D)) = qb;
+        *reinterpret_cast<float4*>(img + ImgOff::KBT + panel_off(kk, c, D)) = kb;
     }
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int r = idx >> 6, c = idx & 63;
-        *reinterpret_cast<float*>(img + ImgOff::AQK + panel_off(r, c, C)) = tf32_round(s.Aqk[r * PA + c]);
-        *reinterpret_cast<float*>(img + ImgOff::AQKT + panel_off(r, c, C)) = tf32_round(scale * s.Aqk[c * PA + r]);
+    for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
+        const int r = idx >> 4, c = (idx & 15) * 4;
+        const float4 a = make_float4(tf32_round(s.Aqk[r * PA + c]), tf32_round(s.Aqk[r * PA + c + 1]),
+                                     tf32_round(s.Aqk[r * PA + c + 2]), tf32_round(s.Aqk[r * PA + c + 3]));
+        const float4 at = make_float4(tf32_round(scale * s.Aqk[c * PA + r]), tf32_round(scale * s.Aqk[(c + 1) * PA + r]),
+                                      tf32_round(scale * s.Aqk[(c + 2) * PA + r]),
+                                      tf32_round(scale * s.Aqk[(c + 3) * PA + r]));
+        *reinterpret_cast<float4*>(img + ImgOff::AQK + panel_off(r, c, C)) = a;
+        *reinterpret_cast<float4*>(img + ImgOff::AQKT + panel_off(r, c, C)) = at;
     }
     if (tid < D) reinterpret_cast<float*>(img + ImgOff::GAML)[tid] = s.fa.gl[tid];
+    __syncthreads();   // shared tiles are rewritten by the next tile
+    }
 }
 
 size_t fwd_intra_smem_bytes() { return sizeof(IntraSmem); }

@@ -29,74 +29,109 @@ struct Factors {
     float gl[D];
 };
 
-// Loads rows of one chunk (warp per row, lane per 4 channels). Any output
-// pointer may be null. xq/xk receive q^, k^; xv receives v; xa receives alpha;
-// beta[r], inq[r], ink[r] receive beta and 1/sqrt(|x|^2 + eps).
+// Raw bf16 rows of one chunk held in registers: warp w holds rows w + 8 b,
+// lane l channels 4l .. 4l+3 (8 warps).
+constexpr int PREP_WARPS = 8;
+constexpr int PREP_RB = C / PREP_WARPS;
+struct RowRegs {
+    uint2 q[PREP_RB], k[PREP_RB], v[PREP_RB], g[PREP_RB];
+    float br[PREP_RB];
+    float dt[4];     // dt_bias[h, 4 lane .. 4 lane + 3]
+    float alog;      // A_log[h]
+};
+
+// Issues the global loads of a chunk's rows (needs 8 warps). Only the tensors
+// whose pointer is non-null are loaded; the rest stay zero. A_log and dt_bias
+// (nullable) of head h are loaded too.
+__device__ __forceinline__ void prep_load(RowRegs& rr, const uint16_t* __restrict__ q,
+                                          const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                          const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
+                                          int t0, int L, int H, int h, const float* __restrict__ A_log = nullptr,
+                                          const float* __restrict__ dt_bias = nullptr) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = lane * 4;
+    rr.alog = A_log ? A_log[h] : 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rr.dt[e] = dt_bias ? dt_bias[h * D + c0 + e] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < PREP_RB; ++b) {
+        const int r = warp + b * PREP_WARPS;
+        rr.q[b] = rr.k[b] = rr.v[b] = rr.g[b] = make_uint2(0u, 0u);
+        rr.br[b] = 0.0f;
+        if (r < L) {
+            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
+            if (q) rr.q[b] = *reinterpret_cast<const uint2*>(q + base);
+            if (k) rr.k[b] = *reinterpret_cast<const uint2*>(k + base);
+            if (v) rr.v[b] = *reinterpret_cast<const uint2*>(v + base);
+            if (g_raw) rr.g[b] = *reinterpret_cast<const uint2*>(g_raw + base);
+            if (beta_raw && lane == 0) rr.br[b] = bf2f(beta_raw[(size_t)(t0 + r) * H + h]);
+        }
+    }
+}
+
+// Turns loaded rows into q^, k^, v, alpha, beta and 1/sqrt(|x|^2 + eps) in
+// shared memory (any output pointer may be null; rows >= L: zeros, alpha = 1,
+// beta = 0).
+__device__ __forceinline__ void prep_compute(const RowRegs& rr, const float* __restrict__ dt_bias, float a_h,
+                                             float lb, int L, int h, float* xq, float* xk, float* xv, float* xa,
+                                             float* beta, float* inq, float* ink) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = lane * 4;
+    float dtv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) dtv[e] = (xa && dt_bias) ? dt_bias[h * D + c0 + e] : rr.dt[e];
+    auto un = [](uint2 w, float* out) {
+        out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
+        out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
+    };
+    // squared norms of all rows first, then the reductions interleaved across rows
+    float sq[PREP_RB], sk[PREP_RB];
+#pragma unroll
+    for (int b = 0; b < PREP_RB; ++b) {
+        float qv[4], kv[4];
+        un(rr.q[b], qv); un(rr.k[b], kv);
+        sq[b] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
+        sk[b] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+        for (int b = 0; b < PREP_RB; ++b) {
+            sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], o);
+            sk[b] += __shfl_xor_sync(0xffffffffu, sk[b], o);
+        }
+#pragma unroll
+    for (int b = 0; b < PREP_RB; ++b) {
+        const int r = warp + b * PREP_WARPS;
+        float qv[4], kv[4], vv[4], gr[4], al[4] = {1, 1, 1, 1};
+        un(rr.q[b], qv); un(rr.k[b], kv); un(rr.v[b], vv); un(rr.g[b], gr);
+        if (xa && r < L) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dtv[e])));
+        }
+        const float iq = rsqrtf(sq[b] + 1e-6f), ik = rsqrtf(sk[b] + 1e-6f);
+        if (xq) *reinterpret_cast<float4*>(xq + r * PS + c0) = make_float4(qv[0] * iq, qv[1] * iq, qv[2] * iq, qv[3] * iq);
+        if (xk) *reinterpret_cast<float4*>(xk + r * PS + c0) = make_float4(kv[0] * ik, kv[1] * ik, kv[2] * ik, kv[3] * ik);
+        if (xv) *reinterpret_cast<float4*>(xv + r * PS + c0) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        if (xa) *reinterpret_cast<float4*>(xa + r * PS + c0) = make_float4(al[0], al[1], al[2], al[3]);
+        if (lane == 0) {
+            if (beta) beta[r] = r < L ? sigmoidf(rr.br[b]) : 0.0f;
+            if (inq) inq[r] = iq;
+            if (ink) ink[r] = ik;
+        }
+    }
+}
+
+// Loads and prepares rows of one chunk in one go (8 warps).
 __device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                           const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
                                           const uint16_t* __restrict__ beta_raw, const float* __restrict__ dt_bias,
                                           float a_h, float lb, int t0, int L, int H, int h, float* xq, float* xk,
                                           float* xv, float* xa, float* beta, float* inq, float* ink) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-    const int c0 = lane * 4;
-    const bool wq = xq || inq, wk = xk || ink;
-    float dtv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dtv[e] = xa ? dt_bias[h * D + c0 + e] : 0.0f;
-    constexpr int RB = C / 8;   // rows per batch of loads (all rows of a warp at 8 warps)
-    for (int rb0 = warp; rb0 < C; rb0 += nw * RB) {
-        uint2 wqv[RB], wkv[RB], wvv[RB], wgv[RB];
-        float brv[RB];
-#pragma unroll
-        for (int b = 0; b < RB; ++b) {
-            const int r = rb0 + b * nw;
-            wqv[b] = wkv[b] = wvv[b] = wgv[b] = make_uint2(0u, 0u);
-            brv[b] = 0.0f;
-            if (r < L) {
-                if (beta && lane == 0) brv[b] = bf2f(beta_raw[(size_t)(t0 + r) * H + h]);
-                const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-                if (wq) wqv[b] = *reinterpret_cast<const uint2*>(q + base);
-                if (wk) wkv[b] = *reinterpret_cast<const uint2*>(k + base);
-                if (xv) wvv[b] = *reinterpret_cast<const uint2*>(v + base);
-                if (xa) wgv[b] = *reinterpret_cast<const uint2*>(g_raw + base);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < RB; ++b) {
-            const int r = rb0 + b * nw;
-            if (r >= C) break;
-            auto un = [](uint2 w, float* out) {
-                out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
-                out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
-            };
-            float qv[4], kv[4], vv[4], gr[4], al[4] = {1, 1, 1, 1};
-            un(wqv[b], qv); un(wkv[b], kv); un(wvv[b], vv); un(wgv[b], gr);
-            if (xa && r < L) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dtv[e])));
-            }
-            float sq = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-            float sk = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                sq += __shfl_xor_sync(0xffffffffu, sq, o);
-                sk += __shfl_xor_sync(0xffffffffu, sk, o);
-            }
-            const float iq = 1.0f / sqrtf(sq + 1e-6f), ik = 1.0f / sqrtf(sk + 1e-6f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                if (xq) xq[r * PS + c0 + e] = qv[e] * iq;
-                if (xk) xk[r * PS + c0 + e] = kv[e] * ik;
-                if (xv) xv[r * PS + c0 + e] = vv[e];
-                if (xa) xa[r * PS + c0 + e] = al[e];
-            }
-            if (lane == 0) {
-                if (beta) beta[r] = r < L ? sigmoidf(brv[b]) : 0.0f;
-                if (inq) inq[r] = iq;
-                if (ink) ink[r] = ik;
-            }
-        }
-    }
+    RowRegs rr;
+    prep_load(rr, (xq || inq) ? q : nullptr, (xk || ink) ? k : nullptr, xv ? v : nullptr, xa ? g_raw : nullptr,
+              beta ? beta_raw : nullptr, t0, L, H, h);
+    prep_compute(rr, dt_bias, a_h, lb, L, h, xq, xk, xv, xa, beta, inq, ink);
 }
 
 // Block products. On entry `ap` holds alpha, `xq`/`xk` hold q^/k^ (either may
