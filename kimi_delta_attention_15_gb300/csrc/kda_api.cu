@@ -211,7 +211,7 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
             q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, shape->scale, ws, lay);
     prof(2, s);
     if (shape->N > 0)
-        kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, fwd_scan_smem_bytes(), s>>>(
+        kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, fwd_scan_smem_bytes(), s>>>(
             h0, o, hT, H, shape->scale, ws, lay);
     prof(3, s);
     return cuda_status(cudaGetLastError(), "kda_fwd launch");
@@ -245,7 +245,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     const dim3 tiles((unsigned)lay.nc_max, (unsigned)H);
     prof(4, s);
     if (shape->N > 0)
-        kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 128, bwd_scan_smem_bytes(), s>>>(
+        kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, bwd_scan_smem_bytes(), s>>>(
             do_, dhT, dh0, H, ws, lay);
     prof(5, s);
     if (lay.nc_max > 0)

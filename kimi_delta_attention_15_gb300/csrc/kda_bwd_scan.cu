@@ -29,7 +29,7 @@ struct BScanSmem {
 
 size_t bwd_scan_smem_bytes() { return sizeof(BScanSmem) + 1024; }
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     kda_bwd_scan_kernel(const uint16_t* __restrict__ dO, const float* __restrict__ dhT, float* __restrict__ dh0,
                         int H, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
@@ -41,7 +41,8 @@ __global__ void __launch_bounds__(128, 1)
     const int cl = reinterpret_cast<const int*>(ws + lay.seq_first)[n + 1];
     const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int v = tid;
+    // threads v and v + 128 own adjoint row v (TMEM lane v) and split its columns
+    const int v = tid & (D - 1), half = tid >> 7;
     const size_t sidx = ((size_t)n * H + h) * D * D;
 
     if (warp == 0) {
@@ -57,9 +58,9 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tm = s.tmem;
     const uint32_t tS = tm, tU = tm + 128;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
         float r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = dhT ? dhT[sidx + (size_t)v * D + c0 + j] : 0.0f;
@@ -82,13 +83,14 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t idN64 = idesc_tf32(128, 64, 0, 0);
     const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
     // dO, exp(G_L) and the chunk record are fetched one chunk ahead
-    uint32_t don[C / 2];
+    uint32_t don[C / 4];   // this thread's 32 rows i of dO (column v), two bf16 per word
     auto fetch_dO = [&](const ChunkInfo& c2) {
 #pragma unroll
-        for (int i = 0; i < C; i += 2) {
+        for (int ii = 0; ii < C / 2; ii += 2) {
+            const int i = 32 * half + ii;
             const uint32_t lo = i < c2.L ? dO[((size_t)(c2.t0 + i) * H + h) * D + v] : 0u;
             const uint32_t hi = i + 1 < c2.L ? dO[((size_t)(c2.t0 + i + 1) * H + h) * D + v] : 0u;
-            don[i >> 1] = lo | (hi << 16);
+            don[ii >> 1] = lo | (hi << 16);
         }
     };
     ChunkInfo ci_next = cf < cl ? chunks[cl - 1] : ChunkInfo{0, 0, 0, 0};
@@ -97,23 +99,23 @@ __global__ void __launch_bounds__(128, 1)
     for (int chunk = cl - 1; chunk >= cf && ok; --chunk) {
         const uint32_t par = (uint32_t)((cl - 1 - chunk) & 1);
         const size_t tile = (size_t)chunk * H + h;
-        s.gam[v] = gam_next;
+        if (half == 0) s.gam[v] = gam_next;
         if (tid == 0) bulk_wait_read_all();   // previous dS checkpoint copy done reading DS
         __syncthreads();
         // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
         // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
 #pragma unroll
-        for (int i = 0; i < C; i += 4)
-            *reinterpret_cast<float4*>(s.DOT + panel_off(v, i, D)) =
-                make_float4(bf2f((uint16_t)(don[i >> 1] & 0xffffu)), bf2f((uint16_t)(don[i >> 1] >> 16)),
-                            bf2f((uint16_t)(don[(i >> 1) + 1] & 0xffffu)), bf2f((uint16_t)(don[(i >> 1) + 1] >> 16)));
+        for (int ii = 0; ii < C / 2; ii += 4)
+            *reinterpret_cast<float4*>(s.DOT + panel_off(v, 32 * half + ii, D)) =
+                make_float4(bf2f((uint16_t)(don[ii >> 1] & 0xffffu)), bf2f((uint16_t)(don[ii >> 1] >> 16)),
+                            bf2f((uint16_t)(don[(ii >> 1) + 1] & 0xffffu)), bf2f((uint16_t)(don[(ii >> 1) + 1] >> 16)));
         if (chunk - 1 >= cf) {
             ci_next = chunks[chunk - 1];
             gam_next = reinterpret_cast<const float*>(img_of(chunk - 1) + ImgOff::GAML)[v];
             fetch_dO(ci_next);
         }
         // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
@@ -155,7 +157,8 @@ __global__ void __launch_bounds__(128, 1)
 
         // -dUt^T into the operand tile (reusing DOT); dUt (fp32) -> workspace [c][v] panels
         uint8_t* gdU = ws + lay.dut + tile * kTileCK;
-        for (int c0 = 0; c0 < C; c0 += 32) {
+        {
+            const int c0 = 32 * half;
             float r[32];
             tmem_ld32(tU + lane_base + c0, r);
 #pragma unroll
@@ -182,7 +185,7 @@ __global__ void __launch_bounds__(128, 1)
     }
     if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
     if (ok && dh0) {
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll

@@ -32,7 +32,7 @@ struct ScanSmem {
 
 size_t fwd_scan_smem_bytes() { return sizeof(ScanSmem) + 1024; }
 
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     kda_fwd_scan_kernel(const float* __restrict__ h0, uint16_t* __restrict__ o, float* __restrict__ hT, int H,
                         float scale, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
@@ -44,7 +44,8 @@ __global__ void __launch_bounds__(128, 1)
     const int cl = reinterpret_cast<const int*>(ws + lay.seq_first)[n + 1];
     const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int v = tid;   // state row / TMEM lane owned by this thread
+    // threads v and v + 128 own state row v (TMEM lane v) and split its columns
+    const int v = tid & (D - 1), half = tid >> 7;
     const size_t sidx = ((size_t)n * H + h) * D * D;
 
     if (warp == 0) {
@@ -60,10 +61,10 @@ __global__ void __launch_bounds__(128, 1)
     tc_fence_after();
     const uint32_t tm = s.tmem;
     const uint32_t tS = tm, tUT = tm + 128, tOT = tm + 192;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     // initial state into TMEM
-    for (int c0 = 0; c0 < D; c0 += 32) {
+    for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
         float r[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = h0 ? h0[sidx + (size_t)v * D + c0 + j] : 0.0f;
@@ -97,7 +98,7 @@ __global__ void __launch_bounds__(128, 1)
         const size_t tile = (size_t)chunk * H + h;
         const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
         const float* gU = reinterpret_cast<const float*>(img + ImgOff::U);
-        s.gam[v] = gam_next;
+        if (half == 0) s.gam[v] = gam_next;
         if (chunk + 1 < cl) {
             ci_next = chunks[chunk + 1];
             gam_next = reinterpret_cast<const float*>(img + (size_t)H * ImgOff::BYTES + ImgOff::GAML)[v];  // chunk + 1
@@ -106,7 +107,7 @@ __global__ void __launch_bounds__(128, 1)
         __syncthreads();
 
         // S0: TMEM -> registers -> tf32 operand in smem; decayed state back to TMEM
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
@@ -139,9 +140,9 @@ __global__ void __launch_bounds__(128, 1)
             }
         }
         // U column v of this chunk
-        float u[C];
+        float u[32];
 #pragma unroll
-        for (int c = 0; c < C; ++c) u[c] = gU[c * D + v];
+        for (int c = 0; c < 32; ++c) u[c] = gU[(32 * half + c) * D + v];
         ok = mbar_wait(&s.barM1, par) && ok;
         ok = __syncthreads_and(ok);
         if (!ok) break;
@@ -150,11 +151,12 @@ __global__ void __launch_bounds__(128, 1)
 
         // Ut^T = U^T - S0 W^T  -> tf32 operand [v][c]; Ut (fp32) -> workspace [c][v] panels
         uint8_t* gUt = ws + lay.ut + tile * kTileCK;
-        for (int c0 = 0; c0 < C; c0 += 32) {
+        {
+            const int c0 = 32 * half;
             float r[32];
             tmem_ld32(tUT + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = u[c0 + j] - r[j];
+            for (int j = 0; j < 32; ++j) r[j] = u[j] - r[j];
 #pragma unroll
             for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gUt + panel_off(c0 + j, v, C)) = r[j];
 #pragma unroll
@@ -185,7 +187,8 @@ __global__ void __launch_bounds__(128, 1)
         if (tid == 0 && chunk + 1 < cl) { issue_B(chunk + 1); ++b_issued; }
 
         // o = scale * O
-        for (int c0 = 0; c0 < C; c0 += 32) {
+        {
+            const int c0 = 32 * half;
             float r[32];
             tmem_ld32(tOT + lane_base + c0, r);
 #pragma unroll
@@ -199,7 +202,7 @@ __global__ void __launch_bounds__(128, 1)
 
     // final state
     if (ok && hT) {
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
