@@ -6,7 +6,7 @@
 // which is the reverse mode of the chunk form
 //   Ut = U - W S0^T,  O = scale[(Q^*Gamma) S0^T + Aqk Ut],
 //   S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
-// dS_L of every chunk (tf32, as the MMAs use it) and dUt (fp32) are stored in the
+// dS_L^T of every chunk (tf32, as the MMAs use it) and dUt (fp32) are stored in the
 // workspace for the per-chunk backward kernels; dh0 = dS at the sequence start.
 #include "kda_internal.cuh"
 #include "umma.cuh"
@@ -100,7 +100,6 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t par = (uint32_t)((cl - 1 - chunk) & 1);
         const size_t tile = (size_t)chunk * H + h;
         if (half == 0) s.gam[v] = gam_next;
-        if (tid == 0) bulk_wait_read_all();   // previous dS checkpoint copy done reading DS
         __syncthreads();
         // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
         // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
@@ -114,14 +113,22 @@ __global__ void __launch_bounds__(256, 1)
             gam_next = reinterpret_cast<const float*>(img_of(chunk - 1) + ImgOff::GAML)[v];
             fetch_dO(ci_next);
         }
-        // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
+        // dS_L: TMEM -> tf32 operand, and dS_L^T [k][v] (tf32) to the workspace
+        // checkpoint; dS_L diag(exp(G_L)) back to TMEM
+        uint8_t* gDST = ws + lay.ds + tile * kTileDD;
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) =
-                    make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]), tf32_round(r[j + 3]));
+            for (int j = 0; j < 32; j += 4) {
+                const float4 q4 = make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]),
+                                              tf32_round(r[j + 3]));
+                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) = q4;
+                *reinterpret_cast<float*>(gDST + panel_off(c0 + j, v, D)) = q4.x;
+                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 1, v, D)) = q4.y;
+                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 2, v, D)) = q4.z;
+                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 3, v, D)) = q4.w;
+            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
             tmem_st32(tS + lane_base + c0, r);
@@ -131,8 +138,6 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         tc_fence_after();
         if (tid == 0) {
-            bulk_s2g(ws + lay.ds + tile * kTileDD, s.DS, (uint32_t)kTileDD);
-            bulk_commit();
             const bool gx = mbar_wait(&s.barX, par), gy = gx && mbar_wait(&s.barY, par);
             x_done += gx; y_done += gy;
             if (!gx || !gy) ok = false;

@@ -1,6 +1,6 @@
 // Backward, state-side products of each chunk: one CTA per (chunk, head), all
-// chunks in parallel. From the checkpoints S0 (forward) and dS_L (backward
-// scan), and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over
+// chunks in parallel. From the checkpoints S0^T (forward) and dS_L^T (backward
+// scan), stored key-major by the scans, and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over
 // the key channel k):
 //   dQbar = scale dO S0            [c][k]
 //   dW    = -dUt S0                [c][k]
@@ -21,7 +21,7 @@ struct BStateSmem {
     uint8_t DST[kTileDD];    // dS_L^T [128 k][128 v]
     uint8_t STK[kTileDD];    // rows 0..63: dO [c][v]; rows 64..127: dUt [c][v]
     uint8_t UT[kTileCK];     // Ut [64 c][128 v]
-    uint64_t bar, barM;
+    uint64_t bar, barC, barM;
     uint32_t tmem;
 };
 }  // namespace
@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(256, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&s.bar, 1); mbar_init(&s.barM, 1);
+        mbar_init(&s.bar, 1); mbar_init(&s.barC, 1); mbar_init(&s.barM, 1);
         fence_mbar_init();
     }
     __syncthreads();
@@ -75,7 +75,13 @@ __global__ void __launch_bounds__(256, 1)
         }
     };
     load_u(0);
-    // transposed checkpoints: threads (v, half) read half of row v of S0 / dS_L, write column v
+    // checkpoints S0^T and dS_L^T arrive in operand layout by bulk copy
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&s.barC, (uint32_t)(2 * kTileDD));
+        bulk_g2s(s.S0T, gS0, (uint32_t)kTileDD, &s.barC);
+        bulk_g2s(s.DST, gDS, (uint32_t)kTileDD, &s.barC);
+    }
+    // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
     {
         const int v = tid & (D - 1), half = tid >> 7;
         uint16_t dov[C / 2];
@@ -85,33 +91,11 @@ __global__ void __launch_bounds__(256, 1)
             dov[i] = c < ci.L ? dO[((size_t)(ci.t0 + c) * H + h) * D + v] : (uint16_t)0;
         }
 #pragma unroll
-        for (int c0 = half * 64; c0 < half * 64 + 64; c0 += 32) {
-            float4 a[8], b[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                a[j] = *reinterpret_cast<const float4*>(gS0 + panel_off(v, c0 + 4 * j, D));
-                b[j] = *reinterpret_cast<const float4*>(gDS + panel_off(v, c0 + 4 * j, D));
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int cc = c0 + 4 * j;
-                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 0, v, D)) = a[j].x;
-                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 1, v, D)) = a[j].y;
-                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 2, v, D)) = a[j].z;
-                *reinterpret_cast<float*>(s.S0T + panel_off(cc + 3, v, D)) = a[j].w;
-                *reinterpret_cast<float*>(s.DST + panel_off(cc + 0, v, D)) = b[j].x;
-                *reinterpret_cast<float*>(s.DST + panel_off(cc + 1, v, D)) = b[j].y;
-                *reinterpret_cast<float*>(s.DST + panel_off(cc + 2, v, D)) = b[j].z;
-                *reinterpret_cast<float*>(s.DST + panel_off(cc + 3, v, D)) = b[j].w;
-            }
-        }
-        // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
-#pragma unroll
         for (int i = 0; i < C / 2; ++i)
             *reinterpret_cast<float*>(s.STK + panel_off(half * (C / 2) + i, v, D)) = bf2f(dov[i]);
     }
     const uint32_t tm = s.tmem;
-    bool ok = mbar_wait(&s.bar, 0);
+    bool ok = mbar_wait(&s.bar, 0) && mbar_wait(&s.barC, 0);
     ok = __syncthreads_and(ok);
     if (ok) split_u(false);
     fence_async_smem();

@@ -9,7 +9,8 @@
 // (chunk form of S_t = S_{t-1} diag(e^{g_t}) (I - b k^ k^T) + b v k^T,
 //  o_t = scale S_t q^_t; flashinfer "kda_backward" contract). S0 of every
 // chunk, rounded to tf32 as the MMAs use it, is checkpointed to the
-// workspace for the backward, together with Ut (fp32).
+// workspace for the backward as S0^T (key-major panels, the operand layout the
+// backward's state products use), together with Ut (fp32).
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
@@ -103,10 +104,11 @@ __global__ void __launch_bounds__(256, 1)
             ci_next = chunks[chunk + 1];
             gam_next = reinterpret_cast<const float*>(img + (size_t)H * ImgOff::BYTES + ImgOff::GAML)[v];  // chunk + 1
         }
-        if (tid == 0) bulk_wait_read_all();   // previous checkpoint copy finished reading S0
         __syncthreads();
 
-        // S0: TMEM -> registers -> tf32 operand in smem; decayed state back to TMEM
+        // S0: TMEM -> registers -> tf32 operand in smem, and its transpose S0^T [k][v]
+        // (tf32) to the workspace checkpoint; decayed state back to TMEM
+        uint8_t* gS0T = ws + lay.s0 + tile * kTileDD;
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
@@ -115,6 +117,10 @@ __global__ void __launch_bounds__(256, 1)
                 const float4 q4 = make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]),
                                               tf32_round(r[j + 3]));
                 *reinterpret_cast<float4*>(s.S0 + panel_off(v, c0 + j, D)) = q4;
+                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j, v, D)) = q4.x;
+                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 1, v, D)) = q4.y;
+                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 2, v, D)) = q4.z;
+                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 3, v, D)) = q4.w;
             }
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
@@ -126,8 +132,6 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
 
         if (tid == 0) {
-            bulk_s2g(ws + lay.s0 + tile * kTileDD, s.S0, (uint32_t)kTileDD);
-            bulk_commit();
             if (!mbar_wait(&s.barA, par)) ok = false;
             else ++a_done;
             if (ok) {

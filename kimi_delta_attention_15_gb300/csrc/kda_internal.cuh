@@ -106,9 +106,9 @@ __host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, i
     l.seq_first = o;   o = align_up(o + (size_t)(N + 1) * 4, 1024);
     l.seq_order = o;   o = align_up(o + (size_t)(N + 1) * 4, 1024);
     l.img = o;         o += (size_t)tiles * ImgOff::BYTES;
-    l.s0 = o;          o += (size_t)tiles * kTileDD;
+    l.s0 = o;          o += (size_t)tiles * kTileDD;   // S0^T  [128 k][128 v] panels (tf32)
     l.ut = o;          o += (size_t)tiles * kTileCK;
-    l.ds = o;          o += (size_t)tiles * kTileDD;
+    l.ds = o;          o += (size_t)tiles * kTileDD;   // dS_L^T [128 k][128 v] panels (tf32)
     l.dut = o;         o += (size_t)tiles * kTileCK;
     l.bg = o;          o += (size_t)tiles * BgOff::BYTES;
     l.wy = o;          o += (size_t)tiles * WyOff::BYTES;
