@@ -207,7 +207,7 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
-        kda_fwd_intra_kernel<<<persistent_grid(lay.nc_max * H), 256, fwd_intra_smem_bytes(), s>>>(
+        kda_fwd_intra_kernel<<<persistent_grid(lay.nc_max * H), 512, fwd_intra_smem_bytes(), s>>>(
             q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, shape->scale, ws, lay);
     prof(2, s);
     if (shape->N > 0)

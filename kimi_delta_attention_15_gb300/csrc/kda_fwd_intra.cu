@@ -43,7 +43,9 @@ struct IntraSmem {
 
 }  // namespace
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int kIntraWarps = 16;
+
+__global__ void __launch_bounds__(kIntraWarps * 32, 1)
     kda_fwd_intra_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
                          const uint16_t* __restrict__ beta_raw, const float* __restrict__ A_log,
@@ -58,33 +60,25 @@ __global__ void __launch_bounds__(256, 1)
     const int gid = lane >> 2, tig = lane & 3;
     // Persistent: this CTA takes tiles blockIdx.x, + gridDim.x, ... (tile = chunk * H + h).
     // The rows of the next tile are loaded into registers while the current one computes.
-    RowRegs rr;
-    // chunk records are read two tiles ahead so the row loads never wait on them
+    // chunk records are read two tiles ahead
     const int step = (int)gridDim.x;
     auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
     ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
-    auto fetch = [&](int t) {   // t: the tile whose record is ci_next
-        if (ci_next.L > 0) prep_load(rr, q, k, v, g_raw, beta_raw, ci_next.t0, ci_next.L, H, t % H, A_log, dt_bias);
-    };
-    if ((int)blockIdx.x < ntiles) fetch(blockIdx.x);
     for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
     const ChunkInfo ci = ci_next;
     const int h = tile_i % H;
     const int nxt = tile_i + step;
-    ci_next = ci_next2;                        // record of tile nxt
+    ci_next = ci_next2;
     ci_next2 = chunk_of(nxt + step);
-    if (ci.L <= 0) {
-        if (nxt < ntiles) fetch(nxt);
-        continue;
-    }
+    if (ci.L <= 0) continue;
     const int L = ci.L;
-    const float a_h = __expf(rr.alog);
+    const float a_h = __expf(A_log[h]);
     const size_t tile = (size_t)tile_i;
     uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
 
-    prep_compute(rr, nullptr, a_h, lb, L, h, s.qe, s.ke, s.v, s.kp, s.beta, nullptr, nullptr);
+    prep_rows<kIntraWarps>(q, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, s.qe, s.ke, s.v, s.kp,
+                           s.beta, nullptr, nullptr);
     __syncthreads();
-    if (nxt < ntiles) fetch(nxt);
     block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);
     // zero the blocks above the diagonal of A, Aqk, X
     for (int idx = tid; idx < C * C; idx += blockDim.x) {
@@ -100,7 +94,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
 
     // ---- pairwise decayed products, 16x16 blocks (I >= J), tf32 mma.sync
-    for (int task = warp; task < 20; task += 8) {
+    for (int task = warp; task < 20; task += kIntraWarps) {
         const int m = task / 10;
         int I, J;
         tri_pair(task % 10, I, J);
@@ -216,12 +210,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();
 
-    // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 64ch..)
+    // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 32ch..)
     {
         const int rb = warp & 3, ch = warp >> 2;
-        float aw[8][4], au[8][4];
+        float aw[4][4], au[4][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) { aw[nt][e] = 0.0f; au[nt][e] = 0.0f; }
         const int ra = rb * SUB + gid, rbb = ra + 8;
@@ -230,8 +224,8 @@ __global__ void __launch_bounds__(256, 1)
             const Frag4 tf = frag4(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
             const float* pb = s.fa.Pb[j0 >> 4];
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int c = ch * 64 + nt * 8 + gid;
+            for (int nt = 0; nt < 4; ++nt) {
+                const int c = ch * 32 + nt * 8 + gid;
                 mma3(aw[nt], tf, frag2(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
                 // v is bf16 data, exact in tf32
                 mma2a(au[nt], tf, tf32_bits(s.v[j0 * P + c]), tf32_bits(s.v[j1 * P + c]));
@@ -239,11 +233,11 @@ __global__ void __launch_bounds__(256, 1)
         }
         float* gU = reinterpret_cast<float*>(img + ImgOff::U);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int row = rb * SUB + gid + hh * 8;
-                const int col = ch * 64 + nt * 8 + tig * 2;
+                const int col = ch * 32 + nt * 8 + tig * 2;
                 const float w0 = tf32_round(aw[nt][hh * 2]), w1 = tf32_round(aw[nt][hh * 2 + 1]);
                 *reinterpret_cast<float2*>(img + ImgOff::W + panel_off(row, col, C)) = make_float2(w0, w1);
                 *reinterpret_cast<float*>(img + ImgOff::WT + panel_off(col, row, D)) = w0;

@@ -29,21 +29,23 @@ struct Factors {
     float gl[D];
 };
 
-// Raw bf16 rows of one chunk held in registers: warp w holds rows w + 8 b,
-// lane l channels 4l .. 4l+3 (8 warps).
-constexpr int PREP_WARPS = 8;
-constexpr int PREP_RB = C / PREP_WARPS;
-struct RowRegs {
-    uint2 q[PREP_RB], k[PREP_RB], v[PREP_RB], g[PREP_RB];
-    float br[PREP_RB];
+// Raw bf16 rows of one chunk held in registers: with NW warps, warp w holds
+// rows w + NW b, lane l channels 4l .. 4l+3.
+template <int NW>
+struct RowRegsT {
+    static constexpr int RB = C / NW;
+    uint2 q[RB], k[RB], v[RB], g[RB];
+    float br[RB];
     float dt[4];     // dt_bias[h, 4 lane .. 4 lane + 3]
     float alog;      // A_log[h]
 };
+using RowRegs = RowRegsT<8>;
 
-// Issues the global loads of a chunk's rows (needs 8 warps). Only the tensors
+// Issues the global loads of a chunk's rows (NW warps). Only the tensors
 // whose pointer is non-null are loaded; the rest stay zero. A_log and dt_bias
 // (nullable) of head h are loaded too.
-__device__ __forceinline__ void prep_load(RowRegs& rr, const uint16_t* __restrict__ q,
+template <int NW>
+__device__ __forceinline__ void prep_load(RowRegsT<NW>& rr, const uint16_t* __restrict__ q,
                                           const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                           const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
                                           int t0, int L, int H, int h, const float* __restrict__ A_log = nullptr,
@@ -54,8 +56,8 @@ __device__ __forceinline__ void prep_load(RowRegs& rr, const uint16_t* __restric
 #pragma unroll
     for (int e = 0; e < 4; ++e) rr.dt[e] = dt_bias ? dt_bias[h * D + c0 + e] : 0.0f;
 #pragma unroll
-    for (int b = 0; b < PREP_RB; ++b) {
-        const int r = warp + b * PREP_WARPS;
+    for (int b = 0; b < RowRegsT<NW>::RB; ++b) {
+        const int r = warp + b * NW;
         rr.q[b] = rr.k[b] = rr.v[b] = rr.g[b] = make_uint2(0u, 0u);
         rr.br[b] = 0.0f;
         if (r < L) {
@@ -72,7 +74,8 @@ __device__ __forceinline__ void prep_load(RowRegs& rr, const uint16_t* __restric
 // Turns loaded rows into q^, k^, v, alpha, beta and 1/sqrt(|x|^2 + eps) in
 // shared memory (any output pointer may be null; rows >= L: zeros, alpha = 1,
 // beta = 0).
-__device__ __forceinline__ void prep_compute(const RowRegs& rr, const float* __restrict__ dt_bias, float a_h,
+template <int NW>
+__device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, const float* __restrict__ dt_bias, float a_h,
                                              float lb, int L, int h, float* xq, float* xk, float* xv, float* xa,
                                              float* beta, float* inq, float* ink) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -85,9 +88,10 @@ __device__ __forceinline__ void prep_compute(const RowRegs& rr, const float* __r
         out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
     };
     // squared norms of all rows first, then the reductions interleaved across rows
-    float sq[PREP_RB], sk[PREP_RB];
+    constexpr int RB = RowRegsT<NW>::RB;
+    float sq[RB], sk[RB];
 #pragma unroll
-    for (int b = 0; b < PREP_RB; ++b) {
+    for (int b = 0; b < RB; ++b) {
         float qv[4], kv[4];
         un(rr.q[b], qv); un(rr.k[b], kv);
         sq[b] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
@@ -96,13 +100,13 @@ __device__ __forceinline__ void prep_compute(const RowRegs& rr, const float* __r
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int b = 0; b < PREP_RB; ++b) {
+        for (int b = 0; b < RB; ++b) {
             sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], o);
             sk[b] += __shfl_xor_sync(0xffffffffu, sk[b], o);
         }
 #pragma unroll
-    for (int b = 0; b < PREP_RB; ++b) {
-        const int r = warp + b * PREP_WARPS;
+    for (int b = 0; b < RB; ++b) {
+        const int r = warp + b * NW;
         float qv[4], kv[4], vv[4], gr[4], al[4] = {1, 1, 1, 1};
         un(rr.q[b], qv); un(rr.k[b], kv); un(rr.v[b], vv); un(rr.g[b], gr);
         if (xa && r < L) {
@@ -122,13 +126,14 @@ __device__ __forceinline__ void prep_compute(const RowRegs& rr, const float* __r
     }
 }
 
-// Loads and prepares rows of one chunk in one go (8 warps).
+// Loads and prepares rows of one chunk in one go (NW warps).
+template <int NW = 8>
 __device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                                           const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
                                           const uint16_t* __restrict__ beta_raw, const float* __restrict__ dt_bias,
                                           float a_h, float lb, int t0, int L, int H, int h, float* xq, float* xk,
                                           float* xv, float* xa, float* beta, float* inq, float* ink) {
-    RowRegs rr;
+    RowRegsT<NW> rr;
     prep_load(rr, (xq || inq) ? q : nullptr, (xk || ink) ? k : nullptr, xv ? v : nullptr, xa ? g_raw : nullptr,
               beta ? beta_raw : nullptr, t0, L, H, h);
     prep_compute(rr, dt_bias, a_h, lb, L, h, xq, xk, xv, xa, beta, inq, ink);
