@@ -34,7 +34,9 @@ struct WySmem {
 
 size_t bwd_wy_smem_bytes() { return sizeof(WySmem); }
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int kWyWarps = 16;
+
+__global__ void __launch_bounds__(kWyWarps * 32, 1)
     kda_bwd_wy_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                       const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
                       const float* __restrict__ A_log, const float* __restrict__ dt_bias, int H, float lb,
@@ -48,41 +50,32 @@ __global__ void __launch_bounds__(256, 1)
     const int gid = lane >> 2, tig = lane & 3;
     // Persistent over tiles (tile = chunk * H + h); the next tile's rows are
     // loaded into registers while the current one computes.
-    RowRegs rr;
-    // chunk records are read two tiles ahead so the row loads never wait on them
+    // chunk records are read two tiles ahead
     const int step = (int)gridDim.x;
     auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
     ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
-    auto fetch = [&](int t) {   // t: the tile whose record is ci_next
-        if (ci_next.L > 0) prep_load(rr, nullptr, k, v, g_raw, beta_raw, ci_next.t0, ci_next.L, H, t % H, A_log, dt_bias);
-    };
-    if ((int)blockIdx.x < ntiles) fetch(blockIdx.x);
     for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
     const ChunkInfo ci = ci_next;
     const int h = tile_i % H;
     const int nxt = tile_i + step;
-    ci_next = ci_next2;                        // record of tile nxt
+    ci_next = ci_next2;
     ci_next2 = chunk_of(nxt + step);
-    if (ci.L <= 0) {
-        if (nxt < ntiles) fetch(nxt);
-        continue;
-    }
+    if (ci.L <= 0) continue;
     const int L = ci.L;
     const size_t tile = (size_t)tile_i;
     const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
     uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
-    const float a_h = __expf(rr.alog);
+    const float a_h = __expf(A_log[h]);
 
     // dU, X, B arrive asynchronously while the rows are prepared
     panels_to_smem_async(s.dU, PS, gdU);
     tile_to_smem_async(s.X, PC, reinterpret_cast<const float*>(img + ImgOff::XM), C, C);
     tile_to_smem_async(s.B, PC, reinterpret_cast<const float*>(img + ImgOff::BM), C, C);
     cp_async_commit();
-    prep_compute(rr, nullptr, a_h, lb, L, h, nullptr, s.kt, s.v, s.dW, s.beta, nullptr, nullptr);
-    __syncthreads();
-    if (nxt < ntiles) fetch(nxt);
+    prep_rows<kWyWarps>(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dW,
+                        s.beta, nullptr, nullptr);
     __syncthreads();
     block_products(s.dW, nullptr, s.kt, nullptr, nullptr, &s.fa);
     __syncthreads();
@@ -102,12 +95,12 @@ __global__ void __launch_bounds__(256, 1)
     }
     __syncthreads();
 
-    // dT = dW Kt^T + dU V^T   (rows 16rb, columns 32ch: 4 n-tiles)
+    // dT = dW Kt^T + dU V^T   (rows 16rb, columns 16ch: 2 n-tiles)
     {
         const int rb = warp & 3, ch = warp >> 2;
-        float acc[4][4];
+        float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
@@ -116,26 +109,26 @@ __global__ void __launch_bounds__(256, 1)
             const Frag4 wf = frag4(s.dW[r0 * PS + k0], s.dW[r1 * PS + k0], s.dW[r0 * PS + k1], s.dW[r1 * PS + k1]);
             const Frag4 uf = frag4(s.dU[r0 * PS + k0], s.dU[r1 * PS + k0], s.dU[r0 * PS + k1], s.dU[r1 * PS + k1]);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int j = ch * 32 + nt * 8 + gid;
+            for (int nt = 0; nt < 2; ++nt) {
+                const int j = ch * 16 + nt * 8 + gid;
                 mma3(acc[nt], wf, frag2(s.kt[j * PS + k0], s.kt[j * PS + k1]));
                 mma2a(acc[nt], uf, tf32_bits(s.v[j * PS + k0]), tf32_bits(s.v[j * PS + k1]));   // v: bf16, exact
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 16 + nt * 8 + tig * 2 + (e & 1);
                 s.dT[row * PC + col] = acc[nt][e];
             }
     }
-    // dKt = T^T dW, dV = T^T dU   (rows j in 16jb, columns 64ch: 8 n-tiles); T[i][j] = 0 for i < j
+    // dKt = T^T dW, dV = T^T dU   (rows j in 16jb, columns 32ch: 4 n-tiles); T[i][j] = 0 for i < j
     {
         const int jb = warp & 3, ch = warp >> 2;
-        float ak[8][4], av[8][4];
+        float ak[4][4], av[4][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) { ak[nt][e] = 0.0f; av[nt][e] = 0.0f; }
         const int j0 = jb * SUB + gid, j1 = j0 + 8;
@@ -143,18 +136,18 @@ __global__ void __launch_bounds__(256, 1)
             const int i0 = ks * 8 + tig, i1 = i0 + 4;
             const Frag4 tf = frag4(s.T[i0 * PC + j0], s.T[i0 * PC + j1], s.T[i1 * PC + j0], s.T[i1 * PC + j1]);
 #pragma unroll
-            for (int nt = 0; nt < 8; ++nt) {
-                const int c = ch * 64 + nt * 8 + gid;
+            for (int nt = 0; nt < 4; ++nt) {
+                const int c = ch * 32 + nt * 8 + gid;
                 mma3(ak[nt], tf, frag2(s.dW[i0 * PS + c], s.dW[i1 * PS + c]));
                 mma3(av[nt], tf, frag2(s.dU[i0 * PS + c], s.dU[i1 * PS + c]));
             }
         }
         float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT);
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int row = jb * SUB + gid + hh * 8, col = ch * 64 + nt * 8 + tig * 2;
+                const int row = jb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
                 *reinterpret_cast<float2*>(gdK + row * D + col) = make_float2(ak[nt][hh * 2], ak[nt][hh * 2 + 1]);
                 if (row < L) {
                     const uint32_t pk = (uint32_t)f2bf(av[nt][hh * 2]) | ((uint32_t)f2bf(av[nt][hh * 2 + 1]) << 16);
@@ -172,9 +165,9 @@ __global__ void __launch_bounds__(256, 1)
     float* M = s.dW;
     {
         const int rb = warp & 3, ch = warp >> 2;
-        float acc[4][4];
+        float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
@@ -182,17 +175,17 @@ __global__ void __launch_bounds__(256, 1)
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
             const Frag4 af = frag4(s.dT[r0 * PC + m0], s.dT[r1 * PC + m0], s.dT[r0 * PC + m1], s.dT[r1 * PC + m1]);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int j = ch * 32 + nt * 8 + gid;
+            for (int nt = 0; nt < 2; ++nt) {
+                const int j = ch * 16 + nt * 8 + gid;
                 mma3(acc[nt], af, frag2(s.T[j * PC + m0], s.T[j * PC + m1]));
             }
         }
         __syncthreads();   // everyone is done reading dW before M overwrites it
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 16 + nt * 8 + tig * 2 + (e & 1);
                 M[row * PC + col] = acc[nt][e];
             }
     }
@@ -200,9 +193,9 @@ __global__ void __launch_bounds__(256, 1)
     // dA = -strict_lower(X^T M) into the dT buffer; X[m][i] = 0 for m < i
     {
         const int ib = warp & 3, ch = warp >> 2;
-        float acc[4][4];
+        float acc[2][4];
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
         const int i0 = ib * SUB + gid, i1 = i0 + 8;
@@ -210,16 +203,16 @@ __global__ void __launch_bounds__(256, 1)
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
             const Frag4 xf = frag4(s.X[m0 * PC + i0], s.X[m0 * PC + i1], s.X[m1 * PC + i0], s.X[m1 * PC + i1]);
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int j = ch * 32 + nt * 8 + gid;
+            for (int nt = 0; nt < 2; ++nt) {
+                const int j = ch * 16 + nt * 8 + gid;
                 mma3(acc[nt], xf, frag2(M[m0 * PC + j], M[m1 * PC + j]));
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = ib * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                const int row = ib * SUB + gid + (e >> 1) * 8, col = ch * 16 + nt * 8 + tig * 2 + (e & 1);
                 s.dT[row * PC + col] = col < row ? -acc[nt][e] : 0.0f;
             }
     }
