@@ -41,7 +41,9 @@ struct PairSmem {
 
 size_t bwd_pair_smem_bytes() { return sizeof(PairSmem); }
 
-__global__ void __launch_bounds__(256, 1)
+constexpr int kPairWarps = 16;
+
+__global__ void __launch_bounds__(kPairWarps * 32, 1)
     kda_bwd_pair_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                         const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
                         const float* __restrict__ A_log, const float* __restrict__ dt_bias, int H, float lb,
@@ -64,8 +66,8 @@ __global__ void __launch_bounds__(256, 1)
     tile_to_smem_async(s.dB, PC, reinterpret_cast<const float*>(wy + WyOff::DB), C, C);
     tile_to_smem_async(s.dA, PC, reinterpret_cast<const float*>(bg + BgOff::DAQK), C, C);
     cp_async_commit();
-    prep_rows(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp, s.beta,
-              s.inq, s.ink);
+    prep_rows<kPairWarps>(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp,
+                          s.beta, s.inq, s.ink);
     cp_async_wait_all();
     __syncthreads();
     block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);
@@ -73,11 +75,12 @@ __global__ void __launch_bounds__(256, 1)
     block_factors(&s.fa);
     __syncthreads();
 
-    // each warp owns rows 16rb + {gid, gid+8}, columns 64ch + 8nt + 2tig + {0,1}
+    // each warp owns rows 16rb + {gid, gid+8}, columns 32ch + 8nt + 2tig + {0,1}
     const int rb = warp & 3, ch = warp >> 2;
-    float adq[8][4], adk[8][4], adg[8][4];
+    constexpr int NT = 4;   // n-tiles of 8 columns per warp
+    float adq[NT][4], adk[NT][4], adg[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) { adq[nt][e] = 0.0f; adk[nt][e] = 0.0f; adg[nt][e] = 0.0f; }
 
@@ -88,9 +91,9 @@ __global__ void __launch_bounds__(256, 1)
             const float* dM = m == 0 ? s.dB : s.dA;
             const float* base = m == 0 ? s.ke : s.qe;
             for (int J = 0; J <= I; ++J) {
-                float acc[8][4];
+                float acc[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
 #pragma unroll
@@ -99,17 +102,17 @@ __global__ void __launch_bounds__(256, 1)
                     const int r0 = I * SUB + gid, r1 = r0 + 8;
                     const Frag4 af = frag4(dM[r0 * PC + j0], dM[r1 * PC + j0], dM[r0 * PC + j1], dM[r1 * PC + j1]);
 #pragma unroll
-                    for (int nt = 0; nt < 8; ++nt) {
-                        const int c = ch * 64 + nt * 8 + gid;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int c = ch * 32 + nt * 8 + gid;
                         mma3(acc[nt], af, frag2(s.kp[j0 * PS + c], s.kp[j1 * PS + c]));
                     }
                 }
                 const float* f = s.fa.F[I][J];
 #pragma unroll
-                for (int nt = 0; nt < 8; ++nt)
+                for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+                        const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
                         const float fc = f[col];
                         const float R = s.em[row * PS + col] * fc;
                         const float Xt = base[row * PS + col] * fc;
@@ -123,9 +126,9 @@ __global__ void __launch_bounds__(256, 1)
     // (b) column side: rows j of block J = rb, row blocks I >= J
     {
         const int J = rb;
-        float acc[8][4];
+        float acc[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
         for (int m = 0; m < 2; ++m) {
@@ -139,8 +142,8 @@ __global__ void __launch_bounds__(256, 1)
                     const int c0 = J * SUB + gid, c1 = c0 + 8;
                     const Frag4 af = frag4(dM[i0 * PC + c0], dM[i0 * PC + c1], dM[i1 * PC + c0], dM[i1 * PC + c1]);
 #pragma unroll
-                    for (int nt = 0; nt < 8; ++nt) {
-                        const int c = ch * 64 + nt * 8 + gid;
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const int c = ch * 32 + nt * 8 + gid;
                         const float fc = f[c];
                         mma3(acc[nt], af, frag2(base[i0 * PS + c] * fc, base[i1 * PS + c] * fc));
                     }
@@ -148,10 +151,10 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const int row = J * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+                const int row = J * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
                 adk[nt][e] += s.ep[row * PS + col] * acc[nt][e];
                 adg[nt][e] -= s.kp[row * PS + col] * acc[nt][e];
             }
@@ -160,12 +163,12 @@ __global__ void __launch_bounds__(256, 1)
     const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB);
     const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB);
     const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT);
-    float pk[8][4];
+    float pk[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int row = rb * SUB + gid + hh * 8, col = ch * 64 + nt * 8 + tig * 2;
+            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
             const float2 dQ2 = *reinterpret_cast<const float2*>(gdQ + row * D + col);
             const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
             const float2 dKt2 = *reinterpret_cast<const float2*>(gdKt + row * D + col);
@@ -185,10 +188,10 @@ __global__ void __launch_bounds__(256, 1)
         }
     __syncthreads();   // all reads of qe, ke, kp, em done
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-            const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 64 + nt * 8 + tig * 2 + (e & 1);
+            const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
             s.qe[row * PS + col] = adq[nt][e];
             s.ke[row * PS + col] = adk[nt][e];
             s.kp[row * PS + col] = adg[nt][e];
@@ -199,10 +202,10 @@ __global__ void __launch_bounds__(256, 1)
     // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); all rows of a warp loaded at once
     {
         const int c0 = lane * 4;
-        uint2 wq[C / 8], wk[C / 8];
+        uint2 wq[C / kPairWarps], wk[C / kPairWarps];
 #pragma unroll
-        for (int b = 0; b < C / 8; ++b) {
-            const int r = warp + 8 * b;
+        for (int b = 0; b < C / kPairWarps; ++b) {
+            const int r = warp + kPairWarps * b;
             wq[b] = wk[b] = make_uint2(0u, 0u);
             if (r < L) {
                 const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
@@ -211,8 +214,8 @@ __global__ void __launch_bounds__(256, 1)
             }
         }
 #pragma unroll
-        for (int b = 0; b < C / 8; ++b) {
-            const int r = warp + 8 * b;
+        for (int b = 0; b < C / kPairWarps; ++b) {
+            const int r = warp + kPairWarps * b;
             if (r >= L) break;
             const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
 #pragma unroll
@@ -257,11 +260,12 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     // gate chain, every thread: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
     {
+        constexpr int RG = kPairWarps * 32 / D;   // row groups (threads per channel)
         const int c = tid & (D - 1), r0 = tid >> 7;
         const float dtc = dt_bias[h * D + c];
         float ddt = 0.0f, dA = 0.0f;
 #pragma unroll 4
-        for (int r = r0; r < L; r += 2) {
+        for (int r = r0; r < L; r += RG) {
             const size_t gi = ((size_t)(t0 + r) * H + h) * D + c;
             const float x = bf2f(g_raw[gi]) + dtc;
             const float dgr = s.kp[r * PS + c] * lb * dsigmoidf(a_h * x) * a_h;
@@ -269,14 +273,18 @@ __global__ void __launch_bounds__(256, 1)
             ddt += dgr;
             dA += dgr * x;
         }
-        // two threads per channel: rows of even / odd index; combined in a fixed order
+        // RG threads per channel (rows r = r0 mod RG); combined below in a fixed order
         s.em[r0 * PS + c] = ddt;
         s.ep[r0 * PS + c] = dA;
     }
     __syncthreads();
     if (tid < D) {
-        part[tid] = s.em[tid] + s.em[PS + tid];
-        s.red[tid] = s.ep[tid] + s.ep[PS + tid];
+        constexpr int RG = kPairWarps * 32 / D;
+        float a = 0.0f, b = 0.0f;
+#pragma unroll
+        for (int g = 0; g < RG; ++g) { a += s.em[g * PS + tid]; b += s.ep[g * PS + tid]; }
+        part[tid] = a;
+        s.red[tid] = b;
     }
     if (tid < L) {
         const float db = reinterpret_cast<const float*>(wy + WyOff::DBETA)[tid];
