@@ -52,21 +52,45 @@ class _Args(ctypes.Structure):
     ]
 
 
-def build(force: bool = False) -> str:
+def build(force: bool = False, mutation: int = 0, out: str | None = None) -> str:
     """Compile the oracle with gcc (no fused multiply-add contraction, so the
-    result is the same on x86-64 and aarch64)."""
+    result is the same on x86-64 and aarch64). `mutation` > 0 plants one of the
+    test mistakes (tests only) into a separate library `out`."""
+    lib = out or _LIB
     with _lock:
-        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-            os.makedirs(os.path.dirname(_LIB), exist_ok=True)
-            tmp = _LIB + f".tmp{os.getpid()}"
+        if force or mutation or not os.path.exists(lib) or os.path.getmtime(lib) < os.path.getmtime(_SRC):
+            os.makedirs(os.path.dirname(lib), exist_ok=True)
+            tmp = lib + f".tmp{os.getpid()}"
             subprocess.check_call(["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fno-fast-math",
+                                   f"-DKDA_ORACLE_MUTATION={int(mutation)}",
                                    "-shared", "-fPIC", "-pthread", _SRC, "-o", tmp, "-lm"])
-            os.replace(tmp, _LIB)
-    return _LIB
+            os.replace(tmp, lib)
+    return lib
+
+
+def _bind(path):
+    lib = ctypes.CDLL(path)
+    lib.kda_oracle_forward.argtypes = [ctypes.POINTER(_Args)]
+    lib.kda_oracle_backward.argtypes = [ctypes.POINTER(_Args)]
+    lib.kda_oracle_args_size.restype = ctypes.c_size_t
+    assert lib.kda_oracle_args_size() == ctypes.sizeof(_Args), "oracle ABI mismatch"
+    return lib
+
+
+_override = None   # a library with a planted mistake, installed by the oracle's own tests
+
+
+def use_library(path):
+    """Tests only: route forward/backward through another build of the oracle
+    (None restores the normal one)."""
+    global _override
+    _override = _bind(path) if path else None
 
 
 def _load():
     global _lib
+    if _override is not None:
+        return _override
     if _lib is None:
         build()
         lib = ctypes.CDLL(_LIB)

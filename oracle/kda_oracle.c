@@ -77,6 +77,13 @@ typedef struct {
 
 enum { SEG = 64 };
 
+/* Test hook: the oracle's own tests rebuild it with KDA_ORACLE_MUTATION = n to
+ * plant one plausible mistake and check that the pins catch it. 0 = none. */
+#ifndef KDA_ORACLE_MUTATION
+#define KDA_ORACLE_MUTATION 0
+#endif
+#define MUT(n) (KDA_ORACLE_MUTATION == (n))
+
 /* Per-token quantities of the step, in the pages' notation. */
 typedef struct {
     double *qh, *kh, *g, *alpha;   /* [K] */
@@ -97,14 +104,14 @@ static void prep_token(const kda_oracle_args *a, int64_t t, int64_t h, tok_t *x)
     if (a->mode == 1) {
         double sq = 0.0, sk = 0.0;
         for (int64_t c = 0; c < K; ++c) { sq += q[c] * q[c]; sk += k[c] * k[c]; }
-        x->nq = sqrt(sq + a->eps);
+        x->nq = MUT(4) ? sqrt(sq) + a->eps : sqrt(sq + a->eps);
         x->nk = sqrt(sk + a->eps);
         const double am = exp(a->A_log[h]);
         for (int64_t c = 0; c < K; ++c) {
             x->qh[c] = q[c] / x->nq;
             x->kh[c] = k[c] / x->nk;
             x->s[c] = sigmoid(am * (gx[c] + a->dt_bias[h * K + c]));
-            x->g[c] = a->lb * x->s[c];
+            x->g[c] = (MUT(3) ? -a->lb : a->lb) * x->s[c];
             x->alpha[c] = exp(x->g[c]);
         }
         x->beta = sigmoid(bx);
@@ -131,15 +138,17 @@ static void step_fwd(const kda_oracle_args *a, const tok_t *x, const double *vt,
         double *row = S + i * K;
         double acc = 0.0;
         for (int64_t c = 0; c < K; ++c) {
-            row[c] *= x->alpha[c];            /* S' = S diag(exp(g)) */
+            row[c] *= MUT(1) ? x->alpha[i % K] : x->alpha[c];   /* S' = S diag(exp(g)) */
             acc += row[c] * x->kh[c];
         }
         r[i] = vt[i] - acc;                   /* r = v - S' k^ */
+        if (MUT(10)) r[i] = vt[i] - (i < K ? S[i * K + i] : 0.0) * x->kh[i % K] - acc;
         const double br = x->beta * r[i];
         double oi = 0.0;
         for (int64_t c = 0; c < K; ++c) {
+            if (MUT(2)) oi += row[c] * x->qh[c];
             row[c] += br * x->kh[c];          /* S = S' + beta r k^T */
-            oi += row[c] * x->qh[c];
+            if (!MUT(2)) oi += row[c] * x->qh[c];
         }
         if (o) o[i] = a->scale * oi;          /* o = scale S q^ */
     }
@@ -278,7 +287,7 @@ static void unit_backward(const kda_oracle_args *a, int64_t n, int64_t h, scratc
                 if (a->dv) a->dv[(t * H + h) * V + i] = dr[i];
                 for (int64_t c = 0; c < K; ++c) {
                     dSp[i * K + c] = dS[i * K + c] - dr[i] * x->kh[c];
-                    dkh[c] -= Sp[i * K + c] * dr[i];
+                    if (!MUT(5)) dkh[c] -= Sp[i * K + c] * dr[i];
                 }
             }
             /* decay S' = S_{t-1} diag(alpha) */
@@ -286,7 +295,7 @@ static void unit_backward(const kda_oracle_args *a, int64_t n, int64_t h, scratc
             for (int64_t i = 0; i < V; ++i)
                 for (int64_t c = 0; c < K; ++c) {
                     dal[c] += dSp[i * K + c] * Sprev[i * K + c];
-                    dS[i * K + c] = dSp[i * K + c] * x->alpha[c];
+                    dS[i * K + c] = MUT(6) ? dSp[i * K + c] : dSp[i * K + c] * x->alpha[c];
                 }
             /* gate, beta and norm chains */
             double *dgo = a->dgx + (t * H + h) * K;
@@ -295,16 +304,16 @@ static void unit_backward(const kda_oracle_args *a, int64_t n, int64_t h, scratc
                 const double *graw = a->gx + (t * H + h) * K;
                 for (int64_t c = 0; c < K; ++c) {
                     const double dg = dal[c] * x->alpha[c];
-                    const double du = dg * a->lb * x->s[c] * (1.0 - x->s[c]);
+                    const double du = dg * a->lb * x->s[c] * (MUT(7) ? 1.0 : (1.0 - x->s[c]));
                     dgo[c] = du * am;
                     ddt[c] += du * am;
-                    dA += du * am * (graw[c] + a->dt_bias[h * K + c]);
+                    dA += du * (MUT(8) ? 1.0 : am) * (graw[c] + a->dt_bias[h * K + c]);
                 }
                 a->dbx[t * H + h] = dbeta * x->beta * (1.0 - x->beta);
                 double pq = 0.0, pk = 0.0;
                 for (int64_t c = 0; c < K; ++c) { pq += x->qh[c] * dqh[c]; pk += x->kh[c] * dkh[c]; }
                 for (int64_t c = 0; c < K; ++c) {
-                    a->dq[(t * H + h) * K + c] = (dqh[c] - x->qh[c] * pq) / x->nq;
+                    a->dq[(t * H + h) * K + c] = (dqh[c] - (MUT(9) ? 0.0 : x->qh[c] * pq)) / x->nq;
                     a->dk[(t * H + h) * K + c] = (dkh[c] - x->kh[c] * pk) / x->nk;
                 }
             } else {
