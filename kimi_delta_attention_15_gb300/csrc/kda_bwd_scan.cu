@@ -21,6 +21,7 @@ struct BScanSmem {
     uint8_t KB[kTileCK];     // KB     [64 c][128 k]   |
     uint8_t AQKT[kTileCC];   // Aqk^T  [64 j][64 i]    /
     uint8_t DOT[kTileCK];    // dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
+    uint16_t DO[C * D];      // dO rows of the next chunk as stored (bf16 [64 i][128 v]), cp.async
     float gam[D];
     uint64_t barX, barY, barM1, barM2;
     uint32_t tmem;
@@ -82,36 +83,39 @@ __global__ void __launch_bounds__(256, 1)
     bool ok = true;
     const uint32_t idN64 = idesc_tf32(128, 64, 0, 0);
     const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
-    // dO, exp(G_L) and the chunk record are fetched one chunk ahead
-    uint32_t don[C / 4];   // this thread's 32 rows i of dO (column v), two bf16 per word
-    auto fetch_dO = [&](const ChunkInfo& c2) {
+    // dO rows of a chunk -> s.DO (rows past the chunk's end read as zero); 16 bytes per
+    // copy, four copies per thread, issued one chunk ahead of use
+    auto issue_dO = [&](const ChunkInfo& c2) {
 #pragma unroll
-        for (int ii = 0; ii < C / 2; ii += 2) {
-            const int i = 32 * half + ii;
-            const uint32_t lo = i < c2.L ? dO[((size_t)(c2.t0 + i) * H + h) * D + v] : 0u;
-            const uint32_t hi = i + 1 < c2.L ? dO[((size_t)(c2.t0 + i + 1) * H + h) * D + v] : 0u;
-            don[ii >> 1] = lo | (hi << 16);
+        for (int r = 0; r < (C * D / 8) / 256; ++r) {
+            const int seg = tid + 256 * r, i = seg >> 4, c8 = (seg & 15) * 8;
+            const bool valid = i < c2.L;
+            const uint16_t* src = dO + ((size_t)(c2.t0 + (valid ? i : 0)) * H + h) * D + c8;
+            cp_async16_zfill(s.DO + i * D + c8, src, valid);
         }
+        cp_async_commit();
     };
-    ChunkInfo ci_next = cf < cl ? chunks[cl - 1] : ChunkInfo{0, 0, 0, 0};
+    // exp(G_L) and the chunk record are read one chunk ahead
     float gam_next = cf < cl ? reinterpret_cast<const float*>(img_of(cl - 1) + ImgOff::GAML)[v] : 0.0f;
-    if (cf < cl) fetch_dO(ci_next);
+    if (cf < cl) issue_dO(chunks[cl - 1]);
     for (int chunk = cl - 1; chunk >= cf && ok; --chunk) {
         const uint32_t par = (uint32_t)((cl - 1 - chunk) & 1);
         const size_t tile = (size_t)chunk * H + h;
         if (half == 0) s.gam[v] = gam_next;
+        ChunkInfo ci_prev{0, 0, 0, 0};
+        if (chunk - 1 >= cf) {
+            ci_prev = chunks[chunk - 1];
+            gam_next = reinterpret_cast<const float*>(img_of(chunk - 1) + ImgOff::GAML)[v];
+        }
+        cp_async_wait_all();
         __syncthreads();
         // dO^T into the operand tile (row v, columns i); bf16 values are exact in tf32
         // (the output scale is folded into the Aqk^T and (Q^*Gamma)^T images)
 #pragma unroll
-        for (int ii = 0; ii < C / 2; ii += 4)
+        for (int ii = 0; ii < C / 2; ii += 4) {
+            const uint16_t* col = s.DO + (32 * half + ii) * D + v;
             *reinterpret_cast<float4*>(s.DOT + panel_off(v, 32 * half + ii, D)) =
-                make_float4(bf2f((uint16_t)(don[ii >> 1] & 0xffffu)), bf2f((uint16_t)(don[ii >> 1] >> 16)),
-                            bf2f((uint16_t)(don[(ii >> 1) + 1] & 0xffffu)), bf2f((uint16_t)(don[(ii >> 1) + 1] >> 16)));
-        if (chunk - 1 >= cf) {
-            ci_next = chunks[chunk - 1];
-            gam_next = reinterpret_cast<const float*>(img_of(chunk - 1) + ImgOff::GAML)[v];
-            fetch_dO(ci_next);
+                make_float4(bf2f(col[0]), bf2f(col[D]), bf2f(col[2 * D]), bf2f(col[3 * D]));
         }
         // dS_L: TMEM -> tf32 operand, and dS_L^T [k][v] (tf32) to the workspace
         // checkpoint; dS_L diag(exp(G_L)) back to TMEM
@@ -137,6 +141,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        if (chunk - 1 >= cf) issue_dO(ci_prev);   // every thread is past its reads of s.DO
         if (tid == 0) {
             const bool gx = mbar_wait(&s.barX, par), gy = gx && mbar_wait(&s.barY, par);
             x_done += gx; y_done += gy;
@@ -202,6 +207,7 @@ __global__ void __launch_bounds__(256, 1)
         for (; y_done < y_issued; ++y_done) mbar_wait(&s.barY, (uint32_t)(y_done & 1));
         bulk_wait_all();
     }
+    cp_async_wait_all();   // dO copies still in flight (only after an aborted scan)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 256);

@@ -24,7 +24,8 @@ struct ScanSmem {
     uint8_t QB[kTileCK];       // [64 c][128 k]     /
     uint8_t KBT[kTileCK];      // [128 k][64 c]     \ one bulk group
     uint8_t AQK[kTileCC];      // [64 i][64 j]      /
-    uint8_t UT[kTileCK];       // [128 v][64 c]
+    uint8_t UT[kTileCK];       // [128 v][64 c]; between the state update and the next
+                               // chunk's Ut also the bf16 output rows [64 i][128 v]
     float gam[D];
     uint64_t barA, barB, barM1, barM2;
     uint32_t tmem;
@@ -93,6 +94,18 @@ __global__ void __launch_bounds__(256, 1)
     float gam_next = cf < cl ? reinterpret_cast<const float*>(ws + lay.img + ((size_t)cf * H + h) * ImgOff::BYTES +
                                                               ImgOff::GAML)[v]
                              : 0.0f;
+    // output rows staged in s.UT wait for the next loop-top barrier, then go out as one
+    // bulk store per token row (threads 128..191, row tid - 128)
+    uint16_t* const ost = reinterpret_cast<uint16_t*>(s.UT);
+    const bool o_thread = tid >= 128 && tid < 128 + C;
+    int o_t0 = 0, o_L = 0;
+    auto store_o_rows = [&]() {
+        if (o_thread && tid - 128 < o_L) {
+            bulk_s2g(o + ((size_t)(o_t0 + tid - 128) * H + h) * D, ost + (tid - 128) * D, (uint32_t)(2 * D));
+            bulk_commit();
+        }
+        o_L = 0;
+    };
     for (int chunk = cf; chunk < cl && ok; ++chunk) {
         const uint32_t par = (uint32_t)((chunk - cf) & 1);
         const ChunkInfo ci = ci_next;
@@ -105,6 +118,7 @@ __global__ void __launch_bounds__(256, 1)
             gam_next = reinterpret_cast<const float*>(img + (size_t)H * ImgOff::BYTES + ImgOff::GAML)[v];  // chunk + 1
         }
         __syncthreads();
+        store_o_rows();
 
         // S0: TMEM -> registers -> tf32 operand in smem, and its transpose S0^T [k][v]
         // (tf32) to the workspace checkpoint; decayed state back to TMEM
@@ -148,6 +162,7 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
         for (int c = 0; c < 32; ++c) u[c] = gU[(32 * half + c) * D + v];
         ok = mbar_wait(&s.barM1, par) && ok;
+        if (o_thread) bulk_wait_read_all();   // s.UT is rewritten below
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
@@ -190,18 +205,21 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         if (tid == 0 && chunk + 1 < cl) { issue_B(chunk + 1); ++b_issued; }
 
-        // o = scale * O
+        // o = scale * O, staged as bf16 rows
         {
             const int c0 = 32 * half;
             float r[32];
             tmem_ld32(tOT + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const int i = c0 + j;
-                if (i < ci.L) o[((size_t)(ci.t0 + i) * H + h) * D + v] = f2bf(scale * r[j]);
-            }
+            for (int j = 0; j < 32; ++j) ost[(c0 + j) * D + v] = f2bf(scale * r[j]);
         }
+        fence_async_smem();
+        o_t0 = ci.t0;
+        o_L = ci.L;
     }
+    __syncthreads();
+    if (ok) store_o_rows();
+    if (o_thread) bulk_wait_all();
     if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
 
     // final state
