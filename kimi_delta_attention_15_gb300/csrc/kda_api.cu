@@ -249,7 +249,8 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
             do_, dhT, dh0, H, ws, lay);
     prof(5, s);
     if (lay.nc_max > 0)
-        kda_bwd_state_kernel<<<tiles, 256, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws, lay);
+        kda_bwd_state_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws,
+                                                                                                  lay);
     prof(6, s);
     if (lay.nc_max > 0)
         kda_bwd_wy_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,

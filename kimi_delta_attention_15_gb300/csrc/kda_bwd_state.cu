@@ -1,7 +1,7 @@
-// Backward, state-side products of each chunk: one CTA per (chunk, head), all
-// chunks in parallel. From the checkpoints S0^T (forward) and dS_L^T (backward
-// scan), stored key-major by the scans, and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over
-// the key channel k):
+// Backward, state-side products of each chunk, all chunks in parallel. From the
+// checkpoints S0^T (forward) and dS_L^T (backward scan), stored key-major by the
+// scans, and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over the
+// key channel k):
 //   dQbar = scale dO S0            [c][k]
 //   dW    = -dUt S0                [c][k]
 //   dKbar = Ut dS_L                [c][k]
@@ -10,186 +10,281 @@
 //                                    before the factor exp(G_L))
 // These are the reverse mode of Ut = U - W S0^T, O = scale[(Q^*Gamma) S0^T + Aqk Ut],
 // S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
+//
+// Persistent and warp-specialised. Every product contracts over the value
+// channel v, so a tile streams through shared memory as four 32-column value
+// panels in a two-stage ring:
+//   warp 0        bulk copies of the panels (and the tile's dO rows)
+//   warps 4..7    split Ut, dUt into tf32 high + low parts, dO to fp32, and the
+//                 diagonal dgam on the CUDA cores
+//   warp 1        the MMAs of a panel into one of two TMEM accumulator sets
+//   warps 8..15   accumulators -> workspace, overlapping the next tile's MMAs
+// S0, dS_L and dO are exact in tf32; Ut and dUt enter as high + low parts.
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
 namespace kda {
 
 namespace {
+constexpr int kStWarps = 16;
+constexpr uint32_t kPanelDD = D * 128;   // one 32-column panel of a 128-row tile (16 KB)
+constexpr uint32_t kPanelCD = C * 128;   // one 32-column panel of a 64-row tile (8 KB)
+constexpr int kDoPitch = 2 * D + 64;     // bytes per staged dO row (padded against bank conflicts)
+
+struct StStage {
+    uint8_t S0T[kPanelDD];   // S0^T   [128 k][32 v]
+    uint8_t DST[kPanelDD];   // dS_L^T [128 k][32 v]
+    uint8_t STK[kPanelDD];   // rows 0..63 dO [c][32 v] (fp32), rows 64..127 dUt high part
+    uint8_t DUL[kPanelCD];   // dUt low part [64 c][32 v]
+    uint8_t UH[kPanelCD];    // Ut as copied, then its high part [64 c][32 v]
+    uint8_t UL[kPanelCD];    // Ut low part
+};
 struct BStateSmem {
-    uint8_t S0T[kTileDD];    // S0^T   [128 k][128 v]
-    uint8_t DST[kTileDD];    // dS_L^T [128 k][128 v]
-    uint8_t STK[kTileDD];    // rows 0..63: dO [c][v]; rows 64..127: dUt [c][v]
-    uint8_t UT[kTileCK];     // Ut [64 c][128 v]
-    uint64_t bar, barC, barM;
+    StStage st[2];
+    uint8_t dos[2][C * kDoPitch];   // dO rows of a tile as stored (bf16), by tile parity
+    uint64_t full[2], ready[2], empty[2], tfull[2], tempty[2], fin;
     uint32_t tmem;
+    int abort;
 };
 }  // namespace
 
 size_t bwd_state_smem_bytes() { return sizeof(BStateSmem) + 1024; }
 
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(kStWarps * 32, 1)
     kda_bwd_state_kernel(const uint16_t* __restrict__ dO, int H, float scale, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
     BStateSmem& s = *reinterpret_cast<BStateSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     if (read_status(ws) != 0) return;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
-    if (ci.L <= 0) return;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const size_t tile = (size_t)chunk * H + h;
-    const uint8_t* gS0 = ws + lay.s0 + tile * kTileDD;
-    const uint8_t* gDS = ws + lay.ds + tile * kTileDD;
-    const uint8_t* gUt = ws + lay.ut + tile * kTileCK;
-    const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int ntiles = lay.nc_max * H;
 
     if (warp == 0) {
         tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&s.bar, 1); mbar_init(&s.barC, 1); mbar_init(&s.barM, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.ready[i], 128);
+            mbar_init(&s.empty[i], 1);
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], 256);
+        }
+        mbar_init(&s.fin, 1);
+        s.abort = 0;
         fence_mbar_init();
     }
+    tc_fence_before();
     __syncthreads();
-    // Ut and dUt (fp32) are used split into tf32 high and low parts, in two
-    // passes over the same buffers: pass 1 with the high parts, pass 2 adds
-    // the products with the low parts (S0, dS_L and dO are exact in tf32).
-    auto load_u = [&](uint32_t) {
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&s.bar, (uint32_t)(2 * kTileCK));
-            bulk_g2s(s.UT, gUt, (uint32_t)kTileCK, &s.bar);
-            for (int p = 0; p < 4; ++p)
-                bulk_g2s(s.STK + p * (D * 128) + 64 * 128, gdU + p * (C * 128), C * 128, &s.bar);
-        }
-    };
-    // to high (lo = false) or low (lo = true) tf32 parts, in place
-    auto split_u = [&](bool lo) {
-        for (int i = tid; i < C * D; i += blockDim.x) {
-            float* a = reinterpret_cast<float*>(s.UT) + i;
-            const int r = i >> 7, c = i & 127;   // any bijection over the 64 x 128 elements
-            float* b = reinterpret_cast<float*>(s.STK + panel_off(64 + r, c, D));
-            const float x = *a, y = *b;
-            *a = lo ? tf32_round(x - tf32_round(x)) : tf32_round(x);
-            *b = lo ? tf32_round(y - tf32_round(y)) : tf32_round(y);
-        }
-    };
-    load_u(0);
-    // checkpoints S0^T and dS_L^T arrive in operand layout by bulk copy
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&s.barC, (uint32_t)(2 * kTileDD));
-        bulk_g2s(s.S0T, gS0, (uint32_t)kTileDD, &s.barC);
-        bulk_g2s(s.DST, gDS, (uint32_t)kTileDD, &s.barC);
-    }
-    // dO rows 0..63 of the stack (bf16 values are exact in tf32; the scale is applied on readback)
-    {
-        const int v = tid & (D - 1), half = tid >> 7;
-        uint16_t dov[C / 2];
-#pragma unroll
-        for (int i = 0; i < C / 2; ++i) {
-            const int c = half * (C / 2) + i;
-            dov[i] = c < ci.L ? dO[((size_t)(ci.t0 + c) * H + h) * D + v] : (uint16_t)0;
-        }
-#pragma unroll
-        for (int i = 0; i < C / 2; ++i)
-            *reinterpret_cast<float*>(s.STK + panel_off(half * (C / 2) + i, v, D)) = bf2f(dov[i]);
-    }
+    tc_fence_after();
     const uint32_t tm = s.tmem;
-    bool ok = mbar_wait(&s.bar, 0) && mbar_wait(&s.barC, 0);
-    ok = __syncthreads_and(ok);
-    if (ok) split_u(false);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t aS = smem_u32(s.S0T), aD = smem_u32(s.DST), aK = smem_u32(s.STK), bU = smem_u32(s.UT);
-    const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
-    if (tid == 0 && ok) {
-        // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T  -> cols 0..127
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 0, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, ks > 0);
-        // dKbar^T = dS_L^T Ut^T                            -> cols 128..191
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
-        // dS_L^T S0 (diagonal used)                         -> cols 256..383
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 256, desc_kmajor(aD, D, ks), desc_kmajor(aS, D, ks), id128, ks > 0);
-        // [dO ; dUt] Ut^T (rows 0..63 used, x scale)      -> cols 384..447
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, ks > 0);
-        umma_commit(&s.barM);
-    }
-    ok = (ok && mbar_wait(&s.barM, 0));
-    ok = __syncthreads_and(ok);
-    // pass 2: the low parts of Ut and dUt
-    if (ok) {
-        tc_fence_after();
-        load_u(1);
-        ok = mbar_wait(&s.bar, 1);
-        ok = __syncthreads_and(ok);
-    }
-    if (ok) split_u(true);
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (tid == 0 && ok) {
-        // (dUt_lo S0)^T                                     -> cols 64..127
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 64, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks, 64), id64, 1);
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 128, desc_kmajor(aD, D, ks), desc_kmajor(bU, C, ks), id64, 1);
-        for (int ks = 0; ks < D / 8; ++ks)
-            umma_tf32(tm + 384, desc_kmajor(aK, D, ks), desc_kmajor(bU, C, ks), id64, 1);
-        umma_commit(&s.barM);
-    }
-    ok = (ok && mbar_wait(&s.barM, 1));
-    ok = __syncthreads_and(ok);
-    tc_fence_after();
-    if (ok) {
-        // warp w reads TMEM lanes 32 (w % 4) .. +31; warps w and w + 4 split the columns
-        const int kq = (warp & 3) * 32 + (tid & 31);   // lane = key channel k (or row i for dAqk)
-        const uint32_t lb = (uint32_t)((warp & 3) * 32) << 16;
-        const int c0 = (warp >> 2) * 32;
-        uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
-        float* gdQ = reinterpret_cast<float*>(bg + BgOff::DQB);
-        float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
-        float* gdK = reinterpret_cast<float*>(bg + BgOff::DKB);
-        float* gdA = reinterpret_cast<float*>(bg + BgOff::DAQK);
-        float* gdG = reinterpret_cast<float*>(bg + BgOff::DGAM);
-        {
-            float r[32];
-            tmem_ld32(tm + lb + c0, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) gdQ[(c0 + j) * D + kq] = scale * r[j];
-            tmem_ld32(tm + lb + 64 + c0, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) gdW[(c0 + j) * D + kq] = -r[j];
-            tmem_ld32(tm + lb + 128 + c0, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) gdK[(c0 + j) * D + kq] = r[j];
+    volatile int* abort_flag = &s.abort;
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
+                const int chunk = tile / H, h = tile - chunk * H;
+                const ChunkInfo ci = chunks[chunk];
+                if (ci.L <= 0) continue;
+                const size_t t = (size_t)chunk * H + h;
+                const uint8_t* gS0 = ws + lay.s0 + t * kTileDD;
+                const uint8_t* gDS = ws + lay.ds + t * kTileDD;
+                const uint8_t* gUt = ws + lay.ut + t * kTileCK;
+                const uint8_t* gdU = ws + lay.dut + t * kTileCK;
+                for (int p = 0; p < 4; ++p, ++it) {
+                    const int sg = it & 1;
+                    if (!mbar_wait(&s.empty[sg], ((it >> 1) & 1) ^ 1) || *abort_flag) { ok = false; break; }
+                    StStage& g = s.st[sg];
+                    const uint32_t bytes = 2 * kPanelDD + 2 * kPanelCD + (p == 0 ? (uint32_t)ci.L * 2 * D : 0u);
+                    mbar_arrive_expect_tx(&s.full[sg], bytes);
+                    bulk_g2s(g.S0T, gS0 + p * kPanelDD, kPanelDD, &s.full[sg]);
+                    bulk_g2s(g.DST, gDS + p * kPanelDD, kPanelDD, &s.full[sg]);
+                    bulk_g2s(g.UH, gUt + p * kPanelCD, kPanelCD, &s.full[sg]);
+                    bulk_g2s(g.STK + kPanelCD, gdU + p * kPanelCD, kPanelCD, &s.full[sg]);
+                    if (p == 0)
+                        for (int c = 0; c < ci.L; ++c)
+                            bulk_g2s(s.dos[n & 1] + c * kDoPitch, dO + ((size_t)(ci.t0 + c) * H + h) * D, 2 * D,
+                                     &s.full[sg]);
+                }
+                ++n;
+            }
+            if (!ok) *abort_flag = 1;
+            // copies still in flight (only after an abort): the last issue of each stage
+            for (int j = it - 1; j >= 0 && j >= it - 2; --j) mbar_wait(&s.full[j & 1], (j >> 1) & 1);
         }
-        if (warp < 4) {
-            float r[32];
-            tmem_ld32(tm + lb + 256 + warp * 32, r);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (lane == 0) {
+            const uint32_t id128 = idesc_tf32(128, 128, 0, 0), id64 = idesc_tf32(128, 64, 0, 0);
+            int it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
+                if (chunks[tile / H].L <= 0) continue;
+                const int tb = n & 1;
+                const uint32_t acc = tm + 256u * tb;
+                for (int p = 0; p < 4; ++p, ++it) {
+                    const int sg = it & 1;
+                    if (!mbar_wait(&s.ready[sg], (it >> 1) & 1) ||
+                        (p == 0 && !mbar_wait(&s.tempty[tb], ((n >> 1) & 1) ^ 1)) || *abort_flag) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const StStage& g = s.st[sg];
+                    const uint32_t aS = smem_u32(g.S0T), aD = smem_u32(g.DST), aK = smem_u32(g.STK);
+                    const uint32_t bDL = smem_u32(g.DUL), bUH = smem_u32(g.UH), bUL = smem_u32(g.UL);
+                    // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T     -> cols 0..127
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc, desc_kmajor(aS, D, ks), desc_kmajor(aK, D, ks), id128, (p | ks) != 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc + 64, desc_kmajor(aS, D, ks), desc_kmajor(bDL, C, ks), id64, 1);
+                    // dKbar^T = dS_L^T Ut^T                              -> cols 128..191
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc + 128, desc_kmajor(aD, D, ks), desc_kmajor(bUH, C, ks), id64, (p | ks) != 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc + 128, desc_kmajor(aD, D, ks), desc_kmajor(bUL, C, ks), id64, 1);
+                    // [dO ; dUt] Ut^T (rows 0..63 used, x scale)          -> cols 192..255
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc + 192, desc_kmajor(aK, D, ks), desc_kmajor(bUH, C, ks), id64, (p | ks) != 0);
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_tf32(acc + 192, desc_kmajor(aK, D, ks), desc_kmajor(bUL, C, ks), id64, 1);
+                    umma_commit(&s.empty[sg]);
+                    if (p == 3) umma_commit(&s.tfull[tb]);
+                }
+                ++n;
+            }
+            if (!ok) *abort_flag = 1;
+            umma_commit(&s.fin);   // every MMA of this CTA has completed once fin flips
+            mbar_wait(&s.fin, 0);
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
+        // --------------------------------------------------------- splitter
+        const int t = tid - 128;   // row k of the key-major panels
+        int it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
+            const int chunk = tile / H;
+            const ChunkInfo ci = chunks[chunk];
+            if (ci.L <= 0) continue;
+            const uint8_t* dos = s.dos[n & 1];
             float dg = 0.0f;
+            for (int p = 0; p < 4; ++p, ++it) {
+                const int sg = it & 1;
+                if (!mbar_wait(&s.full[sg], (it >> 1) & 1) || *abort_flag) { ok = false; break; }
+                StStage& g = s.st[sg];
+                // dgam: row k of S0^T and dS_L^T
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dg = (j == (tid & 31)) ? r[j] : dg;
-            gdG[kq] = dg;
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const uint32_t off = t * 128u + ((j4 ^ (t & 7)) << 4);
+                    const float4 a = *reinterpret_cast<const float4*>(g.S0T + off);
+                    const float4 b = *reinterpret_cast<const float4*>(g.DST + off);
+                    dg = fmaf(a.x, b.x, dg); dg = fmaf(a.y, b.y, dg);
+                    dg = fmaf(a.z, b.z, dg); dg = fmaf(a.w, b.w, dg);
+                }
+                // Ut, dUt -> high (in place) + low parts; dO rows -> fp32 (zero past the chunk)
+#pragma unroll
+                for (int r = 0; r < 4; ++r) {
+                    const int e = t + 128 * r, c = e >> 3, j4 = e & 7;
+                    const uint32_t off = c * 128u + ((j4 ^ (c & 7)) << 4);
+                    float4 x = *reinterpret_cast<const float4*>(g.UH + off);
+                    float4 xh = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
+                    *reinterpret_cast<float4*>(g.UH + off) = xh;
+                    *reinterpret_cast<float4*>(g.UL + off) =
+                        make_float4(tf32_round(x.x - xh.x), tf32_round(x.y - xh.y), tf32_round(x.z - xh.z),
+                                    tf32_round(x.w - xh.w));
+                    x = *reinterpret_cast<const float4*>(g.STK + kPanelCD + off);
+                    xh = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
+                    *reinterpret_cast<float4*>(g.STK + kPanelCD + off) = xh;
+                    *reinterpret_cast<float4*>(g.DUL + off) =
+                        make_float4(tf32_round(x.x - xh.x), tf32_round(x.y - xh.y), tf32_round(x.z - xh.z),
+                                    tf32_round(x.w - xh.w));
+                    float4 d = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (c < ci.L) {
+                        const uint2 w = *reinterpret_cast<const uint2*>(dos + c * kDoPitch + 2 * (32 * p + 4 * j4));
+                        d = make_float4(bf2f((uint16_t)(w.x & 0xffffu)), bf2f((uint16_t)(w.x >> 16)),
+                                        bf2f((uint16_t)(w.y & 0xffffu)), bf2f((uint16_t)(w.y >> 16)));
+                    }
+                    *reinterpret_cast<float4*>(g.STK + off) = d;
+                }
+                fence_async_smem();
+                mbar_arrive(&s.ready[sg]);
+            }
+            if (!ok) break;
+            const size_t tt = (size_t)chunk * H + (tile - chunk * H);
+            reinterpret_cast<float*>(ws + lay.bg + tt * BgOff::BYTES + BgOff::DGAM)[t] = dg;
+            ++n;
         }
-        if ((warp & 3) < 2) {
-            const int i = kq;
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 8) {
+        // --------------------------------------------------------- epilogue
+        const int e = tid - 256, ew = e >> 5, q = ew & 3, hf = ew >> 2;
+        const int kq = 32 * q + lane;   // TMEM lane: key channel k (row i for dAqk)
+        bool ok = true;
+        for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
+            const int chunk = tile / H;
+            if (chunks[chunk].L <= 0) continue;
+            const int tb = n & 1;
+            // the TMEM loads below are warp-collective: decide per warp
+            if (!__all_sync(0xffffffffu, mbar_wait(&s.tfull[tb], (n >> 1) & 1) && !*abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tm + 256u * tb + ((uint32_t)(32 * q) << 16);
+            const size_t tt = (size_t)chunk * H + (tile - chunk * H);
+            uint8_t* bg = ws + lay.bg + tt * BgOff::BYTES;
             float r[32];
-            tmem_ld32(tm + lb + 384 + c0, r);
+            if (hf == 0) {
+                float* gdQ = reinterpret_cast<float*>(bg + BgOff::DQB);
+                float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
+                tmem_ld32(acc + 0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) gdA[i * C + c0 + j] = (c0 + j <= i) ? scale * r[j] : 0.0f;
+                for (int j = 0; j < 32; ++j) gdQ[j * D + kq] = scale * r[j];
+                tmem_ld32(acc + 32, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdQ[(32 + j) * D + kq] = scale * r[j];
+                tmem_ld32(acc + 64, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdW[j * D + kq] = -r[j];
+            } else {
+                float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
+                float* gdK = reinterpret_cast<float*>(bg + BgOff::DKB);
+                tmem_ld32(acc + 96, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdW[(32 + j) * D + kq] = -r[j];
+                tmem_ld32(acc + 128, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdK[j * D + kq] = r[j];
+                tmem_ld32(acc + 160, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdK[(32 + j) * D + kq] = r[j];
+            }
+            if (q < 2) {
+                float* gdA = reinterpret_cast<float*>(bg + BgOff::DAQK);
+                const int i = kq, j0 = 32 * hf;
+                tmem_ld32(acc + 192 + j0, r);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) gdA[i * C + j0 + j] = (j0 + j <= i) ? scale * r[j] : 0.0f;
+            }
+            tc_fence_before();
+            mbar_arrive(&s.tempty[tb]);
+            ++n;
         }
-    } else {
-        raise_status(ws, KDA_ERR_TIMEOUT);
+        if (!ok) *abort_flag = 1;
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 512);
+    if (*abort_flag && tid == 0) raise_status(ws, KDA_ERR_TIMEOUT);
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tm, 512);
+    }
 }
 
 }  // namespace kda
