@@ -16,6 +16,15 @@
 // and j of different sub-blocks are split at the end of j's sub-block, so each
 // factor stays in [e^{-80}, e^{80}] for lb >= -5 (sub-blocks of 16 tokens):
 //   e^{G_i - G_j} = (e^{G_i - G_{e_J}}) * (e^{G_{e_J} - G_j}),  e_J = last row of block J.
+//
+// Schedule of one tile (16 warps). The raw inputs of the CTA's next tile are
+// staged by cp.async while the current tile computes W and U, so the input
+// preparation reads shared memory instead of waiting on global loads:
+//   prep (staged rows) -> block products -> factors
+//   pairs: warps 0..9 the ten A blocks, warps 10..15 six Aqk blocks
+//   warps 0..3 solve (I + A)^{-1} | warps 4..7 the other four Aqk blocks |
+//     warps 8..15 the elementwise images
+//   T, X and Aqk images; then next tile's rows -> staging; W, U
 #include "kda_internal.cuh"
 #include "mma_sync.cuh"
 #include "umma.cuh"
@@ -27,19 +36,27 @@ namespace {
 
 constexpr int P = PS;
 constexpr int PA = PC;
+constexpr int VP = D + 8;   // bf16 row pitch of the staged v rows (conflict-free fragment loads)
 
 struct IntraSmem {
     float qe[C * P];      // q^ * E-
     float ke[C * P];      // k^ * E-
     float kp[C * P];      // alpha, then k^ * E+
-    float v[C * P];
+    // A | Aqk | X are contiguous: from the T step of one tile to the input
+    // preparation of the next they hold that tile's raw q, k, g_raw rows
     float A[C * PA];      // beta-scaled strictly lower A
     float Aqk[C * PA];
     float X[C * PA];      // (I + A)^{-1}
     float T[C * PA];      // X diag(beta)
+    uint16_t vb[2][C * VP];   // raw v rows (bf16, exact in tf32), by tile parity
     Factors fa;
+    float dtb[D];         // dt_bias of the staged tile's head
     float beta[C];
+    uint16_t braw[C];
 };
+static_assert(3 * C * PA * 4 >= 3 * C * D * 2, "the staged rows fit in A | Aqk | X");
+
+__device__ __forceinline__ void bar_solve() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 }  // namespace
 
@@ -59,45 +76,37 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     // Persistent: this CTA takes tiles blockIdx.x, + gridDim.x, ... (tile = chunk * H + h).
-    // The rows of the next tile are loaded into registers while the current one computes.
-    // chunk records are read two tiles ahead
+    // Empty chunk records only follow the last real chunk, so the first empty
+    // tile ends the CTA's work.
     const int step = (int)gridDim.x;
-    auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
-    ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
-    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
-    const ChunkInfo ci = ci_next;
-    const int h = tile_i % H;
-    const int nxt = tile_i + step;
-    ci_next = ci_next2;
-    ci_next2 = chunk_of(nxt + step);
-    if (ci.L <= 0) continue;
-    const int L = ci.L;
-    const float a_h = __expf(A_log[h]);
-    const size_t tile = (size_t)tile_i;
-    uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
+    int tile_i = blockIdx.x;
+    ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
+    if (ci.L <= 0) return;
 
-    prep_rows<kIntraWarps>(q, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, s.qe, s.ke, s.v, s.kp,
-                           s.beta, nullptr, nullptr);
-    __syncthreads();
-    block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);
-    // zero the blocks above the diagonal of A, Aqk, X
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int r = idx >> 6, cc = idx & 63;
-        if ((cc >> 4) > (r >> 4)) {
-            s.A[r * PA + cc] = 0.0f;
-            s.Aqk[r * PA + cc] = 0.0f;
-            s.X[r * PA + cc] = 0.0f;
+    uint16_t* const stg = reinterpret_cast<uint16_t*>(s.A);   // staged q, k, g_raw rows
+    float alog_next = 0.0f;
+    uint16_t braw_next = 0;
+    // raw rows of tile t_i (record cn) -> staging and vdst; rows past the chunk read as zero
+    auto stage_tile = [&](int t_i, const ChunkInfo& cn, uint16_t* vdst) {
+        const int hn = t_i % H;
+        for (int seg = tid; seg < 4 * C * (D / 8); seg += kIntraWarps * 32) {
+            const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
+            const uint16_t* src = which == 0 ? q : which == 1 ? k : which == 2 ? g_raw : v;
+            const bool valid = r < cn.L;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
+            uint16_t* dst = which < 3 ? stg + which * C * D + r * D + c8 : vdst + r * VP + c8;
+            cp_async16_zfill(dst, src, valid);
         }
-    }
-    __syncthreads();
-    block_factors(&s.fa);
-    __syncthreads();
+        if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
+        cp_async_commit();
+        alog_next = A_log[hn];
+        if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
+    };
 
-    // ---- pairwise decayed products, 16x16 blocks (I >= J), tf32 mma.sync
-    for (int task = warp; task < 20; task += kIntraWarps) {
-        const int m = task / 10;
+    // one 16x16 block of A (m = 0) or Aqk (m = 1), tf32 split products
+    auto pair_task = [&](int m, int t, uint8_t* img) {
         int I, J;
-        tri_pair(task % 10, I, J);
+        tri_pair(t, I, J);
         const float* base = m == 0 ? s.ke : s.qe;
         const float* f = s.fa.F[I][J];
         float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
@@ -137,154 +146,234 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
                     s.Aqk[row * PA + col] = col <= row ? val : 0.0f;
                 }
             }
-    }
-    __syncthreads();
+    };
 
-    // ---- X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution
-    if (warp < NSUB && lane < SUB) {
-        const int I = warp, col = lane;
-        float x[SUB];
-#pragma unroll
-        for (int i = 0; i < SUB; ++i) {
-            float acc = (i == col) ? 1.0f : 0.0f;
-#pragma unroll
-            for (int m2 = 0; m2 < i; ++m2) acc -= s.A[(I * SUB + i) * PA + I * SUB + m2] * x[m2];
-            x[i] = acc;
-            s.X[(I * SUB + i) * PA + I * SUB + col] = acc;
-        }
-    }
-    __syncthreads();
-    // off-diagonal blocks, by distance d from the diagonal (the tasks of a level
-    // run on separate warps; split-tf32 products keep fp32-level accuracy):
-    //   X_IJ = -X_II * sum_{J <= K' < I} A_IK' X_K'J
-    for (int d = 1; d < NSUB; ++d) {
-        if (warp < NSUB - d) {
-            const int J = warp, I = J + d;
-            float* Y = s.T + warp * SUB * PA;   // per-warp [16][16] scratch (T is not yet in use)
-            float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-            const int r0 = I * SUB + gid, r1 = r0 + 8;
-            for (int ks = 2 * J; ks < 2 * I; ++ks) {
-                const int m0 = ks * 8 + tig, m1 = m0 + 4;
-                const Frag4 af = frag4(s.A[r0 * PA + m0], s.A[r1 * PA + m0], s.A[r0 * PA + m1], s.A[r1 * PA + m1]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int cc = J * SUB + nt * 8 + gid;
-                    mma3(acc[nt], af, frag2(s.X[m0 * PA + cc], s.X[m1 * PA + cc]));
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) Y[(gid + (e >> 1) * 8) * PA + nt * 8 + tig * 2 + (e & 1)] = acc[nt][e];
-            __syncwarp();
-            float xr[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-#pragma unroll
-            for (int ks = 0; ks < 2; ++ks) {
-                const int m0 = ks * 8 + tig, m1 = m0 + 4;
-                const Frag4 af = frag4(s.X[r0 * PA + I * SUB + m0], s.X[r1 * PA + I * SUB + m0],
-                                       s.X[r0 * PA + I * SUB + m1], s.X[r1 * PA + I * SUB + m1]);
-#pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int cc = nt * 8 + gid;
-                    mma3(xr[nt], af, frag2(Y[m0 * PA + cc], Y[m1 * PA + cc]));
-                }
-            }
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    s.X[(I * SUB + gid + (e >> 1) * 8) * PA + J * SUB + nt * 8 + tig * 2 + (e & 1)] = -xr[nt][e];
+    stage_tile(tile_i, ci, s.vb[0]);
+    float alog = alog_next;
+    uint16_t braw = braw_next;
+    int par = 0;
+    while (true) {
+        const int nxt = tile_i + step;
+        const ChunkInfo cn = nxt < ntiles ? chunks[nxt / H] : ChunkInfo{0, 0, 0, 0};
+        const int L = ci.L;
+        const float a_h = __expf(alog);
+        uint8_t* img = ws + lay.img + (size_t)tile_i * ImgOff::BYTES;
+        if (tid < C) s.braw[tid] = braw;
+        cp_async_wait_all();
+        __syncthreads();
+        {
+            RowRegsT<kIntraWarps> rr;
+            prep_load_staged(rr, stg, stg + C * D, stg + 2 * C * D, s.braw, s.dtb, L);
+            prep_compute(rr, nullptr, a_h, lb, L, 0, s.qe, s.ke, nullptr, s.kp, s.beta, nullptr, nullptr);
         }
         __syncthreads();
-    }
-    // T = X diag(beta); X and the zero upper blocks of B to the workspace
-    for (int idx = tid; idx < C * C; idx += blockDim.x) {
-        const int r = idx >> 6, cc = idx & 63;
-        s.T[r * PA + cc] = s.X[r * PA + cc] * s.beta[cc];
-    }
-    for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
-        const int r = idx >> 4, cc = (idx & 15) * 4;
-        *reinterpret_cast<float4*>(img + ImgOff::XM + (r * C + cc) * 4) = *reinterpret_cast<const float4*>(&s.X[r * PA + cc]);
-        if ((cc >> 4) > (r >> 4))
-            *reinterpret_cast<float4*>(img + ImgOff::BM + (r * C + cc) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    __syncthreads();
-
-    // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 32ch..)
-    {
-        const int rb = warp & 3, ch = warp >> 2;
-        float aw[4][4], au[4][4];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) { aw[nt][e] = 0.0f; au[nt][e] = 0.0f; }
-        const int ra = rb * SUB + gid, rbb = ra + 8;
-        for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
-            const int j0 = ks * 8 + tig, j1 = j0 + 4;
-            const Frag4 tf = frag4(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
-            const float* pb = s.fa.Pb[j0 >> 4];
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int c = ch * 32 + nt * 8 + gid;
-                mma3(aw[nt], tf, frag2(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
-                // v is bf16 data, exact in tf32
-                mma2a(au[nt], tf, tf32_bits(s.v[j0 * P + c]), tf32_bits(s.v[j1 * P + c]));
+        block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);
+        // zero the blocks above the diagonal of A, Aqk, X (the staged rows are consumed)
+        for (int idx = tid; idx < C * C; idx += blockDim.x) {
+            const int r = idx >> 6, cc = idx & 63;
+            if ((cc >> 4) > (r >> 4)) {
+                s.A[r * PA + cc] = 0.0f;
+                s.Aqk[r * PA + cc] = 0.0f;
+                s.X[r * PA + cc] = 0.0f;
             }
         }
-        float* gU = reinterpret_cast<float*>(img + ImgOff::U);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int row = rb * SUB + gid + hh * 8;
-                const int col = ch * 32 + nt * 8 + tig * 2;
-                const float w0 = tf32_round(aw[nt][hh * 2]), w1 = tf32_round(aw[nt][hh * 2 + 1]);
-                *reinterpret_cast<float2*>(img + ImgOff::W + panel_off(row, col, C)) = make_float2(w0, w1);
-                *reinterpret_cast<float*>(img + ImgOff::WT + panel_off(col, row, D)) = w0;
-                *reinterpret_cast<float*>(img + ImgOff::WT + panel_off(col + 1, row, D)) = w1;
-                *reinterpret_cast<float2*>(gU + row * D + col) = make_float2(au[nt][hh * 2], au[nt][hh * 2 + 1]);
-            }
-    }
+        __syncthreads();
+        block_factors(&s.fa);
+        __syncthreads();
 
-    // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G), Aqk, and their transposes
-    //      (16-byte stores: a 16-byte chunk of a panel row is 4 consecutive columns)
-    for (int idx = tid; idx < C * D / 4; idx += blockDim.x) {
-        const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
-        const float* pb = s.fa.Pb[r >> 4];
-        const float* sf = s.fa.Sf[r >> 4];
-        float4 qb, kb;
-        qb.x = tf32_round(s.qe[r * P + c] * pb[c]);         kb.x = tf32_round(s.kp[r * P + c] * sf[c]);
-        qb.y = tf32_round(s.qe[r * P + c + 1] * pb[c + 1]); kb.y = tf32_round(s.kp[r * P + c + 1] * sf[c + 1]);
-        qb.z = tf32_round(s.qe[r * P + c + 2] * pb[c + 2]); kb.z = tf32_round(s.kp[r * P + c + 2] * sf[c + 2]);
-        qb.w = tf32_round(s.qe[r * P + c + 3] * pb[c + 3]); kb.w = tf32_round(s.kp[r * P + c + 3] * sf[c + 3]);
-        *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
-        *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
-    }
-    for (int idx = tid; idx < C * D / 4; idx += blockDim.x) {
-        const int kk = idx >> 4, c = (idx & 15) * 4;         // [128][64], 4 columns (rows of the source) per thread
-        float4 qb, kb;
-        float* qp = &qb.x;
-        float* kp = &kb.x;
+        // ---- pairwise decayed products: all of A first (the solve needs it)
+        if (warp < 10) pair_task(0, warp, img);
+        else pair_task(1, warp - 10, img);
+        __syncthreads();
+
+        if (warp < NSUB) {
+            // ---- X = (I + A)^{-1}: diagonal 16x16 blocks by forward substitution
+            if (lane < SUB) {
+                const int I = warp, col = lane;
+                float x[SUB];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            qp[e] = tf32_round(scale * (s.qe[(c + e) * P + kk] * s.fa.Pb[(c + e) >> 4][kk]));
-            kp[e] = tf32_round(s.kp[(c + e) * P + kk] * s.fa.Sf[(c + e) >> 4][kk]);
+                for (int i = 0; i < SUB; ++i) {
+                    float acc = (i == col) ? 1.0f : 0.0f;
+#pragma unroll
+                    for (int m2 = 0; m2 < i; ++m2) acc -= s.A[(I * SUB + i) * PA + I * SUB + m2] * x[m2];
+                    x[i] = acc;
+                    s.X[(I * SUB + i) * PA + I * SUB + col] = acc;
+                }
+            }
+            bar_solve();
+            // off-diagonal blocks, by distance d from the diagonal (split-tf32 products
+            // keep fp32-level accuracy):  X_IJ = -X_II * sum_{J <= K' < I} A_IK' X_K'J
+            for (int d = 1; d < NSUB; ++d) {
+                if (warp < NSUB - d) {
+                    const int J = warp, I = J + d;
+                    float* Y = s.T + warp * SUB * PA;   // per-warp [16][16] scratch (T is not yet in use)
+                    float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+                    const int r0 = I * SUB + gid, r1 = r0 + 8;
+                    for (int ks = 2 * J; ks < 2 * I; ++ks) {
+                        const int m0 = ks * 8 + tig, m1 = m0 + 4;
+                        const Frag4 af =
+                            frag4(s.A[r0 * PA + m0], s.A[r1 * PA + m0], s.A[r0 * PA + m1], s.A[r1 * PA + m1]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int cc = J * SUB + nt * 8 + gid;
+                            mma3(acc[nt], af, frag2(s.X[m0 * PA + cc], s.X[m1 * PA + cc]));
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            Y[(gid + (e >> 1) * 8) * PA + nt * 8 + tig * 2 + (e & 1)] = acc[nt][e];
+                    __syncwarp();
+                    float xr[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
+#pragma unroll
+                    for (int ks = 0; ks < 2; ++ks) {
+                        const int m0 = ks * 8 + tig, m1 = m0 + 4;
+                        const Frag4 af = frag4(s.X[r0 * PA + I * SUB + m0], s.X[r1 * PA + I * SUB + m0],
+                                               s.X[r0 * PA + I * SUB + m1], s.X[r1 * PA + I * SUB + m1]);
+#pragma unroll
+                        for (int nt = 0; nt < 2; ++nt) {
+                            const int cc = nt * 8 + gid;
+                            mma3(xr[nt], af, frag2(Y[m0 * PA + cc], Y[m1 * PA + cc]));
+                        }
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            s.X[(I * SUB + gid + (e >> 1) * 8) * PA + J * SUB + nt * 8 + tig * 2 + (e & 1)] =
+                                -xr[nt][e];
+                }
+                bar_solve();
+            }
+        } else if (warp < 8) {
+            pair_task(1, 6 + warp - NSUB, img);
+        } else {
+            // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G) and their transposes
+            const int et = tid - 256, ew = warp - 8;
+            for (int idx = et; idx < C * D / 4; idx += 256) {
+                const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
+                const float* pb = s.fa.Pb[r >> 4];
+                const float* sf = s.fa.Sf[r >> 4];
+                float4 qb, kb;
+                qb.x = tf32_round(s.qe[r * P + c] * pb[c]);         kb.x = tf32_round(s.kp[r * P + c] * sf[c]);
+                qb.y = tf32_round(s.qe[r * P + c + 1] * pb[c + 1]); kb.y = tf32_round(s.kp[r * P + c + 1] * sf[c + 1]);
+                qb.z = tf32_round(s.qe[r * P + c + 2] * pb[c + 2]); kb.z = tf32_round(s.kp[r * P + c + 2] * sf[c + 2]);
+                qb.w = tf32_round(s.qe[r * P + c + 3] * pb[c + 3]); kb.w = tf32_round(s.kp[r * P + c + 3] * sf[c + 3]);
+                *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
+                *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
+            }
+            // transposes by 4x4 blocks: rows c0.. of the source, columns kk0..
+            for (int w2 = 0; w2 < 2; ++w2) {
+                const int wi = ew + 8 * w2;
+                const int kk0 = 4 * ((wi & 3) * 8 + (lane & 7)), c0 = 4 * ((wi >> 2) * 4 + (lane >> 3));
+                const float4 pb4 = *reinterpret_cast<const float4*>(&s.fa.Pb[c0 >> 4][kk0]);
+                const float4 sf4 = *reinterpret_cast<const float4*>(&s.fa.Sf[c0 >> 4][kk0]);
+                const float pbv[4] = {pb4.x, pb4.y, pb4.z, pb4.w}, sfv[4] = {sf4.x, sf4.y, sf4.z, sf4.w};
+                float qv[4][4], kv[4][4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float4 a = *reinterpret_cast<const float4*>(&s.qe[(c0 + e) * P + kk0]);
+                    const float4 b = *reinterpret_cast<const float4*>(&s.kp[(c0 + e) * P + kk0]);
+                    qv[e][0] = a.x; qv[e][1] = a.y; qv[e][2] = a.z; qv[e][3] = a.w;
+                    kv[e][0] = b.x; kv[e][1] = b.y; kv[e][2] = b.z; kv[e][3] = b.w;
+                }
+#pragma unroll
+                for (int e2 = 0; e2 < 4; ++e2) {
+                    float4 qb, kb;
+                    float* qp = &qb.x;
+                    float* kq = &kb.x;
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        qp[e] = tf32_round(scale * (qv[e][e2] * pbv[e2]));
+                        kq[e] = tf32_round(kv[e][e2] * sfv[e2]);
+                    }
+                    *reinterpret_cast<float4*>(img + ImgOff::QBT + panel_off(kk0 + e2, c0, D)) = qb;
+                    *reinterpret_cast<float4*>(img + ImgOff::KBT + panel_off(kk0 + e2, c0, D)) = kb;
+                }
+            }
+            if (et < D) reinterpret_cast<float*>(img + ImgOff::GAML)[et] = s.fa.gl[et];
         }
-        *reinterpret_cast<float4*>(img + ImgOff::QBT + panel_off(kk, c, D)) = qb;
-        *reinterpret_cast<float4*>(img + ImgOff::KBT + panel_off(kk, c, D)) = kb;
-    }
-    for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
-        const int r = idx >> 4, c = (idx & 15) * 4;
-        const float4 a = make_float4(tf32_round(s.Aqk[r * PA + c]), tf32_round(s.Aqk[r * PA + c + 1]),
-                                     tf32_round(s.Aqk[r * PA + c + 2]), tf32_round(s.Aqk[r * PA + c + 3]));
-        const float4 at = make_float4(tf32_round(scale * s.Aqk[c * PA + r]), tf32_round(scale * s.Aqk[(c + 1) * PA + r]),
-                                      tf32_round(scale * s.Aqk[(c + 2) * PA + r]),
-                                      tf32_round(scale * s.Aqk[(c + 3) * PA + r]));
-        *reinterpret_cast<float4*>(img + ImgOff::AQK + panel_off(r, c, C)) = a;
-        *reinterpret_cast<float4*>(img + ImgOff::AQKT + panel_off(r, c, C)) = at;
-    }
-    if (tid < D) reinterpret_cast<float*>(img + ImgOff::GAML)[tid] = s.fa.gl[tid];
-    __syncthreads();   // shared tiles are rewritten by the next tile
+        __syncthreads();
+
+        // T = X diag(beta); X, the zero upper blocks of B and the Aqk images to the workspace
+        for (int idx = tid; idx < C * C; idx += blockDim.x) {
+            const int r = idx >> 6, cc = idx & 63;
+            s.T[r * PA + cc] = s.X[r * PA + cc] * s.beta[cc];
+        }
+        for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
+            const int r = idx >> 4, cc = (idx & 15) * 4;
+            *reinterpret_cast<float4*>(img + ImgOff::XM + (r * C + cc) * 4) =
+                *reinterpret_cast<const float4*>(&s.X[r * PA + cc]);
+            if ((cc >> 4) > (r >> 4))
+                *reinterpret_cast<float4*>(img + ImgOff::BM + (r * C + cc) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float4 a = make_float4(tf32_round(s.Aqk[r * PA + cc]), tf32_round(s.Aqk[r * PA + cc + 1]),
+                                         tf32_round(s.Aqk[r * PA + cc + 2]), tf32_round(s.Aqk[r * PA + cc + 3]));
+            *reinterpret_cast<float4*>(img + ImgOff::AQK + panel_off(r, cc, C)) = a;
+        }
+        if (warp < 8) {
+            // (scale Aqk)^T by 4x4 blocks
+            const int r0 = 4 * ((warp & 1) * 8 + (lane & 7)), c0 = 4 * ((warp >> 1) * 4 + (lane >> 3));
+            float av[4][4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float4 a = *reinterpret_cast<const float4*>(&s.Aqk[(c0 + e) * PA + r0]);
+                av[e][0] = a.x; av[e][1] = a.y; av[e][2] = a.z; av[e][3] = a.w;
+            }
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float4 at = make_float4(tf32_round(scale * av[0][e2]), tf32_round(scale * av[1][e2]),
+                                              tf32_round(scale * av[2][e2]), tf32_round(scale * av[3][e2]));
+                *reinterpret_cast<float4*>(img + ImgOff::AQKT + panel_off(r0 + e2, c0, C)) = at;
+            }
+        }
+        __syncthreads();
+
+        // the next tile's rows stream in while W and U are formed
+        if (cn.L > 0) stage_tile(nxt, cn, s.vb[par ^ 1]);
+
+        // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 32ch..)
+        {
+            const uint16_t* vv = s.vb[par];
+            const int rb = warp & 3, ch = warp >> 2;
+            float aw[4][4], au[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) { aw[nt][e] = 0.0f; au[nt][e] = 0.0f; }
+            const int ra = rb * SUB + gid, rbb = ra + 8;
+            for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
+                const int j0 = ks * 8 + tig, j1 = j0 + 4;
+                const Frag4 tf = frag4(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
+                const float* pb = s.fa.Pb[j0 >> 4];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const int c = ch * 32 + nt * 8 + gid;
+                    mma3(aw[nt], tf, frag2(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
+                    // v is bf16 data: its fp32 bit pattern is exact in tf32
+                    mma2a(au[nt], tf, (uint32_t)vv[j0 * VP + c] << 16, (uint32_t)vv[j1 * VP + c] << 16);
+                }
+            }
+            float* gU = reinterpret_cast<float*>(img + ImgOff::U);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int row = rb * SUB + gid + hh * 8;
+                    const int col = ch * 32 + nt * 8 + tig * 2;
+                    const float w0 = tf32_round(aw[nt][hh * 2]), w1 = tf32_round(aw[nt][hh * 2 + 1]);
+                    *reinterpret_cast<float2*>(img + ImgOff::W + panel_off(row, col, C)) = make_float2(w0, w1);
+                    *reinterpret_cast<float*>(img + ImgOff::WT + panel_off(col, row, D)) = w0;
+                    *reinterpret_cast<float*>(img + ImgOff::WT + panel_off(col + 1, row, D)) = w1;
+                    *reinterpret_cast<float2*>(gU + row * D + col) = make_float2(au[nt][hh * 2], au[nt][hh * 2 + 1]);
+                }
+        }
+        if (cn.L <= 0) break;
+        tile_i = nxt;
+        ci = cn;
+        par ^= 1;
+        alog = alog_next;
+        braw = braw_next;
     }
 }
 

@@ -71,6 +71,32 @@ __device__ __forceinline__ void prep_load(RowRegsT<NW>& rr, const uint16_t* __re
     }
 }
 
+// The same rows taken from raw bf16 copies already in shared memory (q, k, g_raw
+// as [64][128], beta_raw [64], dt_bias [128] of the head; any may be null),
+// for kernels that stage a tile's inputs ahead of use. Filling the same
+// registers keeps prep_compute, and so every derived value, unchanged.
+template <int NW>
+__device__ __forceinline__ void prep_load_staged(RowRegsT<NW>& rr, const uint16_t* qs, const uint16_t* ks,
+                                                 const uint16_t* gs, const uint16_t* bs, const float* dtb, int L) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c0 = lane * 4;
+    rr.alog = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) rr.dt[e] = dtb ? dtb[c0 + e] : 0.0f;
+#pragma unroll
+    for (int b = 0; b < RowRegsT<NW>::RB; ++b) {
+        const int r = warp + b * NW;
+        rr.q[b] = rr.k[b] = rr.v[b] = rr.g[b] = make_uint2(0u, 0u);
+        rr.br[b] = 0.0f;
+        if (r < L) {
+            if (qs) rr.q[b] = *reinterpret_cast<const uint2*>(qs + r * D + c0);
+            if (ks) rr.k[b] = *reinterpret_cast<const uint2*>(ks + r * D + c0);
+            if (gs) rr.g[b] = *reinterpret_cast<const uint2*>(gs + r * D + c0);
+            if (bs && lane == 0) rr.br[b] = bf2f(bs[r]);
+        }
+    }
+}
+
 // Turns loaded rows into q^, k^, v, alpha, beta and 1/sqrt(|x|^2 + eps) in
 // shared memory (any output pointer may be null; rows >= L: zeros, alpha = 1,
 // beta = 0).
