@@ -9,6 +9,10 @@
 //   dA    = -strict_lower(X^T dT T^T),   dB = diag(beta) dA
 // Split-tf32 mma.sync on 16-row tiles (the gate gradient needs the extra
 // precision); dKt, dB and dbeta go to the workspace.
+// The raw k, v, g_raw rows of the CTA's next tile are staged by cp.async during
+// the second half of a tile, so the input preparation reads shared memory.
+// Warps take row blocks skewed by their index (block (w + w/4) mod 4), so the
+// triangular products spread over the four SM sub-partitions evenly.
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -17,19 +21,23 @@
 namespace kda {
 
 namespace {
+constexpr int VP = D + 8;   // bf16 row pitch of the staged v rows (conflict-free fragment loads)
 struct WySmem {
     float kt[C * PS];    // k^, then K^*Gamma
-    float v[C * PS];
     float dW[C * PS];    // alpha scratch, then dW, then M = dT T^T (stride PC)
-    float dU[C * PS];
+    float dU[C * PS];    // dU; after the dKt step the next tile's raw k, g_raw rows
+    uint16_t vb[2][C * VP];   // raw v rows (bf16, exact in tf32), by tile parity
     float X[C * PC];
     float B[C * PC];
     float T[C * PC];
     float dT[C * PC];    // dT, then dA
     Factors fa;
+    float dtb[D];        // dt_bias of the staged tile's head
     float beta[C];
     float dbeta[C];
+    uint16_t braw[C];
 };
+static_assert(C * PS * 4 >= 2 * C * D * 2, "the staged rows fit in dU");
 }  // namespace
 
 size_t bwd_wy_smem_bytes() { return sizeof(WySmem); }
@@ -48,34 +56,62 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     const int ntiles = (int)lay.nc_max * H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    // Persistent over tiles (tile = chunk * H + h); the next tile's rows are
-    // loaded into registers while the current one computes.
-    // chunk records are read two tiles ahead
+    // Persistent over tiles (tile = chunk * H + h). Empty chunk records only
+    // follow the last real chunk, so the first empty tile ends the CTA's work.
     const int step = (int)gridDim.x;
-    auto chunk_of = [&](int t) { return t < ntiles ? chunks[t / H] : ChunkInfo{0, 0, 0, 0}; };
-    ChunkInfo ci_next = chunk_of(blockIdx.x), ci_next2 = chunk_of(blockIdx.x + step);
-    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
-    const ChunkInfo ci = ci_next;
-    const int h = tile_i % H;
+    int tile_i = blockIdx.x;
+    ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
+    if (ci.L <= 0) return;
+    uint16_t* const stg = reinterpret_cast<uint16_t*>(s.dU);   // staged k, g_raw rows
+    float alog_next = 0.0f;
+    uint16_t braw_next = 0;
+    // raw rows of tile t_i (record cn) -> staging and vdst; rows past the chunk read as zero
+    auto stage_tile = [&](int t_i, const ChunkInfo& cn, uint16_t* vdst) {
+        const int hn = t_i % H;
+        for (int seg = tid; seg < 3 * C * (D / 8); seg += kWyWarps * 32) {
+            const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
+            const uint16_t* src = which == 0 ? k : which == 1 ? g_raw : v;
+            const bool valid = r < cn.L;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
+            uint16_t* dst = which < 2 ? stg + which * C * D + r * D + c8 : vdst + r * VP + c8;
+            cp_async16_zfill(dst, src, valid);
+        }
+        if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
+        cp_async_commit();
+        alog_next = A_log[hn];
+        if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
+    };
+    stage_tile(tile_i, ci, s.vb[0]);
+    float alog = alog_next;
+    uint16_t braw = braw_next;
+    int par = 0;
+    while (true) {
     const int nxt = tile_i + step;
-    ci_next = ci_next2;
-    ci_next2 = chunk_of(nxt + step);
-    if (ci.L <= 0) continue;
+    const ChunkInfo cn = nxt < ntiles ? chunks[nxt / H] : ChunkInfo{0, 0, 0, 0};
+    const int h = tile_i % H;
     const int L = ci.L;
     const size_t tile = (size_t)tile_i;
     const uint8_t* img = ws + lay.img + tile * ImgOff::BYTES;
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* gdU = ws + lay.dut + tile * kTileCK;
     uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
-    const float a_h = __expf(A_log[h]);
+    const float a_h = __expf(alog);
+    const uint16_t* vv = s.vb[par];
 
-    // dU, X, B arrive asynchronously while the rows are prepared
-    panels_to_smem_async(s.dU, PS, gdU);
+    if (tid < C) s.braw[tid] = braw;
+    cp_async_wait_all();
+    __syncthreads();
+    // X, B, then (once the staged rows are read) dU arrive while the rows are prepared
     tile_to_smem_async(s.X, PC, reinterpret_cast<const float*>(img + ImgOff::XM), C, C);
     tile_to_smem_async(s.B, PC, reinterpret_cast<const float*>(img + ImgOff::BM), C, C);
-    cp_async_commit();
-    prep_rows<kWyWarps>(nullptr, k, v, g_raw, beta_raw, dt_bias, a_h, lb, ci.t0, L, H, h, nullptr, s.kt, s.v, s.dW,
-                        s.beta, nullptr, nullptr);
+    {
+        RowRegsT<kWyWarps> rr;
+        prep_load_staged(rr, nullptr, stg, stg + C * D, s.braw, s.dtb, L);
+        __syncthreads();
+        panels_to_smem_async(s.dU, PS, gdU);
+        cp_async_commit();
+        prep_compute(rr, nullptr, a_h, lb, L, 0, nullptr, s.kt, nullptr, s.dW, s.beta, nullptr, nullptr);
+    }
     __syncthreads();
     block_products(s.dW, nullptr, s.kt, nullptr, nullptr, &s.fa);
     __syncthreads();
@@ -112,7 +148,8 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = ch * 16 + nt * 8 + gid;
                 mma3(acc[nt], wf, frag2(s.kt[j * PS + k0], s.kt[j * PS + k1]));
-                mma2a(acc[nt], uf, tf32_bits(s.v[j * PS + k0]), tf32_bits(s.v[j * PS + k1]));   // v: bf16, exact
+                // v is bf16 data: its fp32 bit pattern is exact in tf32
+                mma2a(acc[nt], uf, (uint32_t)vv[j * VP + k0] << 16, (uint32_t)vv[j * VP + k1] << 16);
             }
         }
 #pragma unroll
@@ -125,7 +162,7 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     }
     // dKt = T^T dW, dV = T^T dU   (rows j in 16jb, columns 32ch: 4 n-tiles); T[i][j] = 0 for i < j
     {
-        const int jb = warp & 3, ch = warp >> 2;
+        const int jb = (warp + (warp >> 2)) & 3, ch = warp >> 2;
         float ak[4][4], av[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -156,6 +193,8 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
             }
     }
     __syncthreads();
+    // k^, v and dU are no longer read: the next tile's rows stream in
+    if (cn.L > 0) stage_tile(nxt, cn, s.vb[par ^ 1]);
     // dbeta from T = X diag(beta); M = dT T^T into the dW buffer
     if (tid < C) {
         float acc = 0.0f;
@@ -192,7 +231,7 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     __syncthreads();
     // dA = -strict_lower(X^T M) into the dT buffer; X[m][i] = 0 for m < i
     {
-        const int ib = warp & 3, ch = warp >> 2;
+        const int ib = (warp + (warp >> 2)) & 3, ch = warp >> 2;
         float acc[2][4];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -227,7 +266,12 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         for (int j = 0; j < tid; ++j) acc += s.dT[tid * PC + j] * s.B[tid * PC + j];
         reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] = acc;
     }
-    __syncthreads();   // shared tiles are rewritten by the next tile
+    if (cn.L <= 0) break;
+    tile_i = nxt;
+    ci = cn;
+    par ^= 1;
+    alog = alog_next;
+    braw = braw_next;
     }
 }
 

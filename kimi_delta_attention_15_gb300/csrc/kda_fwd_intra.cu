@@ -335,7 +335,9 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         // ---- W = T (K^ * Gamma), U = T V   (rows 16rb.., columns 32ch..)
         {
             const uint16_t* vv = s.vb[par];
-            const int rb = warp & 3, ch = warp >> 2;
+            // row block skewed by the warp index: the triangular work spreads over
+            // the four SM sub-partitions (warp % 4) evenly
+            const int rb = (warp + (warp >> 2)) & 3, ch = warp >> 2;
             float aw[4][4], au[4][4];
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt)
