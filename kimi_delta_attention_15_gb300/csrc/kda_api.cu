@@ -257,7 +257,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
                                                                    ws, lay);
     prof(7, s);
     if (lay.nc_max > 0)
-        kda_bwd_pair_kernel<<<tiles, 512, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
+        kda_bwd_pair_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
                                                                        dq, dk, dg_raw, dbeta_raw, ws, lay);
     prof(8, s);
     kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);

@@ -17,6 +17,8 @@
 // which is the same sum without the cancellation of the Kbar terms.
 // Then du = dg lb s (1 - s), dg_raw = du exp(A_log), and the per-chunk
 // partial sums of ddt_bias and dA_log go to the workspace.
+// Persistent over tiles: at the start of a tile the CTA asks L2 for every
+// input of its next tile (bulk prefetches), so the loads of that tile hit L2.
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -52,13 +54,39 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     extern __shared__ uint8_t smem_raw[];
     PairSmem& s = *reinterpret_cast<PairSmem*>(smem_raw);
     if (read_status(ws) != 0) return;
-    const int chunk = blockIdx.x, h = blockIdx.y;
-    const ChunkInfo ci = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks)[chunk];
-    if (ci.L <= 0) return;
-    const int L = ci.L, t0 = ci.t0;
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int ntiles = (int)lay.nc_max * H;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const size_t tile = (size_t)chunk * H + h;
+    const int step = (int)gridDim.x;
+    // record of the next tile, read one tile ahead (empty records only follow the last chunk)
+    ChunkInfo cnext = (int)blockIdx.x + step < ntiles ? chunks[((int)blockIdx.x + step) / H] : ChunkInfo{0, 0, 0, 0};
+    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += step) {
+    const int chunk = tile_i / H, h = tile_i - chunk * H;
+    const ChunkInfo ci = chunks[chunk];
+    if (ci.L <= 0) break;
+    const int L = ci.L, t0 = ci.t0;
+    const size_t tile = (size_t)tile_i;
+    {
+        // L2 prefetch of the next tile: raw q, k, g_raw rows and its workspace inputs
+        const int nt_i = tile_i + step;
+        const ChunkInfo cn = cnext;
+        cnext = nt_i + step < ntiles ? chunks[(nt_i + step) / H] : ChunkInfo{0, 0, 0, 0};
+        if (cn.L > 0) {
+            const int nh = nt_i % H;
+            if (tid < 3 * C) {
+                const int which = tid >> 6, r = tid & (C - 1);
+                const uint16_t* src = which == 0 ? q : which == 1 ? k : g_raw;
+                if (r < cn.L) bulk_prefetch_l2(src + ((size_t)(cn.t0 + r) * H + nh) * D, 2 * D);
+            } else if (tid == 3 * C) {
+                const uint8_t* nbg = ws + lay.bg + (size_t)nt_i * BgOff::BYTES;
+                bulk_prefetch_l2(nbg + BgOff::DQB, (uint32_t)kTileCK);
+                bulk_prefetch_l2(nbg + BgOff::DKB, (uint32_t)(BgOff::DGAM + D * 4 - BgOff::DKB));
+            } else if (tid == 3 * C + 32) {
+                bulk_prefetch_l2(ws + lay.wy + (size_t)nt_i * WyOff::BYTES, (uint32_t)(WyOff::DBETA + C * 4));
+            }
+        }
+    }
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
     const float a_h = __expf(A_log[h]);
@@ -239,35 +267,56 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
             }
         }
     }
-    // dg: sums over rows per key channel (threads 0..127), written back as dg_t
+    // thread (row group rg, channel c) owns rows rg + RG b of channel c in the gate chain;
+    // its raw gates are loaded now, all at once
+    constexpr int RG = kPairWarps * 32 / D;   // row groups (threads per channel)
+    const int cc = tid & (D - 1), rg = tid >> 7;
+    uint16_t graw[C / RG];
+#pragma unroll
+    for (int b = 0; b < C / RG; ++b) {
+        const int r = rg + RG * b;
+        graw[b] = r < L ? g_raw[((size_t)(t0 + r) * H + h) * D + cc] : (uint16_t)0;
+    }
+    const float dtc = dt_bias[h * D + cc];
+    // dg: sums over rows per key channel, written back as dg_t
     //   dg_t = sum_{i>=t} dG'_i + sum_{i<t} dKbar_i Kbar_i + dgam exp(G_L)
+    // blocked over RG contiguous row segments of SEG rows: segment sums first (scratch in
+    // the dB tile, which is no longer read), then each segment from its offsets
     float* part = reinterpret_cast<float*>(ws + lay.part) + tile * (D + 4);
-    if (tid < D) {
-        const int c = tid;
-        const float dgam = reinterpret_cast<const float*>(bg + BgOff::DGAM)[c] * s.fa.gl[c];
-        float run = 0.0f;
-        for (int r = 0; r < L; ++r) {
-            const float p = s.em[r * PS + c];
-            s.em[r * PS + c] = run;
+    {
+        constexpr int SEG = C / RG;
+        float* segE = s.dB;            // [RG][128] sums of the dKbar Kbar terms
+        float* segK = s.dB + RG * D;   // [RG][128] sums of dG'
+        const int r0 = rg * SEG, r1 = min(r0 + SEG, L);
+        float se = 0.0f, sk = 0.0f;
+        for (int r = r0; r < r1; ++r) { se += s.em[r * PS + cc]; sk += s.kp[r * PS + cc]; }
+        segE[rg * D + cc] = se;
+        segK[rg * D + cc] = sk;
+        __syncthreads();
+        float run = 0.0f, rev = reinterpret_cast<const float*>(bg + BgOff::DGAM)[cc] * s.fa.gl[cc];
+        for (int g2 = 0; g2 < rg; ++g2) run += segE[g2 * D + cc];
+        for (int g2 = RG - 1; g2 > rg; --g2) rev += segK[g2 * D + cc];
+        for (int r = r0; r < r1; ++r) {
+            const float p = s.em[r * PS + cc];
+            s.em[r * PS + cc] = run;
             run += p;
         }
-        float rev = 0.0f;
-        for (int r = L - 1; r >= 0; --r) {
-            rev += s.kp[r * PS + c];
-            s.kp[r * PS + c] = rev + s.em[r * PS + c] + dgam;
+        for (int r = r1 - 1; r >= r0; --r) {
+            rev += s.kp[r * PS + cc];
+            s.kp[r * PS + cc] = rev + s.em[r * PS + cc];
         }
     }
     __syncthreads();
     // gate chain, every thread: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
     {
-        constexpr int RG = kPairWarps * 32 / D;   // row groups (threads per channel)
-        const int c = tid & (D - 1), r0 = tid >> 7;
-        const float dtc = dt_bias[h * D + c];
+        const int c = cc, r0 = rg;
         float ddt = 0.0f, dA = 0.0f;
-#pragma unroll 4
-        for (int r = r0; r < L; r += RG) {
+#pragma unroll
+        for (int b = 0; b < C / RG; ++b) {
+            const int r = r0 + RG * b;
+            if (r >= L) break;
             const size_t gi = ((size_t)(t0 + r) * H + h) * D + c;
-            const float x = bf2f(g_raw[gi]) + dtc;
+            const float x = bf2f(graw[b]) + dtc;
             const float dgr = s.kp[r * PS + c] * lb * dsigmoidf(a_h * x) * a_h;
             dg_raw[gi] = f2bf(dgr);
             ddt += dgr;
@@ -279,7 +328,6 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     }
     __syncthreads();
     if (tid < D) {
-        constexpr int RG = kPairWarps * 32 / D;
         float a = 0.0f, b = 0.0f;
 #pragma unroll
         for (int g = 0; g < RG; ++g) { a += s.em[g * PS + tid]; b += s.ep[g * PS + tid]; }
@@ -296,6 +344,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
         __syncthreads();
     }
     if (tid == 0) part[D] = s.red[0];
+    __syncthreads();   // shared tiles are rewritten by the next tile
+    }
 }
 
 // Deterministic sum of the per-chunk parameter partials, chunk order, per head.

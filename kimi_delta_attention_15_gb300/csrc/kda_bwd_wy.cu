@@ -4,7 +4,7 @@
 // kernel) and dU = dUt (backward scan):
 //   dT    = dW (K^*Gamma)^T + dU V^T
 //   dKt   = T^T dW        (adjoint of K^*Gamma)
-//   dV    = T^T dU        (final dv)
+//   dV    = T^T dU        (final dv; plain tf32, it feeds only the bf16 output)
 //   dbeta_j  = sum_i dT_ij X_ij + sum_l dA_jl B_jl
 //   dA    = -strict_lower(X^T dT T^T),   dB = diag(beta) dA
 // Split-tf32 mma.sync on 16-row tiles (the gate gradient needs the extra
@@ -78,6 +78,13 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         }
         if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
         cp_async_commit();
+        // the tile's workspace inputs (X, B images, dU, dW) are asked into L2 now
+        if (tid == D / 4) {
+            const uint8_t* nimg = ws + lay.img + (size_t)t_i * ImgOff::BYTES;
+            bulk_prefetch_l2(nimg + ImgOff::XM, (uint32_t)(2 * kTileCC));
+            bulk_prefetch_l2(ws + lay.dut + (size_t)t_i * kTileCK, (uint32_t)kTileCK);
+            bulk_prefetch_l2(ws + lay.bg + (size_t)t_i * BgOff::BYTES + BgOff::DW, (uint32_t)kTileCK);
+        }
         alog_next = A_log[hn];
         if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
     };
@@ -176,7 +183,9 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
             for (int nt = 0; nt < 4; ++nt) {
                 const int c = ch * 32 + nt * 8 + gid;
                 mma3(ak[nt], tf, frag2(s.dW[i0 * PS + c], s.dW[i1 * PS + c]));
-                mma3(av[nt], tf, frag2(s.dU[i0 * PS + c], s.dU[i1 * PS + c]));
+                // dV only feeds the bf16 output dv: one tf32 product is accurate enough
+                mma_tf32_16x8x8(av[nt], tf.hi[0], tf.hi[1], tf.hi[2], tf.hi[3], tf32_bits(s.dU[i0 * PS + c]),
+                                tf32_bits(s.dU[i1 * PS + c]));
             }
         }
         float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT);
