@@ -17,8 +17,7 @@
 // which is the same sum without the cancellation of the Kbar terms.
 // Then du = dg lb s (1 - s), dg_raw = du exp(A_log), and the per-chunk
 // partial sums of ddt_bias and dA_log go to the workspace.
-// Persistent over tiles: at the start of a tile the CTA asks L2 for every
-// input of its next tile (bulk prefetches), so the loads of that tile hit L2.
+// Persistent over tiles (one CTA per SM).
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -59,34 +58,13 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int step = (int)gridDim.x;
-    // record of the next tile, read one tile ahead (empty records only follow the last chunk)
-    ChunkInfo cnext = (int)blockIdx.x + step < ntiles ? chunks[((int)blockIdx.x + step) / H] : ChunkInfo{0, 0, 0, 0};
+    // empty chunk records only follow the last real chunk
     for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += step) {
     const int chunk = tile_i / H, h = tile_i - chunk * H;
     const ChunkInfo ci = chunks[chunk];
     if (ci.L <= 0) break;
     const int L = ci.L, t0 = ci.t0;
     const size_t tile = (size_t)tile_i;
-    {
-        // L2 prefetch of the next tile: raw q, k, g_raw rows and its workspace inputs
-        const int nt_i = tile_i + step;
-        const ChunkInfo cn = cnext;
-        cnext = nt_i + step < ntiles ? chunks[(nt_i + step) / H] : ChunkInfo{0, 0, 0, 0};
-        if (cn.L > 0) {
-            const int nh = nt_i % H;
-            if (tid < 3 * C) {
-                const int which = tid >> 6, r = tid & (C - 1);
-                const uint16_t* src = which == 0 ? q : which == 1 ? k : g_raw;
-                if (r < cn.L) bulk_prefetch_l2(src + ((size_t)(cn.t0 + r) * H + nh) * D, 2 * D);
-            } else if (tid == 3 * C) {
-                const uint8_t* nbg = ws + lay.bg + (size_t)nt_i * BgOff::BYTES;
-                bulk_prefetch_l2(nbg + BgOff::DQB, (uint32_t)kTileCK);
-                bulk_prefetch_l2(nbg + BgOff::DKB, (uint32_t)(BgOff::DGAM + D * 4 - BgOff::DKB));
-            } else if (tid == 3 * C + 32) {
-                bulk_prefetch_l2(ws + lay.wy + (size_t)nt_i * WyOff::BYTES, (uint32_t)(WyOff::DBETA + C * 4));
-            }
-        }
-    }
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
     const float a_h = __expf(A_log[h]);

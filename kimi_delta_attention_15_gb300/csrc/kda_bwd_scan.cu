@@ -117,22 +117,15 @@ __global__ void __launch_bounds__(256, 1)
             *reinterpret_cast<float4*>(s.DOT + panel_off(v, 32 * half + ii, D)) =
                 make_float4(bf2f(col[0]), bf2f(col[D]), bf2f(col[2 * D]), bf2f(col[3 * D]));
         }
-        // dS_L: TMEM -> tf32 operand, and dS_L^T [k][v] (tf32) to the workspace
-        // checkpoint; dS_L diag(exp(G_L)) back to TMEM
+        // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
         uint8_t* gDST = ws + lay.ds + tile * kTileDD;
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 q4 = make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]),
-                                              tf32_round(r[j + 3]));
-                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) = q4;
-                *reinterpret_cast<float*>(gDST + panel_off(c0 + j, v, D)) = q4.x;
-                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 1, v, D)) = q4.y;
-                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 2, v, D)) = q4.z;
-                *reinterpret_cast<float*>(gDST + panel_off(c0 + j + 3, v, D)) = q4.w;
-            }
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) =
+                    make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]), tf32_round(r[j + 3]));
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
             tmem_st32(tS + lane_base + c0, r);
@@ -159,6 +152,16 @@ __global__ void __launch_bounds__(256, 1)
                 umma_commit(&s.barM1);
             }
         }
+        // the dS_L^T checkpoint [k][v] (tf32, as the MMAs use it), read back from this
+        // thread's row of the operand tile while the tensor core works on it
+#pragma unroll 4
+        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 4) {
+            const float4 q4 = *reinterpret_cast<const float4*>(s.DS + panel_off(v, c0, D));
+            *reinterpret_cast<float*>(gDST + panel_off(c0, v, D)) = q4.x;
+            *reinterpret_cast<float*>(gDST + panel_off(c0 + 1, v, D)) = q4.y;
+            *reinterpret_cast<float*>(gDST + panel_off(c0 + 2, v, D)) = q4.z;
+            *reinterpret_cast<float*>(gDST + panel_off(c0 + 3, v, D)) = q4.w;
+        }
         ok = mbar_wait(&s.barM1, par) && ok;
         ok = __syncthreads_and(ok);
         if (!ok) break;
@@ -167,16 +170,14 @@ __global__ void __launch_bounds__(256, 1)
 
         // -dUt^T into the operand tile (reusing DOT); dUt (fp32) -> workspace [c][v] panels
         uint8_t* gdU = ws + lay.dut + tile * kTileCK;
+        float du[32];   // to the workspace once the state update is issued
         {
             const int c0 = 32 * half;
-            float r[32];
-            tmem_ld32(tU + lane_base + c0, r);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(c0 + j, v, C)) = r[j];
+            tmem_ld32(tU + lane_base + c0, du);
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(s.DOT + panel_off(v, c0 + j, D)) =
-                    make_float4(-tf32_round(r[j]), -tf32_round(r[j + 1]), -tf32_round(r[j + 2]), -tf32_round(r[j + 3]));
+                *reinterpret_cast<float4*>(s.DOT + panel_off(v, c0 + j, D)) = make_float4(
+                    -tf32_round(du[j]), -tf32_round(du[j + 1]), -tf32_round(du[j + 2]), -tf32_round(du[j + 3]));
         }
         fence_async_smem();
         tc_fence_before();
@@ -187,6 +188,8 @@ __global__ void __launch_bounds__(256, 1)
                 umma_tf32(tS, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.WT), D, ks), idN128, 1);
             umma_commit(&s.barM2);
         }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(32 * half + j, v, C)) = du[j];
         ok = mbar_wait(&s.barM2, par) && ok;
         ok = __syncthreads_and(ok);
         if (!ok) break;

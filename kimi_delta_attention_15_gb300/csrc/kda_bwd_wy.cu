@@ -78,13 +78,6 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         }
         if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
         cp_async_commit();
-        // the tile's workspace inputs (X, B images, dU, dW) are asked into L2 now
-        if (tid == D / 4) {
-            const uint8_t* nimg = ws + lay.img + (size_t)t_i * ImgOff::BYTES;
-            bulk_prefetch_l2(nimg + ImgOff::XM, (uint32_t)(2 * kTileCC));
-            bulk_prefetch_l2(ws + lay.dut + (size_t)t_i * kTileCK, (uint32_t)kTileCK);
-            bulk_prefetch_l2(ws + lay.bg + (size_t)t_i * BgOff::BYTES + BgOff::DW, (uint32_t)kTileCK);
-        }
         alog_next = A_log[hn];
         if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
     };

@@ -11,6 +11,9 @@
 // chunk, rounded to tf32 as the MMAs use it, is checkpointed to the
 // workspace for the backward as S0^T (key-major panels, the operand layout the
 // backward's state products use), together with Ut (fp32).
+// The MMAs with S0 read it from a tf32 copy in tensor memory (A operand in
+// TMEM), which leaves shared memory for two W, Q^*Gamma buffers: those operands
+// are requested two chunks ahead.
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
@@ -19,15 +22,13 @@ namespace kda {
 namespace {
 struct ScanSmem {
     // operand tiles, 1024-byte aligned (panels)
-    uint8_t S0[kTileDD];       // [128 v][128 k]
-    uint8_t W[kTileCK];        // [64 c][128 k]     \ one bulk group
-    uint8_t QB[kTileCK];       // [64 c][128 k]     /
+    uint8_t WQ[2][2 * kTileCK];   // W [64 c][128 k] then QB [64 c][128 k]: one bulk group, by chunk parity
     uint8_t KBT[kTileCK];      // [128 k][64 c]     \ one bulk group
     uint8_t AQK[kTileCC];      // [64 i][64 j]      /
     uint8_t UT[kTileCK];       // [128 v][64 c]; between the state update and the next
                                // chunk's Ut also the bf16 output rows [64 i][128 v]
     float gam[D];
-    uint64_t barA, barB, barM1, barM2;
+    uint64_t barA[2], barB, barM1, barM2;
     uint32_t tmem;
 };
 }  // namespace
@@ -51,18 +52,18 @@ __global__ void __launch_bounds__(256, 1)
     const size_t sidx = ((size_t)n * H + h) * D * D;
 
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&s.barA, 1); mbar_init(&s.barB, 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
+        mbar_init(&s.barA[0], 1); mbar_init(&s.barA[1], 1); mbar_init(&s.barB, 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = s.tmem;
-    const uint32_t tS = tm, tUT = tm + 128, tOT = tm + 192;
+    const uint32_t tS = tm, tUT = tm + 128, tOT = tm + 192, tS0 = tm + 256;   // tS0: tf32 copy of S0
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     // initial state into TMEM
@@ -73,18 +74,25 @@ __global__ void __launch_bounds__(256, 1)
         tmem_st32(tS + lane_base + c0, r);
     }
 
+    // W, QB of chunk cf + i go to buffer i & 1 and complete phase (i >> 1) of barA[i & 1]
     auto issue_A = [&](int chunk) {
+        const int b = (chunk - cf) & 1;
         const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
-        mbar_arrive_expect_tx(&s.barA, (uint32_t)(2 * kTileCK));
-        bulk_g2s(s.W, img + ImgOff::W, (uint32_t)(2 * kTileCK), &s.barA);
+        mbar_arrive_expect_tx(&s.barA[b], (uint32_t)(2 * kTileCK));
+        bulk_g2s(s.WQ[b], img + ImgOff::W, (uint32_t)(2 * kTileCK), &s.barA[b]);
     };
     auto issue_B = [&](int chunk) {
         const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
         mbar_arrive_expect_tx(&s.barB, (uint32_t)(kTileCK + kTileCC));
         bulk_g2s(s.KBT, img + ImgOff::KBT, (uint32_t)(kTileCK + kTileCC), &s.barB);
     };
-    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;   // bulk groups (thread 0)
-    if (tid == 0 && cf < cl) { issue_A(cf); issue_B(cf); a_issued = b_issued = 1; }
+    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;   // bulk groups (thread 0), in chunk order
+    if (tid == 0 && cf < cl) {
+        issue_A(cf);
+        issue_B(cf);
+        a_issued = b_issued = 1;
+        if (cf + 1 < cl) { issue_A(cf + 1); a_issued = 2; }
+    }
 
     bool ok = true;
     const uint32_t idS0W = idesc_tf32(128, 64, 0, 0);
@@ -120,40 +128,35 @@ __global__ void __launch_bounds__(256, 1)
         __syncthreads();
         store_o_rows();
 
-        // S0: TMEM -> registers -> tf32 operand in smem, and its transpose S0^T [k][v]
-        // (tf32) to the workspace checkpoint; decayed state back to TMEM
+        // S0: TMEM -> registers -> tf32 copy in TMEM (the MMA operand), and its transpose
+        // S0^T [k][v] to the workspace checkpoint; decayed state back to TMEM
         uint8_t* gS0T = ws + lay.s0 + tile * kTileDD;
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-            float r[32];
+            float r[32], q[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4) {
-                const float4 q4 = make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]),
-                                              tf32_round(r[j + 3]));
-                *reinterpret_cast<float4*>(s.S0 + panel_off(v, c0 + j, D)) = q4;
-                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j, v, D)) = q4.x;
-                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 1, v, D)) = q4.y;
-                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 2, v, D)) = q4.z;
-                *reinterpret_cast<float*>(gS0T + panel_off(c0 + j + 3, v, D)) = q4.w;
-            }
+            for (int j = 0; j < 32; ++j) q[j] = tf32_round(r[j]);
+            tmem_st32(tS0 + lane_base + c0, q);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gS0T + panel_off(c0 + j, v, D)) = q[j];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
             tmem_st32(tS + lane_base + c0, r);
         }
-        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
 
+        const int ab = (chunk - cf) & 1;
         if (tid == 0) {
-            if (!mbar_wait(&s.barA, par)) ok = false;
+            if (!mbar_wait(&s.barA[ab], (uint32_t)(((chunk - cf) >> 1) & 1))) ok = false;
             else ++a_done;
             if (ok) {
-                const uint32_t a = smem_u32(s.S0), bw = smem_u32(s.W), bq = smem_u32(s.QB);
+                const uint32_t bw = smem_u32(s.WQ[ab]), bq = bw + (uint32_t)kTileCK;
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_tf32(tUT, desc_kmajor(a, D, ks), desc_kmajor(bw, C, ks), idS0W, ks > 0);
+                    umma_tf32_ta(tUT, tS0 + 8 * ks, desc_kmajor(bw, C, ks), idS0W, ks > 0);
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_tf32(tOT, desc_kmajor(a, D, ks), desc_kmajor(bq, C, ks), idS0W, ks > 0);
+                    umma_tf32_ta(tOT, tS0 + 8 * ks, desc_kmajor(bq, C, ks), idS0W, ks > 0);
                 umma_commit(&s.barM1);
             }
         }
@@ -166,7 +169,7 @@ __global__ void __launch_bounds__(256, 1)
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && chunk + 1 < cl) { issue_A(chunk + 1); ++a_issued; }
+        if (tid == 0 && chunk + 2 < cl) { issue_A(chunk + 2); ++a_issued; }   // into this chunk's buffer
 
         // Ut^T = U^T - S0 W^T  -> tf32 operand [v][c]; Ut (fp32) -> workspace [c][v] panels
         uint8_t* gUt = ws + lay.ut + tile * kTileCK;
@@ -233,13 +236,13 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (tid == 0) {
         // drain copies still in flight (only after an aborted scan), bounded
-        for (; a_done < a_issued; ++a_done) mbar_wait(&s.barA, (uint32_t)(a_done & 1));
+        for (; a_done < a_issued; ++a_done) mbar_wait(&s.barA[a_done & 1], (uint32_t)((a_done >> 1) & 1));
         for (; b_done < b_issued; ++b_done) mbar_wait(&s.barB, (uint32_t)(b_done & 1));
         bulk_wait_all();
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 }  // namespace kda
