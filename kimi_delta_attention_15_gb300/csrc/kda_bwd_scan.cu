@@ -8,6 +8,11 @@
 //   S_L = S0 diag(exp(G_L)) + Ut^T (K^*e^{G_L-G}).
 // dS_L^T of every chunk (tf32, as the MMAs use it) and dUt (fp32) are stored in the
 // workspace for the per-chunk backward kernels; dh0 = dS at the sequence start.
+// dS_L enters the MMA from a tf32 copy in tensor memory (A operand in TMEM). The
+// two products with A = dO^T run as one MMA over stacked B operands:
+//   dUt^T = dS_L KB^T;  [dUt^T | dS] += dO^T [scale Aqk ; Q^*Gamma]      (N = 192)
+// so TMEM holds dUt^T (columns 0..63), dS (64..191), tf32 dS_L (256..383). W^T, used
+// by the second MMA only, is double-buffered and requested two chunks ahead.
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
@@ -15,15 +20,14 @@ namespace kda {
 
 namespace {
 struct BScanSmem {
-    uint8_t DS[kTileDD];     // dS_L operand [128 v][128 k]
-    uint8_t WT[kTileCK];     // W^T    [128 k][64 c]     bulk group Y (second MMA group)
-    uint8_t QBT[kTileCK];    // QB^T   [128 k][64 i]   \ bulk group X (first MMA group)
-    uint8_t KB[kTileCK];     // KB     [64 c][128 k]   |
-    uint8_t AQKT[kTileCC];   // Aqk^T  [64 j][64 i]    /
+    uint8_t WT[2][kTileCK];  // W^T [128 k][64 c]: bulk group Y (second MMA), by chunk parity
+    // [Aqk^T ; QB^T] as one 192-row operand: panel p = Aqk^T rows (8 KB) then QB^T rows (16 KB)
+    uint8_t AQ[kTileCK + kTileCC];   // \ bulk group X (first MMA)
+    uint8_t KB[kTileCK];             // / KB [64 c][128 k]
     uint8_t DOT[kTileCK];    // dO^T [128 v][64 i], then -dUt^T [128 v][64 c]
     uint16_t DO[C * D];      // dO rows of the next chunk as stored (bf16 [64 i][128 v]), cp.async
     float gam[D];
-    uint64_t barX, barY, barM1, barM2;
+    uint64_t barX, barY[2], barM1, barM2;
     uint32_t tmem;
 };
 }  // namespace
@@ -47,18 +51,18 @@ __global__ void __launch_bounds__(256, 1)
     const size_t sidx = ((size_t)n * H + h) * D * D;
 
     if (warp == 0) {
-        tmem_alloc(&s.tmem, 256);
+        tmem_alloc(&s.tmem, 512);
         tmem_relinquish();
     }
     if (tid == 0) {
-        mbar_init(&s.barX, 1); mbar_init(&s.barY, 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
+        mbar_init(&s.barX, 1); mbar_init(&s.barY[0], 1); mbar_init(&s.barY[1], 1); mbar_init(&s.barM1, 1); mbar_init(&s.barM2, 1);
         fence_mbar_init();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = s.tmem;
-    const uint32_t tS = tm, tU = tm + 128;
+    const uint32_t tU = tm, tS = tm + 64, tDS = tm + 256;   // tDS: tf32 copy of dS_L
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
@@ -70,19 +74,32 @@ __global__ void __launch_bounds__(256, 1)
 
     auto img_of = [&](int chunk) { return ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES; };
     auto issue_X = [&](int chunk) {
+        const uint8_t* img = img_of(chunk);
         mbar_arrive_expect_tx(&s.barX, (uint32_t)(2 * kTileCK + kTileCC));
-        bulk_g2s(s.QBT, img_of(chunk) + ImgOff::QBT, (uint32_t)(2 * kTileCK + kTileCC), &s.barX);
+        for (int p = 0; p < 2; ++p) {
+            bulk_g2s(s.AQ + p * (C + D) * 128, img + ImgOff::AQKT + p * C * 128, C * 128, &s.barX);
+            bulk_g2s(s.AQ + p * (C + D) * 128 + C * 128, img + ImgOff::QBT + p * D * 128, D * 128, &s.barX);
+        }
+        bulk_g2s(s.KB, img + ImgOff::KB, (uint32_t)kTileCK, &s.barX);
     };
+    // W^T of the i-th chunk from the end goes to buffer i & 1, phase (i >> 1) of barY[i & 1]
     auto issue_Y = [&](int chunk) {
-        mbar_arrive_expect_tx(&s.barY, (uint32_t)kTileCK);
-        bulk_g2s(s.WT, img_of(chunk) + ImgOff::WT, (uint32_t)kTileCK, &s.barY);
+        const int b = (cl - 1 - chunk) & 1;
+        mbar_arrive_expect_tx(&s.barY[b], (uint32_t)kTileCK);
+        bulk_g2s(s.WT[b], img_of(chunk) + ImgOff::WT, (uint32_t)kTileCK, &s.barY[b]);
     };
-    int x_issued = 0, y_issued = 0, x_done = 0, y_done = 0;
-    if (tid == 0 && cf < cl) { issue_X(cl - 1); issue_Y(cl - 1); x_issued = y_issued = 1; }
+    int x_issued = 0, y_issued = 0, x_done = 0, y_done = 0;   // in chunk order (thread 0)
+    if (tid == 0 && cf < cl) {
+        issue_X(cl - 1);
+        issue_Y(cl - 1);
+        x_issued = y_issued = 1;
+        if (cl - 2 >= cf) { issue_Y(cl - 2); y_issued = 2; }
+    }
 
     bool ok = true;
     const uint32_t idN64 = idesc_tf32(128, 64, 0, 0);
     const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
+    const uint32_t idN192 = idesc_tf32(128, 192, 0, 0);
     // dO rows of a chunk -> s.DO (rows past the chunk's end read as zero); 16 bytes per
     // copy, four copies per thread, issued one chunk ahead of use
     auto issue_dO = [&](const ChunkInfo& c2) {
@@ -117,15 +134,17 @@ __global__ void __launch_bounds__(256, 1)
             *reinterpret_cast<float4*>(s.DOT + panel_off(v, 32 * half + ii, D)) =
                 make_float4(bf2f(col[0]), bf2f(col[D]), bf2f(col[2 * D]), bf2f(col[3 * D]));
         }
-        // dS_L: TMEM -> tf32 operand; dS_L diag(exp(G_L)) back to TMEM
+        // dS_L: TMEM -> tf32 copy in TMEM (the MMA operand), and dS_L^T [k][v] to the
+        // workspace checkpoint; dS_L diag(exp(G_L)) back to TMEM
         uint8_t* gDST = ws + lay.ds + tile * kTileDD;
         for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-            float r[32];
+            float r[32], q[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(s.DS + panel_off(v, c0 + j, D)) =
-                    make_float4(tf32_round(r[j]), tf32_round(r[j + 1]), tf32_round(r[j + 2]), tf32_round(r[j + 3]));
+            for (int j = 0; j < 32; ++j) q[j] = tf32_round(r[j]);
+            tmem_st32(tDS + lane_base + c0, q);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gDST + panel_off(c0 + j, v, D)) = q[j];
 #pragma unroll
             for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
             tmem_st32(tS + lane_base + c0, r);
@@ -136,31 +155,18 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         if (chunk - 1 >= cf) issue_dO(ci_prev);   // every thread is past its reads of s.DO
         if (tid == 0) {
-            const bool gx = mbar_wait(&s.barX, par), gy = gx && mbar_wait(&s.barY, par);
-            x_done += gx; y_done += gy;
-            if (!gx || !gy) ok = false;
+            if (!mbar_wait(&s.barX, par)) ok = false;
+            else ++x_done;
             if (ok) {
-                const uint32_t aD = smem_u32(s.DOT), aS = smem_u32(s.DS);
-                // dUt^T = dO^T (scale Aqk) + dS_L KB^T
-                for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32(tU, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.AQKT), C, ks), idN64, ks > 0);
+                // dUt^T = dS_L KB^T
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_tf32(tU, desc_kmajor(aS, D, ks), desc_kmajor(smem_u32(s.KB), C, ks), idN64, 1);
-                // dS += dO^T (scale QB)
+                    umma_tf32_ta(tU, tDS + 8 * ks, desc_kmajor(smem_u32(s.KB), C, ks), idN64, ks > 0);
+                // [dUt^T | dS] += dO^T [scale Aqk ; scale QB]
                 for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32(tS, desc_kmajor(aD, D, ks), desc_kmajor(smem_u32(s.QBT), D, ks), idN128, 1);
+                    umma_tf32(tU, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.AQ), C + D, ks),
+                              idN192, 1);
                 umma_commit(&s.barM1);
             }
-        }
-        // the dS_L^T checkpoint [k][v] (tf32, as the MMAs use it), read back from this
-        // thread's row of the operand tile while the tensor core works on it
-#pragma unroll 4
-        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 4) {
-            const float4 q4 = *reinterpret_cast<const float4*>(s.DS + panel_off(v, c0, D));
-            *reinterpret_cast<float*>(gDST + panel_off(c0, v, D)) = q4.x;
-            *reinterpret_cast<float*>(gDST + panel_off(c0 + 1, v, D)) = q4.y;
-            *reinterpret_cast<float*>(gDST + panel_off(c0 + 2, v, D)) = q4.z;
-            *reinterpret_cast<float*>(gDST + panel_off(c0 + 3, v, D)) = q4.w;
         }
         ok = mbar_wait(&s.barM1, par) && ok;
         ok = __syncthreads_and(ok);
@@ -183,10 +189,16 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
+        const int yb = (cl - 1 - chunk) & 1;
         if (tid == 0) {
-            for (int ks = 0; ks < C / 8; ++ks)
-                umma_tf32(tS, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.WT), D, ks), idN128, 1);
-            umma_commit(&s.barM2);
+            if (!mbar_wait(&s.barY[yb], (uint32_t)(((cl - 1 - chunk) >> 1) & 1))) ok = false;
+            else ++y_done;
+            if (ok) {
+                for (int ks = 0; ks < C / 8; ++ks)
+                    umma_tf32(tS, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.WT[yb]), D, ks),
+                              idN128, 1);
+                umma_commit(&s.barM2);
+            }
         }
 #pragma unroll
         for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gdU + panel_off(32 * half + j, v, C)) = du[j];
@@ -194,7 +206,7 @@ __global__ void __launch_bounds__(256, 1)
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && chunk - 1 >= cf) { issue_Y(chunk - 1); ++y_issued; }
+        if (tid == 0 && chunk - 2 >= cf) { issue_Y(chunk - 2); ++y_issued; }   // into this chunk's buffer
     }
     if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
     if (ok && dh0) {
@@ -207,13 +219,13 @@ __global__ void __launch_bounds__(256, 1)
     }
     if (tid == 0) {
         for (; x_done < x_issued; ++x_done) mbar_wait(&s.barX, (uint32_t)(x_done & 1));
-        for (; y_done < y_issued; ++y_done) mbar_wait(&s.barY, (uint32_t)(y_done & 1));
+        for (; y_done < y_issued; ++y_done) mbar_wait(&s.barY[y_done & 1], (uint32_t)((y_done >> 1) & 1));
         bulk_wait_all();
     }
     cp_async_wait_all();   // dO copies still in flight (only after an aborted scan)
     tc_fence_before();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tm, 256);
+    if (warp == 0) tmem_dealloc(tm, 512);
 }
 
 }  // namespace kda

@@ -13,7 +13,11 @@
 // backward's state products use), together with Ut (fp32).
 // The MMAs with S0 read it from a tf32 copy in tensor memory (A operand in
 // TMEM), which leaves shared memory for two W, Q^*Gamma buffers: those operands
-// are requested two chunks ahead.
+// are requested two chunks ahead. Products that share their A operand run as
+// one wide MMA over stacked B operands (panels interleaved in shared memory):
+//   [Ut^T | O^T]   = S0 [W ; Q^*Gamma]^T                 (N = 128)
+//   [O^T | S_L]   += Ut^T [Aqk ; (K^*e^{G_L-G})^T]^T     (N = 192)
+// so TMEM holds Ut^T (columns 0..63), O^T (64..127), S (128..255), tf32 S0 (256..383).
 #include "kda_internal.cuh"
 #include "umma.cuh"
 
@@ -22,9 +26,10 @@ namespace kda {
 namespace {
 struct ScanSmem {
     // operand tiles, 1024-byte aligned (panels)
-    uint8_t WQ[2][2 * kTileCK];   // W [64 c][128 k] then QB [64 c][128 k]: one bulk group, by chunk parity
-    uint8_t KBT[kTileCK];      // [128 k][64 c]     \ one bulk group
-    uint8_t AQK[kTileCC];      // [64 i][64 j]      /
+    // [W ; QB] as one 128-row operand: panel p = W rows (8 KB) then QB rows (8 KB); by chunk parity
+    uint8_t WQ[2][2 * kTileCK];
+    // [Aqk ; KBT] as one 192-row operand: panel p = Aqk rows (8 KB) then KBT rows (16 KB)
+    uint8_t AK[kTileCK + kTileCC];
     uint8_t UT[kTileCK];       // [128 v][64 c]; between the state update and the next
                                // chunk's Ut also the bf16 output rows [64 i][128 v]
     float gam[D];
@@ -63,7 +68,7 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tm = s.tmem;
-    const uint32_t tS = tm, tUT = tm + 128, tOT = tm + 192, tS0 = tm + 256;   // tS0: tf32 copy of S0
+    const uint32_t tUT = tm, tOT = tm + 64, tS = tm + 128, tS0 = tm + 256;   // tS0: tf32 copy of S0
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     // initial state into TMEM
@@ -79,12 +84,18 @@ __global__ void __launch_bounds__(256, 1)
         const int b = (chunk - cf) & 1;
         const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
         mbar_arrive_expect_tx(&s.barA[b], (uint32_t)(2 * kTileCK));
-        bulk_g2s(s.WQ[b], img + ImgOff::W, (uint32_t)(2 * kTileCK), &s.barA[b]);
+        for (int p = 0; p < 4; ++p) {
+            bulk_g2s(s.WQ[b] + p * 2 * C * 128, img + ImgOff::W + p * C * 128, C * 128, &s.barA[b]);
+            bulk_g2s(s.WQ[b] + p * 2 * C * 128 + C * 128, img + ImgOff::QB + p * C * 128, C * 128, &s.barA[b]);
+        }
     };
     auto issue_B = [&](int chunk) {
         const uint8_t* img = ws + lay.img + ((size_t)chunk * H + h) * ImgOff::BYTES;
         mbar_arrive_expect_tx(&s.barB, (uint32_t)(kTileCK + kTileCC));
-        bulk_g2s(s.KBT, img + ImgOff::KBT, (uint32_t)(kTileCK + kTileCC), &s.barB);
+        for (int p = 0; p < 2; ++p) {
+            bulk_g2s(s.AK + p * (C + D) * 128, img + ImgOff::AQK + p * C * 128, C * 128, &s.barB);
+            bulk_g2s(s.AK + p * (C + D) * 128 + C * 128, img + ImgOff::KBT + p * D * 128, D * 128, &s.barB);
+        }
     };
     int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;   // bulk groups (thread 0), in chunk order
     if (tid == 0 && cf < cl) {
@@ -95,8 +106,8 @@ __global__ void __launch_bounds__(256, 1)
     }
 
     bool ok = true;
-    const uint32_t idS0W = idesc_tf32(128, 64, 0, 0);
-    const uint32_t idS = idesc_tf32(128, 128, 0, 0);
+    const uint32_t idN128 = idesc_tf32(128, 128, 0, 0);
+    const uint32_t idN192 = idesc_tf32(128, 192, 0, 0);
     // per-chunk scalars are fetched one chunk ahead
     ChunkInfo ci_next = cf < cl ? chunks[cf] : ChunkInfo{0, 0, 0, 0};
     float gam_next = cf < cl ? reinterpret_cast<const float*>(ws + lay.img + ((size_t)cf * H + h) * ImgOff::BYTES +
@@ -152,11 +163,9 @@ __global__ void __launch_bounds__(256, 1)
             if (!mbar_wait(&s.barA[ab], (uint32_t)(((chunk - cf) >> 1) & 1))) ok = false;
             else ++a_done;
             if (ok) {
-                const uint32_t bw = smem_u32(s.WQ[ab]), bq = bw + (uint32_t)kTileCK;
+                const uint32_t bwq = smem_u32(s.WQ[ab]);
                 for (int ks = 0; ks < D / 8; ++ks)
-                    umma_tf32_ta(tUT, tS0 + 8 * ks, desc_kmajor(bw, C, ks), idS0W, ks > 0);
-                for (int ks = 0; ks < D / 8; ++ks)
-                    umma_tf32_ta(tOT, tS0 + 8 * ks, desc_kmajor(bq, C, ks), idS0W, ks > 0);
+                    umma_tf32_ta(tUT, tS0 + 8 * ks, desc_kmajor(bwq, 2 * C, ks), idN128, ks > 0);
                 umma_commit(&s.barM1);
             }
         }
@@ -194,11 +203,9 @@ __global__ void __launch_bounds__(256, 1)
             if (!mbar_wait(&s.barB, par)) ok = false;
             else ++b_done;
             if (ok) {
-                const uint32_t a = smem_u32(s.UT), bq = smem_u32(s.AQK), bk = smem_u32(s.KBT);
+                const uint32_t a = smem_u32(s.UT), bak = smem_u32(s.AK);
                 for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32(tOT, desc_kmajor(a, D, ks), desc_kmajor(bq, C, ks), idS0W, 1);
-                for (int ks = 0; ks < C / 8; ++ks)
-                    umma_tf32(tS, desc_kmajor(a, D, ks), desc_kmajor(bk, D, ks), idS, 1);
+                    umma_tf32(tOT, desc_kmajor(a, D, ks), desc_kmajor(bak, C + D, ks), idN192, 1);
                 umma_commit(&s.barM2);
             }
         }
