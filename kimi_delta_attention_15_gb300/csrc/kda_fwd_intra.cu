@@ -22,13 +22,15 @@
 // preparation reads shared memory instead of waiting on global loads:
 //   prep (staged rows) -> block products -> factors
 //   pairs: warps 0..9 the ten A blocks, warps 10..15 six Aqk blocks
-//   warps 0..3 solve (I + A)^{-1} | warps 4..7 the other four Aqk blocks |
-//     warps 8..15 the elementwise images
+//   warps 0..3 solve (I + A)^{-1} | warps 4..11 the other four Aqk blocks, by
+//     halves (8 columns each) | warps 12..15 the elementwise images
 //   T, X and Aqk images; then next tile's rows -> staging; W, U
 #include "kda_internal.cuh"
 #include "mma_sync.cuh"
 #include "umma.cuh"
 #include "kda_prep.cuh"
+
+#include <type_traits>
 
 namespace kda {
 
@@ -103,14 +105,19 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
     };
 
-    // one 16x16 block of A (m = 0) or Aqk (m = 1), tf32 split products
-    auto pair_task = [&](int m, int t, uint8_t* img) {
+    // NTN n-tiles (8 columns each, from n-tile nt0) of one 16x16 block of A (m = 0)
+    // or Aqk (m = 1), tf32 split products
+    auto pair_task = [&](auto ntn, int m, int t, uint8_t* img, int nt0) {
+        constexpr int NTN = decltype(ntn)::value;
         int I, J;
         tri_pair(t, I, J);
         const float* base = m == 0 ? s.ke : s.qe;
         const float* f = s.fa.F[I][J];
-        float acc[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};
-        float acc2[2][4] = {{0, 0, 0, 0}, {0, 0, 0, 0}};   // second chain: odd k-steps
+        float acc[NTN][4], acc2[NTN][4];   // acc2: second chain, odd k-steps
+#pragma unroll
+        for (int nt = 0; nt < NTN; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.0f;
         const int r0 = I * SUB + gid, r1 = r0 + 8;
 #pragma unroll 2
         for (int ks = 0; ks < D / 8; ks += 2) {
@@ -121,22 +128,22 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
                 const Frag4 af = frag4(base[r0 * P + k0] * f0, base[r1 * P + k0] * f0, base[r0 * P + k1] * f1,
                                        base[r1 * P + k1] * f1);
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
-                    const int j = J * SUB + nt * 8 + gid;
+                for (int nt = 0; nt < NTN; ++nt) {
+                    const int j = J * SUB + (nt0 + nt) * 8 + gid;
                     mma3(u == 0 ? acc[nt] : acc2[nt], af, frag2(s.kp[j * P + k0], s.kp[j * P + k1]));
                 }
             }
         }
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const int row = I * SUB + gid + (e >> 1) * 8;
-                const int col = J * SUB + nt * 8 + tig * 2 + (e & 1);
+                const int col = J * SUB + (nt0 + nt) * 8 + tig * 2 + (e & 1);
                 const float val = acc[nt][e];
                 if (m == 0) {
                     const float b = col < row ? val : 0.0f;
@@ -182,8 +189,10 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         __syncthreads();
 
         // ---- pairwise decayed products: all of A first (the solve needs it)
-        if (warp < 10) pair_task(0, warp, img);
-        else pair_task(1, warp - 10, img);
+        using Two = std::integral_constant<int, 2>;
+        using One = std::integral_constant<int, 1>;
+        if (warp < 10) pair_task(Two{}, 0, warp, img, 0);
+        else pair_task(Two{}, 1, warp - 10, img, 0);
         __syncthreads();
 
         if (warp < NSUB) {
@@ -246,12 +255,12 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
                 }
                 bar_solve();
             }
-        } else if (warp < 8) {
-            pair_task(1, 6 + warp - NSUB, img);
+        } else if (warp < 12) {
+            pair_task(One{}, 1, 6 + ((warp - NSUB) >> 1), img, (warp - NSUB) & 1);
         } else {
             // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G) and their transposes
-            const int et = tid - 256, ew = warp - 8;
-            for (int idx = et; idx < C * D / 4; idx += 256) {
+            const int et = tid - 384, ew = warp - 12;
+            for (int idx = et; idx < C * D / 4; idx += 128) {
                 const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
                 const float* pb = s.fa.Pb[r >> 4];
                 const float* sf = s.fa.Sf[r >> 4];
@@ -264,8 +273,8 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
                 *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
             }
             // transposes by 4x4 blocks: rows c0.. of the source, columns kk0..
-            for (int w2 = 0; w2 < 2; ++w2) {
-                const int wi = ew + 8 * w2;
+            for (int w2 = 0; w2 < 4; ++w2) {
+                const int wi = ew + 4 * w2;
                 const int kk0 = 4 * ((wi & 3) * 8 + (lane & 7)), c0 = 4 * ((wi >> 2) * 4 + (lane >> 3));
                 const float4 pb4 = *reinterpret_cast<const float4*>(&s.fa.Pb[c0 >> 4][kk0]);
                 const float4 sf4 = *reinterpret_cast<const float4*>(&s.fa.Sf[c0 >> 4][kk0]);

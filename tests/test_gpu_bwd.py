@@ -49,6 +49,17 @@ def test_fwd_bwd_packed_with_empty_and_tiny_sequences():
         np.testing.assert_array_equal(out["dh0"][n].cpu().numpy(), dhT[n])
 
 
+def test_fwd_bwd_many_short_packed_sequences():
+    # 200 sequences of 0..70 tokens: more chunk x head tiles than SMs, so the
+    # persistent kernels run several tiles each and reach the empty chunk slots
+    # that follow the last real chunk of a packed batch
+    rng = np.random.default_rng(14)
+    lengths = tuple(int(x) for x in rng.integers(0, 71, size=200))
+    inp = I.make_inputs(I.custom(lengths, 2, h0=True, dhT=True), seed=14)
+    out = run_fwd_bwd(inp)
+    _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
+
+
 def test_strong_decay_gate():
     inp = I.make_inputs(I.custom((256,), 2, g_std=4.0, h0=True, dhT=True), seed=12)
     inp["A_log"] = torch.full((2,), float(np.log(16.0)))
