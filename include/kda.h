@@ -188,6 +188,17 @@ int kda_diag_umma_selftest(int a_mn, int b_mn, int N, int Kd, const float* A, co
  * context stays usable afterwards. */
 int kda_diag_wait_timeout(unsigned long long limit_ns, void* workspace, void* stream);
 
+/* Diagnostics: for each of the n floats in `in` (device memory) writes the
+ * library's own tf32 rounding to `out` and the hardware conversion
+ * cvt.rna.tf32.f32 (round to nearest, ties away from zero) to `ref` (device
+ * memory, n floats each, caller-owned). The kernels round tf32 operands with
+ * integer operations (add half a tf32 unit in the last place to the magnitude
+ * bits unless the value is a NaN, clear the 13 bits below tf32); the tests use
+ * this entry point to check that it equals the hardware conversion bit for
+ * bit on every input. n < 0 gives
+ * KDA_ERR_SHAPE, a null pointer (n > 0) KDA_ERR_NULL. */
+int kda_diag_tf32_round(const float* in, float* out, float* ref, long long n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -96,7 +96,29 @@ __global__ void wait_timeout_kernel(uint64_t limit_ns, uint8_t* status_word) {
     if (!ok && threadIdx.x == 0) raise_status(status_word, KDA_ERR_TIMEOUT);
 }
 
+// Both tf32 roundings of each input: the library's (tf32_round, integer operations)
+// and the hardware conversion cvt.rna.tf32.f32 it stands in for.
+__global__ void tf32_round_kernel(const float* __restrict__ in, float* __restrict__ out,
+                                  float* __restrict__ ref, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+        const float x = in[i];
+        uint32_t r;
+        asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+        out[i] = tf32_round(x);
+        ref[i] = __uint_as_float(r);
+    }
+}
+
 }  // namespace kda
+
+extern "C" int kda_diag_tf32_round(const float* in, float* out, float* ref, long long n, void* stream) {
+    if (n < 0) return KDA_ERR_SHAPE;
+    if (n == 0) return KDA_OK;
+    if (!in || !out || !ref) return KDA_ERR_NULL;
+    const long long blocks = (n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096;
+    kda::tf32_round_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(in, out, ref, (int64_t)n);
+    return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
 
 extern "C" int kda_diag_wait_timeout(unsigned long long limit_ns, void* workspace, void* stream) {
     if (!workspace) return KDA_ERR_NULL;

@@ -10,10 +10,10 @@
 
 namespace kda {
 
+// x rounded to tf32 (nearest, ties away from zero), as bits: the same rounding as
+// tf32_round_bits in umma.cuh, and as the cvt.rna.tf32.f32 conversion
 __device__ __forceinline__ uint32_t tf32_bits(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return r;
+    return (__float_as_uint(x) + (x != x ? 0u : 0x1000u)) & 0xffffe000u;
 }
 
 __device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
@@ -29,15 +29,16 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], uint32_t a0, uint
 
 namespace kda {
 
-// Split-tf32 ("3xTF32") products: x = hi + lo with hi = tf32(x), lo = tf32(x - hi),
-// and a*b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps about 21 bits of the
-// fp32 operands instead of 10. Used where the gate gradient needs more than tf32.
+// Split-tf32 ("3xTF32") products: x = hi + lo exactly, hi = x with the 13 mantissa
+// bits below tf32 cleared, lo = x - hi (exact in fp32; the tensor core reads its top
+// 19 bits), and a*b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps about 20 bits of
+// the fp32 operands instead of 10. Used where the gate gradient needs more than tf32.
 struct Frag4 { uint32_t hi[4], lo[4]; };
 struct Frag2 { uint32_t hi[2], lo[2]; };
 
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
-    hi = tf32_bits(x);
-    lo = tf32_bits(x - __uint_as_float(hi));
+    hi = __float_as_uint(x) & 0xffffe000u;
+    lo = __float_as_uint(x - __uint_as_float(hi));
 }
 __device__ __forceinline__ Frag4 frag4(float a0, float a1, float a2, float a3) {
     Frag4 f;

@@ -240,10 +240,16 @@ __device__ __forceinline__ uint64_t desc_mnmajor(uint32_t tile_saddr, uint32_t R
     return sdesc_sw128(tile_saddr + (c0 >> 5) * R * 128u + s * 1024u, R * 128u, 1024u);
 }
 
-__device__ __forceinline__ float tf32_round(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+// Round to the nearest tf32 value, ties away from zero, exactly as the
+// cvt.rna.tf32.f32 conversion does: add half a tf32 unit in the last place to the
+// magnitude bits, then clear the 13 bits below tf32 (a carry runs into the
+// exponent as it should; infinities stay infinite). A NaN is not rounded, only
+// cleared, like the conversion does, so its sign and upper payload are kept. A few
+// integer operations in place of the conversion (checked bit for bit against it
+// by kda_diag_tf32_round).
+__device__ __forceinline__ uint32_t tf32_round_bits(float x) {
+    return (__float_as_uint(x) + (x != x ? 0u : 0x1000u)) & 0xffffe000u;
 }
+__device__ __forceinline__ float tf32_round(float x) { return __uint_as_float(tf32_round_bits(x)); }
 
 }  // namespace kda

@@ -77,6 +77,8 @@ def load(build_if_missing: bool = True):
         lib.kda_diag_wait_timeout.restype = ctypes.c_int
         lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
         lib.kda_diag_umma_selftest.restype = ctypes.c_int
+        lib.kda_diag_tf32_round.argtypes = [P, P, P, ctypes.c_longlong, P]
+        lib.kda_diag_tf32_round.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -194,6 +196,15 @@ def device_status(workspace, stream=None) -> int:
 def wait_timeout(workspace, limit_ns: int = 20_000_000):
     """Diagnostic: a kernel whose wait runs out sets KDA_ERR_TIMEOUT in `workspace`."""
     _check(load().kda_diag_wait_timeout(limit_ns, _ptr(workspace), _stream_handle()), "kda_diag_wait_timeout")
+
+
+def tf32_round_check(x):
+    """Diagnostics: (library rounding, hardware cvt.rna) of a float32 CUDA tensor."""
+    x = x.contiguous()
+    out, ref = torch.empty_like(x), torch.empty_like(x)
+    _check(load().kda_diag_tf32_round(_ptr(x), _ptr(out), _ptr(ref), x.numel(), _stream_handle()),
+           "kda_diag_tf32_round")
+    return out, ref
 
 
 def umma_selftest(A, B, a_mn: int, b_mn: int):
