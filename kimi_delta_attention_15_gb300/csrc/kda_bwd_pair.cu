@@ -90,43 +90,43 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
 #pragma unroll
         for (int e = 0; e < 4; ++e) { adq[nt][e] = 0.0f; adk[nt][e] = 0.0f; adg[nt][e] = 0.0f; }
 
-    // (a) row side: rows of block I = rb, columns blocks J <= I
+    // (a) row side: rows of block I = rb, column blocks J <= I; the products with dB
+    // and with dAqk share their B fragments (k^ E+ of block J) and the decay R
     {
         const int I = rb;
-        for (int m = 0; m < 2; ++m) {
-            const float* dM = m == 0 ? s.dB : s.dA;
-            const float* base = m == 0 ? s.ke : s.qe;
-            for (int J = 0; J <= I; ++J) {
-                float acc[NT][4];
+        const int r0 = I * SUB + gid, r1 = r0 + 8;
+        for (int J = 0; J <= I; ++J) {
+            float accB[NT][4], accA[NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
+                for (int e = 0; e < 4; ++e) accB[nt][e] = accA[nt][e] = 0.0f;
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
-                    const int r0 = I * SUB + gid, r1 = r0 + 8;
-                    const Frag4 af = frag4(dM[r0 * PC + j0], dM[r1 * PC + j0], dM[r0 * PC + j1], dM[r1 * PC + j1]);
+            for (int kk = 0; kk < 2; ++kk) {
+                const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
+                const Frag4 fb = frag4(s.dB[r0 * PC + j0], s.dB[r1 * PC + j0], s.dB[r0 * PC + j1], s.dB[r1 * PC + j1]);
+                const Frag4 fa = frag4(s.dA[r0 * PC + j0], s.dA[r1 * PC + j0], s.dA[r0 * PC + j1], s.dA[r1 * PC + j1]);
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int c = ch * 32 + nt * 8 + gid;
-                        mma3(acc[nt], af, frag2(s.kp[j0 * PS + c], s.kp[j1 * PS + c]));
-                    }
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int c = ch * 32 + nt * 8 + gid;
+                    const Frag2 kb = frag2(s.kp[j0 * PS + c], s.kp[j1 * PS + c]);
+                    mma3(accB[nt], fb, kb);
+                    mma3(accA[nt], fa, kb);
                 }
-                const float* f = s.fa.F[I][J];
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
-                        const float fc = f[col];
-                        const float R = s.em[row * PS + col] * fc;
-                        const float Xt = base[row * PS + col] * fc;
-                        if (m == 0) adk[nt][e] += R * acc[nt][e];
-                        else adq[nt][e] += R * acc[nt][e];
-                        adg[nt][e] += Xt * acc[nt][e];
-                    }
             }
+            const float* f = s.fa.F[I][J];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
+                    const float fc = f[col];
+                    const float R = s.em[row * PS + col] * fc;
+                    adk[nt][e] += R * accB[nt][e];
+                    adq[nt][e] += R * accA[nt][e];
+                    adg[nt][e] += (s.ke[row * PS + col] * fc) * accB[nt][e];
+                    adg[nt][e] += (s.qe[row * PS + col] * fc) * accA[nt][e];
+                }
         }
     }
     // (b) column side: rows j of block J = rb, row blocks I >= J
