@@ -48,12 +48,11 @@ KERNEL_MODEL = {
 }
 
 # DRAM traffic per tile (dram__bytes_read.sum + dram__bytes_write.sum, one ncu capture
-# on T=4096 H=32, 2,048 tiles; profiles/kernels_fixed_T4096_H32.md). Valid only for the
-# kernel sources it was measured on: `sources` is a hash of csrc/, checked at run time.
+# on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
+# `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "beb975906222fd6e",
-    "per_tile": {"fwd_intra": 332168, "fwd_scan": 244300, "bwd_scan": 211651, "bwd_state": 311142,
-                 "bwd_wy": 200034, "bwd_pair": 222258},
+    "sources": "58d20b74434467d3",
+    "per_tile": {"fwd_intra": 333472, "fwd_scan": 244155, "bwd_scan": 211569, "bwd_state": 309004, "bwd_wy": 198715, "bwd_pair": 222264},
 }
 
 
