@@ -72,6 +72,23 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     tile_to_smem_async(s.dB, PC, reinterpret_cast<const float*>(wy + WyOff::DB), C, C);
     tile_to_smem_async(s.dA, PC, reinterpret_cast<const float*>(bg + BgOff::DAQK), C, C);
     cp_async_commit();
+    // each warp owns rows 16rb + {gid, gid+8}, columns 32ch + 8nt + 2tig + {0,1}
+    const int rb = warp & 3, ch = warp >> 2;
+    constexpr int NT = 4;   // n-tiles of 8 columns per warp
+    // operands of the elementwise terms (dQbar, dKt) of this thread's elements: loaded
+    // now, so that their latency hides under the row preparation
+    const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB);
+    const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB);
+    const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT);
+    float2 eQ[NT][2], eKt[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
+            eQ[nt][hh] = *reinterpret_cast<const float2*>(gdQ + row * D + col);
+            eKt[nt][hh] = *reinterpret_cast<const float2*>(gdKt + row * D + col);
+        }
     prep_rows<kPairWarps>(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp,
                           s.beta, s.inq, s.ink);
     cp_async_wait_all();
@@ -81,14 +98,26 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     block_factors(&s.fa);
     __syncthreads();
 
-    // each warp owns rows 16rb + {gid, gid+8}, columns 32ch + 8nt + 2tig + {0,1}
-    const int rb = warp & 3, ch = warp >> 2;
-    constexpr int NT = 4;   // n-tiles of 8 columns per warp
+    // (c) elementwise terms of Q^*Gamma and K^*Gamma start the accumulators (the Kbar terms
+    // follow the pair products, from an L2-warm reload of dKbar)
     float adq[NT][4], adk[NT][4], adg[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) { adq[nt][e] = 0.0f; adk[nt][e] = 0.0f; adg[nt][e] = 0.0f; }
+        for (int hh = 0; hh < 2; ++hh) {
+            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
+            const float dQv[2] = {eQ[nt][hh].x, eQ[nt][hh].y}, dKtv[2] = {eKt[nt][hh].x, eKt[nt][hh].y};
+#pragma unroll
+            for (int e2 = 0; e2 < 2; ++e2) {
+                const int e = hh * 2 + e2, cc = col + e2, I = row >> 4;
+                const float pb = s.fa.Pb[I][cc];
+                const float gam = s.em[row * PS + cc] * pb;
+                const float qb = s.qe[row * PS + cc] * pb, kt = s.ke[row * PS + cc] * pb;
+                adq[nt][e] = dQv[e2] * gam;
+                adk[nt][e] = dKtv[e2] * gam;
+                adg[nt][e] = dQv[e2] * qb + dKtv[e2] * kt;
+            }
+        }
 
     // (a) row side: rows of block I = rb, column blocks J <= I; the products with dB
     // and with dAqk share their B fragments (k^ E+ of block J) and the decay R
@@ -165,30 +194,21 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
                 adg[nt][e] -= s.kp[row * PS + col] * acc[nt][e];
             }
     }
-    // (c) elementwise terms of Q^*Gamma, K^*Gamma, Kbar
-    const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB);
-    const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB);
-    const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT);
+    // (c) elementwise terms of Kbar
     float pk[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
-            const float2 dQ2 = *reinterpret_cast<const float2*>(gdQ + row * D + col);
             const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
-            const float2 dKt2 = *reinterpret_cast<const float2*>(gdKt + row * D + col);
-            const float dQv[2] = {dQ2.x, dQ2.y}, dKbv[2] = {dKb2.x, dKb2.y}, dKtv[2] = {dKt2.x, dKt2.y};
+            const float dKbv[2] = {dKb2.x, dKb2.y};
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
                 const int e = hh * 2 + e2, cc = col + e2, I = row >> 4;
-                const float pb = s.fa.Pb[I][cc], sf = s.fa.Sf[I][cc];
-                const float gam = s.em[row * PS + cc] * pb;
-                const float qb = s.qe[row * PS + cc] * pb, kt = s.ke[row * PS + cc] * pb;
+                const float sf = s.fa.Sf[I][cc];
                 const float el = s.ep[row * PS + cc] * sf, kb = s.kp[row * PS + cc] * sf;
-                adq[nt][e] += dQv[e2] * gam;
-                adk[nt][e] += dKtv[e2] * gam + dKbv[e2] * el;
-                adg[nt][e] += dQv[e2] * qb + dKtv[e2] * kt;
+                adk[nt][e] += dKbv[e2] * el;
                 pk[nt][e] = dKbv[e2] * kb;
             }
         }
