@@ -17,7 +17,9 @@
 // which is the same sum without the cancellation of the Kbar terms.
 // Then du = dg lb s (1 - s), dg_raw = du exp(A_log), and the per-chunk
 // partial sums of ddt_bias and dA_log go to the workspace.
-// Persistent over tiles (one CTA per SM).
+// Persistent over tiles (one CTA per SM). The raw q, k, g_raw rows of the CTA's next
+// tile are staged by cp.async in the dAqk and E+ tiles, which are free from the
+// write-back of the adjoints to the end of the tile.
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -37,7 +39,10 @@ struct PairSmem {
     Factors fa;
     float beta[C], inq[C], ink[C];
     float red[D];
+    float dtb[D];        // dt_bias of the staged tile's head
+    uint16_t braw[C];    // beta_raw of the current tile
 };
+static_assert(C * PC * 4 >= C * D * 2 && C * PS * 4 >= 2 * C * D * 2, "the staged rows fit in dA and ep");
 }  // namespace
 
 size_t bwd_pair_smem_bytes() { return sizeof(PairSmem); }
@@ -58,17 +63,50 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
     const int step = (int)gridDim.x;
-    // empty chunk records only follow the last real chunk
-    for (int tile_i = blockIdx.x; tile_i < ntiles; tile_i += step) {
+    // empty chunk records only follow the last real chunk: the first one ends the CTA's work
+    int tile_i = blockIdx.x;
+    ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
+    if (ci.L <= 0) return;
+    uint16_t* const stq = reinterpret_cast<uint16_t*>(s.dA);   // staged q rows
+    uint16_t* const stk = reinterpret_cast<uint16_t*>(s.ep);   // staged k rows, then g_raw rows
+    float alog_next = 0.0f;
+    uint16_t braw_next = 0;
+    // raw rows of tile t_i (record cn) -> staging; rows past the chunk read as zero
+    auto stage_tile = [&](int t_i, const ChunkInfo& cn) {
+        const int hn = t_i % H;
+        for (int seg = tid; seg < 3 * C * (D / 8); seg += kPairWarps * 32) {
+            const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
+            const uint16_t* src = which == 0 ? q : which == 1 ? k : g_raw;
+            const bool valid = r < cn.L;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
+            uint16_t* dst = which == 0 ? stq + r * D + c8 : stk + (which - 1) * C * D + r * D + c8;
+            cp_async16_zfill(dst, src, valid);
+        }
+        if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
+        cp_async_commit();
+        alog_next = A_log[hn];
+        if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
+    };
+    stage_tile(tile_i, ci);
+    float alog = alog_next;
+    uint16_t braw = braw_next;
+    while (true) {
+    const int nxt = tile_i + step;
+    const ChunkInfo cn = nxt < ntiles ? chunks[nxt / H] : ChunkInfo{0, 0, 0, 0};
     const int chunk = tile_i / H, h = tile_i - chunk * H;
-    const ChunkInfo ci = chunks[chunk];
-    if (ci.L <= 0) break;
     const int L = ci.L, t0 = ci.t0;
     const size_t tile = (size_t)tile_i;
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
-    const float a_h = __expf(A_log[h]);
+    const float a_h = __expf(alog);
+    (void)chunk;
 
+    if (tid < C) s.braw[tid] = braw;
+    cp_async_wait_all();
+    __syncthreads();
+    RowRegsT<kPairWarps> rr;
+    prep_load_staged(rr, stq, stk, stk + C * D, s.braw, s.dtb, L);
+    __syncthreads();   // the staged rows are read: dA is reloaded and ep rewritten below
     tile_to_smem_async(s.dB, PC, reinterpret_cast<const float*>(wy + WyOff::DB), C, C);
     tile_to_smem_async(s.dA, PC, reinterpret_cast<const float*>(bg + BgOff::DAQK), C, C);
     cp_async_commit();
@@ -89,8 +127,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
             eQ[nt][hh] = *reinterpret_cast<const float2*>(gdQ + row * D + col);
             eKt[nt][hh] = *reinterpret_cast<const float2*>(gdKt + row * D + col);
         }
-    prep_rows<kPairWarps>(q, k, nullptr, g_raw, beta_raw, dt_bias, a_h, lb, t0, L, H, h, s.qe, s.ke, nullptr, s.kp,
-                          s.beta, s.inq, s.ink);
+    prep_compute(rr, nullptr, a_h, lb, L, 0, s.qe, s.ke, nullptr, s.kp, s.beta, s.inq, s.ink);
     cp_async_wait_all();
     __syncthreads();
     block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);
@@ -224,6 +261,8 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
             s.em[row * PS + col] = pk[nt][e];
         }
     __syncthreads();
+    // dA and ep are no longer read: the next tile's rows stream in during the chains below
+    if (cn.L > 0) stage_tile(nxt, cn);
 
     // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); all rows of a warp loaded at once
     {
@@ -321,14 +360,14 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
             dA += dgr * x;
         }
         // RG threads per channel (rows r = r0 mod RG); combined below in a fixed order
-        s.em[r0 * PS + c] = ddt;
-        s.ep[r0 * PS + c] = dA;
+        s.dB[(2 * RG + r0) * D + c] = ddt;
+        s.dB[(3 * RG + r0) * D + c] = dA;
     }
     __syncthreads();
     if (tid < D) {
         float a = 0.0f, b = 0.0f;
 #pragma unroll
-        for (int g = 0; g < RG; ++g) { a += s.em[g * PS + tid]; b += s.ep[g * PS + tid]; }
+        for (int g = 0; g < RG; ++g) { a += s.dB[(2 * RG + g) * D + tid]; b += s.dB[(3 * RG + g) * D + tid]; }
         part[tid] = a;
         s.red[tid] = b;
     }
@@ -342,7 +381,11 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
         __syncthreads();
     }
     if (tid == 0) part[D] = s.red[0];
-    __syncthreads();   // shared tiles are rewritten by the next tile
+    if (cn.L <= 0) break;
+    tile_i = nxt;
+    ci = cn;
+    alog = alog_next;
+    braw = braw_next;
     }
 }
 
