@@ -319,13 +319,18 @@ def run_gb300(args, ws, rank, local):
 
 
 def e2e(args, inp, dev, w):
-    """Same metric with host buffers: H2D of every input from pinned memory,
-    kda_fwd + kda_bwd, D2H of the output and every gradient, all timed."""
+    """Same metric with host buffers: every step copies all of its inputs from pinned
+    host memory to the device, runs kda_fwd + kda_bwd, and copies the output and every
+    gradient back, all inside the timed region. Reported two ways:
+      pipelined (the `value`): inputs of step n+1 go up on one copy stream and results
+        of step n-1 come down on another while the kernels of step n run (two device
+        input buffers), as a training loop streaming batches from the host would;
+      serial: copy in, compute, copy out, one after the other on one stream."""
     import torch
     from kimi_delta_attention_15_gb300 import ops
     names = ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias", "do")
     host = {k: inp[k].pin_memory() for k in names}
-    dv = {k: torch.empty_like(host[k], device=dev) for k in names}
+    dvs = [{k: torch.empty_like(host[k], device=dev) for k in names} for _ in range(2)]
     cu = inp["cu_seqlens"].to(dev) if w.packed else None
     shape = ops.make_shape(w.T, w.H, w.N)
     wsp = ops.alloc_workspace(shape, dev)
@@ -334,31 +339,80 @@ def e2e(args, inp, dev, w):
         out_host["d" + k] = torch.empty_like(host[k]).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    stream = torch.cuda.current_stream()
+    comp = torch.cuda.current_stream()
+    up, down = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def step():
-        for k in names:
-            dv[k].copy_(host[k], non_blocking=True)
+    def compute(dv):
         o, _, _ = ops.fwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"],
                           cu_seqlens=cu, workspace=wsp, want_hT=False)
         g = ops.bwd(dv["q"], dv["k"], dv["v"], dv["g_raw"], dv["beta_raw"], dv["A_log"], dv["dt_bias"], dv["do"],
                     wsp, cu_seqlens=cu, want_dh0=False)
-        out_host["o"].copy_(o, non_blocking=True)
-        for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias"):
-            out_host["d" + k].copy_(g["d" + k], non_blocking=True)
+        res = {"o": o}
+        res.update({"d" + k: g["d" + k] for k in ("q", "k", "v", "g_raw", "beta_raw", "A_log", "dt_bias")})
+        return res
+
+    def copy_down(res):
+        for k, t in res.items():
+            t.record_stream(down)
+            out_host[k].copy_(t, non_blocking=True)
+
+    def serial_step():
+        dv = dvs[0]
+        for k in names:
+            dv[k].copy_(host[k], non_blocking=True)
+        res = compute(dv)
+        for k, t in res.items():
+            out_host[k].copy_(t, non_blocking=True)
+
+    def pipelined(nsteps):
+        free = [torch.cuda.Event(), torch.cuda.Event()]   # compute done reading buffer b
+        for ev in free:
+            ev.record(comp)
+        ready = [torch.cuda.Event(), torch.cuda.Event()]  # inputs of buffer b on the device
+
+        def upload(i):
+            b = i % 2
+            up.wait_event(free[b])
+            with torch.cuda.stream(up):
+                for k in names:
+                    dvs[b][k].copy_(host[k], non_blocking=True)
+                ready[b].record(up)
+
+        upload(0)
+        for i in range(nsteps):
+            b = i % 2
+            if i + 1 < nsteps:
+                upload(i + 1)
+            comp.wait_event(ready[b])
+            res = compute(dvs[b])
+            free[b].record(comp)
+            done = torch.cuda.Event()
+            done.record(comp)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                copy_down(res)
+        comp.wait_stream(down)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(comp)
+        up.wait_stream(comp)
+        down.wait_stream(comp)
+        fn()
+        e.record(comp)
+        e.synchronize()
+        return s.elapsed_time(e) / args.steps
 
     for _ in range(max(1, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    s.record(stream)
-    for _ in range(args.steps):
-        step()
-    e.record(stream)
-    e.synchronize()
-    ms = s.elapsed_time(e) / args.steps
+        serial_step()
+    pipelined(max(2, args.warmup))
+    ms_serial = timed(lambda: [serial_step() for _ in range(args.steps)])
+    ms = timed(lambda: pipelined(args.steps))
     return {"value": w.token_heads / (ms * 1e-3), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "mode": "pipelined: step n+1 inputs up and step n-1 results down overlap step n kernels",
+            "serial": {"value": w.token_heads / (ms_serial * 1e-3), "ms_per_step": ms_serial}}
 
 
 def main():
