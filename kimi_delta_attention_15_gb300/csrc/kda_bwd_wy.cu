@@ -4,11 +4,12 @@
 // kernel) and dU = dUt (backward scan):
 //   dT    = dW (K^*Gamma)^T + dU V^T
 //   dKt   = T^T dW        (adjoint of K^*Gamma)
-//   dV    = T^T dU        (final dv; plain tf32, it feeds only the bf16 output)
+//   dV    = T^T dU        (final dv)
 //   dbeta_j  = sum_i dT_ij X_ij + sum_l dA_jl B_jl
 //   dA    = -strict_lower(X^T dT T^T),   dB = diag(beta) dA
-// Split-tf32 mma.sync on 16-row tiles (the gate gradient needs the extra
-// precision); dKt, dB and dbeta go to the workspace.
+// Single tf32 mma.sync products on 16-row tiles: with them every output stays well
+// inside its tolerance (measured against the fp64 reference; the pair-term kernel is
+// the one that needs split operands); dKt, dB and dbeta go to the workspace.
 // The raw k, v, g_raw rows of the CTA's next tile are staged by cp.async during
 // the second half of a tile, so the input preparation reads shared memory.
 // Warps take row blocks skewed by their index (block (w + w/4) mod 4), so the
@@ -142,14 +143,14 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < D / 8; ++ks) {
             const int k0 = ks * 8 + tig, k1 = k0 + 4;
-            const Frag4 wf = frag4(s.dW[r0 * PS + k0], s.dW[r1 * PS + k0], s.dW[r0 * PS + k1], s.dW[r1 * PS + k1]);
-            const Frag4 uf = frag4(s.dU[r0 * PS + k0], s.dU[r1 * PS + k0], s.dU[r0 * PS + k1], s.dU[r1 * PS + k1]);
+            const Frag4t wf = frag4t(s.dW[r0 * PS + k0], s.dW[r1 * PS + k0], s.dW[r0 * PS + k1], s.dW[r1 * PS + k1]);
+            const Frag4t uf = frag4t(s.dU[r0 * PS + k0], s.dU[r1 * PS + k0], s.dU[r0 * PS + k1], s.dU[r1 * PS + k1]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = ch * 16 + nt * 8 + gid;
-                mma3(acc[nt], wf, frag2(s.kt[j * PS + k0], s.kt[j * PS + k1]));
+                mma1(acc[nt], wf, frag2t(s.kt[j * PS + k0], s.kt[j * PS + k1]));
                 // v is bf16 data: its fp32 bit pattern is exact in tf32
-                mma2a(acc[nt], uf, (uint32_t)vv[j * VP + k0] << 16, (uint32_t)vv[j * VP + k1] << 16);
+                mma1(acc[nt], uf, (uint32_t)vv[j * VP + k0] << 16, (uint32_t)vv[j * VP + k1] << 16);
             }
         }
 #pragma unroll
@@ -171,14 +172,12 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         const int j0 = jb * SUB + gid, j1 = j0 + 8;
         for (int ks = 2 * jb; ks < C / 8; ++ks) {
             const int i0 = ks * 8 + tig, i1 = i0 + 4;
-            const Frag4 tf = frag4(s.T[i0 * PC + j0], s.T[i0 * PC + j1], s.T[i1 * PC + j0], s.T[i1 * PC + j1]);
+            const Frag4t tf = frag4t(s.T[i0 * PC + j0], s.T[i0 * PC + j1], s.T[i1 * PC + j0], s.T[i1 * PC + j1]);
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const int c = ch * 32 + nt * 8 + gid;
-                mma3(ak[nt], tf, frag2(s.dW[i0 * PS + c], s.dW[i1 * PS + c]));
-                // dV only feeds the bf16 output dv: one tf32 product is accurate enough
-                mma_tf32_16x8x8(av[nt], tf.hi[0], tf.hi[1], tf.hi[2], tf.hi[3], tf32_bits(s.dU[i0 * PS + c]),
-                                tf32_bits(s.dU[i1 * PS + c]));
+                mma1(ak[nt], tf, frag2t(s.dW[i0 * PS + c], s.dW[i1 * PS + c]));
+                mma1(av[nt], tf, frag2t(s.dU[i0 * PS + c], s.dU[i1 * PS + c]));
             }
         }
         float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT);
@@ -214,11 +213,11 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < C / 8; ++ks) {
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
-            const Frag4 af = frag4(s.dT[r0 * PC + m0], s.dT[r1 * PC + m0], s.dT[r0 * PC + m1], s.dT[r1 * PC + m1]);
+            const Frag4t af = frag4t(s.dT[r0 * PC + m0], s.dT[r1 * PC + m0], s.dT[r0 * PC + m1], s.dT[r1 * PC + m1]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = ch * 16 + nt * 8 + gid;
-                mma3(acc[nt], af, frag2(s.T[j * PC + m0], s.T[j * PC + m1]));
+                mma1(acc[nt], af, frag2t(s.T[j * PC + m0], s.T[j * PC + m1]));
             }
         }
         __syncthreads();   // everyone is done reading dW before M overwrites it
@@ -242,11 +241,11 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         const int i0 = ib * SUB + gid, i1 = i0 + 8;
         for (int ks = 2 * ib; ks < C / 8; ++ks) {
             const int m0 = ks * 8 + tig, m1 = m0 + 4;
-            const Frag4 xf = frag4(s.X[m0 * PC + i0], s.X[m0 * PC + i1], s.X[m1 * PC + i0], s.X[m1 * PC + i1]);
+            const Frag4t xf = frag4t(s.X[m0 * PC + i0], s.X[m0 * PC + i1], s.X[m1 * PC + i0], s.X[m1 * PC + i1]);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = ch * 16 + nt * 8 + gid;
-                mma3(acc[nt], xf, frag2(M[m0 * PC + j], M[m1 * PC + j]));
+                mma1(acc[nt], xf, frag2t(M[m0 * PC + j], M[m1 * PC + j]));
             }
         }
 #pragma unroll

@@ -57,6 +57,23 @@ __device__ __forceinline__ void mma3(float (&c)[4], const Frag4& a, const Frag2&
     mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.lo[0], b.lo[1]);
     mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.hi[0], b.hi[1]);
 }
+// Single tf32 products, for products whose outputs stay well inside their tolerances
+// without the split (measured against the fp64 reference): the fp32 operands go in
+// unconverted and the tensor core reads their top 19 bits (truncation toward zero),
+// which costs no instruction.
+struct Frag4t { uint32_t r[4]; };
+struct Frag2t { uint32_t r[2]; };
+__device__ __forceinline__ Frag4t frag4t(float a0, float a1, float a2, float a3) {
+    return Frag4t{{__float_as_uint(a0), __float_as_uint(a1), __float_as_uint(a2), __float_as_uint(a3)}};
+}
+__device__ __forceinline__ Frag2t frag2t(float b0, float b1) { return Frag2t{{__float_as_uint(b0), __float_as_uint(b1)}}; }
+__device__ __forceinline__ void mma1(float (&c)[4], const Frag4t& a, const Frag2t& b) {
+    mma_tf32_16x8x8(c, a.r[0], a.r[1], a.r[2], a.r[3], b.r[0], b.r[1]);
+}
+__device__ __forceinline__ void mma1(float (&c)[4], const Frag4t& a, uint32_t b0, uint32_t b1) {
+    mma_tf32_16x8x8(c, a.r[0], a.r[1], a.r[2], a.r[3], b0, b1);
+}
+
 // c += a * b, b exact in tf32 (e.g. bf16 data)
 __device__ __forceinline__ void mma2a(float (&c)[4], const Frag4& a, uint32_t b0, uint32_t b1) {
     mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b0, b1);
