@@ -389,7 +389,9 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     }
 }
 
-// Deterministic sum of the per-chunk parameter partials, chunk order, per head.
+// Deterministic sum of the per-chunk parameter partials, per head: eight running sums
+// over the chunks (chunk index mod 8), then combined in a fixed order. Empty chunk
+// records only follow the last real chunk.
 __global__ void __launch_bounds__(128)
     kda_param_reduce_kernel(int H, float* __restrict__ dA_log, float* __restrict__ ddt_bias,
                             uint8_t* __restrict__ ws, Layout lay) {
@@ -397,15 +399,40 @@ __global__ void __launch_bounds__(128)
     if (read_status(ws) != 0) return;
     const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
     const float* part = reinterpret_cast<const float*>(ws + lay.part);
-    float acc = 0.0f, accA = 0.0f;
-    for (int64_t ch = 0; ch < lay.nc_max; ++ch) {
-        if (chunks[ch].L <= 0) continue;
-        const float* p = part + ((size_t)ch * H + h) * (D + 4);
-        acc += p[c];
-        if (c == 0) accA += p[D];
+    __shared__ int nreal;
+    if (c == 0) {
+        int lo = 0, hi = (int)lay.nc_max;   // first empty record (binary search)
+        while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (chunks[mid].L > 0) lo = mid + 1;
+            else hi = mid;
+        }
+        nreal = lo;
     }
-    ddt_bias[h * D + c] = acc;
-    if (c == 0) dA_log[h] = accA;
+    __syncthreads();
+    const int n = nreal;
+    float acc[8], accA[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) acc[u] = accA[u] = 0.0f;
+    int ch = 0;
+    for (; ch + 8 <= n; ch += 8) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
+            acc[u] += p[c];
+            if (c == 0) accA[u] += p[D];
+        }
+    }
+    for (int u = 0; ch + u < n; ++u) {
+        const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
+        acc[u] += p[c];
+        if (c == 0) accA[u] += p[D];
+    }
+    float tot = 0.0f, totA = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) { tot += acc[u]; totA += accA[u]; }
+    ddt_bias[h * D + c] = tot;
+    if (c == 0) dA_log[h] = totA;
 }
 
 }  // namespace kda
