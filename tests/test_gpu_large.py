@@ -46,3 +46,29 @@ def test_full_size_sampled_heads(idx, hs):
         check(k, x, ref[k])
     for k in ("hT", "dh0"):
         check(k, out[k][:, hs], ref[k])
+
+
+# The other shapes the pages admit: T=17 with 16 heads, T=1024 with 4 heads (every
+# head checked), and eight packed sequences of 1024 tokens at 96 heads (sampled heads).
+@pytest.mark.parametrize("name,hs", [("fixed_T17_H16", None), ("fixed_T1024_H4", None),
+                                     ("varlen_8x1024_H96", [2, 45, 71, 95])])
+def test_other_admitted_shapes(name, hs):
+    w = next(x for x in I.EXTRA_WORKLOADS if x.name == name)
+    inp = I.make_inputs(w, seed=I.BASE_SEED + 100 + I.EXTRA_WORKLOADS.index(w))
+    out = run_fwd_bwd(inp)
+    assert out["status"] == 0
+    sub = inp if hs is None else _heads(inp, hs)
+    ref = dict(oracle.forward(sub))
+    ref.update(oracle.backward(sub))
+    sel = (lambda x: x) if hs is None else (lambda x: x[:, hs])
+    for k in ("o", "dq", "dk", "dv", "dg_raw", "dbeta_raw"):
+        check(k, sel(out[k]), ref[k])
+    for k in ("hT", "dh0"):
+        if ref.get(k) is not None and out.get(k) is not None:
+            check(k, sel(out[k]), ref[k])
+    # a parameter gradient of one head is a sum over all of its tokens: checked where
+    # the head has many of them (T=17 leaves too few for the relative criterion)
+    if w.T >= 1024:
+        for k in ("dA_log", "ddt_bias"):
+            x = out[k] if hs is None else out[k][hs]
+            check(k, x, ref[k])
