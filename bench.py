@@ -305,6 +305,8 @@ def run_gb300(args, ws, rank, local):
     # end to end through the public API with pinned host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(args, inp, dev, w)
+    if not args.no_e2e:
+        line["decode"] = decode_bench(dev, hbm)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         cores = oracle.default_threads()
@@ -413,6 +415,38 @@ def e2e(args, inp, dev, w):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "mode": "pipelined: step n+1 inputs up and step n-1 results down overlap step n kernels",
             "serial": {"value": w.token_heads / (ms_serial * 1e-3), "ms_per_step": ms_serial}}
+
+
+def decode_bench(dev, hbm_peak, n_req=256, H=96, steps=20):
+    """One decode step (kda_decode) for n_req requests x H heads: each (request, head)
+    reads and writes its 64 KB fp32 state once, 3.2 GB in all, more than L2, so the
+    step streams from HBM. Times `steps` consecutive steps with CUDA events."""
+    import torch
+    from kimi_delta_attention_15_gb300 import ops
+    g = torch.Generator(device="cpu").manual_seed(20261202)
+    tok = lambda: torch.randn(n_req, H, 128, generator=g).to(torch.bfloat16).to(dev)
+    q, k, v, g_raw = tok(), tok(), tok(), tok()
+    beta_raw = torch.randn(n_req, H, generator=g).to(torch.bfloat16).to(dev)
+    A_log = torch.log(torch.rand(H, generator=g) * 15 + 1).to(dev)
+    dt_bias = (0.1 * torch.randn(H, 128, generator=g)).to(dev)
+    state = (0.1 * torch.randn(n_req, H, 128, 128, generator=g)).to(dev)
+    o = torch.empty_like(v)
+    for _ in range(3):
+        ops.decode(q, k, v, g_raw, beta_raw, A_log, dt_bias, state, o=o)
+    torch.cuda.synchronize()
+    s0, e0 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s0.record()
+    for _ in range(steps):
+        ops.decode(q, k, v, g_raw, beta_raw, A_log, dt_bias, state, o=o)
+    e0.record()
+    e0.synchronize()
+    ms = s0.elapsed_time(e0) / steps
+    units = n_req * H
+    bytes_step = units * (2 * 128 * 128 * 4 + 5 * 128 * 2 + 2)   # state in + out, q k v g o rows, beta
+    gbs = bytes_step / (ms * 1e-3) / 1e9
+    return {"workload": f"decode_{n_req}req_H{H}", "ms_per_step": ms,
+            "tokens_heads_per_s": units / (ms * 1e-3), "bound": "hbm", "achieved_gbs": gbs,
+            "peak_gbs": hbm_peak, "frac": gbs / hbm_peak, "bytes_per_step": bytes_step}
 
 
 def main():

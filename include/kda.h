@@ -112,6 +112,26 @@ kda_status kda_bwd(const kda_shape* shape,
                    kda_bf16* dbeta_raw, float* dA_log, float* ddt_bias, float* dh0,
                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* One decode step for a batch of requests: the single-token step of the
+ * recurrence above, batched over (request, head) pairs (the batched decode
+ * entry of the kda-neuron-kernels commit log). For each of the n_req requests
+ * and H heads, one token of q, k, v, g_raw [n_req, H, 128] bf16 and beta_raw
+ * [n_req, H] bf16 advances the value-first state [n_req, H, 128, 128] fp32
+ * IN PLACE and writes o [n_req, H, 128] bf16 (read from the updated state).
+ * A_log [H] and dt_bias [H, 128] fp32 as in kda_fwd. No workspace; the caller
+ * owns every buffer. The result is that of kda_fwd over sequences of one token
+ * with h0 = the state before and hT = the state after.
+ * Errors: n_req < 0, H <= 0 or n_req * H >= 2^31 -> KDA_ERR_SHAPE; scale not
+ * finite and > 0, or lower_bound outside [-5, 0) -> KDA_ERR_UNSUPPORTED; a NULL
+ * pointer (n_req > 0) -> KDA_ERR_NULL; a pointer not 16-byte aligned ->
+ * KDA_ERR_ALIGN; a failed launch -> KDA_ERR_CUDA (text in kda_last_error()).
+ * n_req = 0 does nothing. */
+kda_status kda_decode(long long n_req, long long H, float scale, float lower_bound,
+                      const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                      const kda_bf16* g_raw, const kda_bf16* beta_raw,
+                      const float* A_log, const float* dt_bias,
+                      float* state, kda_bf16* o, void* stream);
+
 /* Synchronises `stream` and returns the device status word of `workspace`
  * (KDA_OK, KDA_ERR_OFFSETS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
  * stream reported an error. Clears nothing. */

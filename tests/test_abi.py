@@ -72,3 +72,21 @@ def test_selftest_rejects_bad_shapes(lib):
     p = ctypes.c_void_p(16)
     assert lib.kda_diag_umma_selftest(0, 0, 300, 64, p, p, p, None) == 3
     assert lib.kda_diag_umma_selftest(1, 0, 64, 64, p, p, p, None) == 4
+
+
+def test_decode_host_validation_codes(lib):
+    def call(n=2, H=3, scale=0.088, lb=-5.0, ptr=16, bad=None):
+        ps = [ctypes.c_void_p(ptr) for _ in range(9)]
+        if bad is not None:
+            ps[bad] = ctypes.c_void_p(ptr + 8)
+        return lib.kda_decode(n, H, scale, lb, *ps, None)
+    assert call(n=-1) == 3                    # negative batch
+    assert call(H=0) == 3
+    assert call(n=1 << 30, H=8) == 3          # more than 2^31 - 1 units
+    assert call(lb=-6.0) == 4                 # lower bound outside [-5, 0)
+    assert call(lb=0.0) == 4
+    assert call(scale=float("inf")) == 4
+    assert call(ptr=0) == 1                   # NULL
+    for i in range(9):
+        assert call(bad=i) == 2               # each pointer must be 16-byte aligned
+    assert call(n=0, ptr=0) == 0              # empty batch: nothing to do
