@@ -140,15 +140,16 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-        const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < D / 8; ++ks) {
             const int k0 = ks * 8 + tig, k1 = k0 + 4;
-            const Frag4t wf = frag4t(s.dW[r0 * PS + k0], s.dW[r1 * PS + k0], s.dW[r0 * PS + k1], s.dW[r1 * PS + k1]);
-            const Frag4t uf = frag4t(s.dU[r0 * PS + k0], s.dU[r1 * PS + k0], s.dU[r0 * PS + k1], s.dU[r1 * PS + k1]);
+            const Frag4t wf = ldsm_a(s.dW, PS, rb * SUB, ks * 8);
+            const Frag4t uf = ldsm_a(s.dU, PS, rb * SUB, ks * 8);
+            Frag2t kb[2];
+            ldsm_b2(kb[0], kb[1], s.kt, PS, ch * 16, ks * 8);
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int j = ch * 16 + nt * 8 + gid;
-                mma1(acc[nt], wf, frag2t(s.kt[j * PS + k0], s.kt[j * PS + k1]));
+                mma1(acc[nt], wf, kb[nt]);
                 // v is bf16 data: its fp32 bit pattern is exact in tf32
                 mma1(acc[nt], uf, (uint32_t)vv[j * VP + k0] << 16, (uint32_t)vv[j * VP + k1] << 16);
             }
@@ -210,15 +211,12 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-        const int r0 = rb * SUB + gid, r1 = r0 + 8;
         for (int ks = 0; ks < C / 8; ++ks) {
-            const int m0 = ks * 8 + tig, m1 = m0 + 4;
-            const Frag4t af = frag4t(s.dT[r0 * PC + m0], s.dT[r1 * PC + m0], s.dT[r0 * PC + m1], s.dT[r1 * PC + m1]);
+            const Frag4t af = ldsm_a(s.dT, PC, rb * SUB, ks * 8);
+            Frag2t tb[2];
+            ldsm_b2(tb[0], tb[1], s.T, PC, ch * 16, ks * 8);
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int j = ch * 16 + nt * 8 + gid;
-                mma1(acc[nt], af, frag2t(s.T[j * PC + m0], s.T[j * PC + m1]));
-            }
+            for (int nt = 0; nt < 2; ++nt) mma1(acc[nt], af, tb[nt]);
         }
         __syncthreads();   // everyone is done reading dW before M overwrites it
 #pragma unroll

@@ -74,6 +74,33 @@ __device__ __forceinline__ void mma1(float (&c)[4], const Frag4t& a, uint32_t b0
     mma_tf32_16x8x8(c, a.r[0], a.r[1], a.r[2], a.r[3], b0, b1);
 }
 
+// Fragments straight from shared memory with ldmatrix: an 8x8 b16 matrix is an 8x4
+// tile of 32-bit values, and lane i receives the word (row i/4, column i%4) of each
+// matrix, the layout of the tf32 A and B fragments. Every lane passes the address of
+// one 16-byte row (lanes 8m .. 8m+7: the rows of matrix m).
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* row) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(static_cast<uint32_t>(__cvta_generic_to_shared(row))));
+}
+// A fragment (16 x 8, rows r0.., columns k0..) of a row-major fp32 tile with row
+// stride ld floats (16-byte aligned rows), as fp32 bit patterns
+__device__ __forceinline__ Frag4t ldsm_a(const float* tile, int ld, int r0, int k0) {
+    const int lane = threadIdx.x & 31, m = lane >> 3;
+    Frag4t f;
+    ldsm_x4(f.r, tile + (size_t)(r0 + (m & 1) * 8 + (lane & 7)) * ld + k0 + (m >> 1) * 4);
+    return f;
+}
+// B fragments of the n-tiles n0.. and n0+8.. at columns k0.. of a tile stored with
+// n as its row index (row stride ld floats), as fp32 bit patterns
+__device__ __forceinline__ void ldsm_b2(Frag2t& b0, Frag2t& b1, const float* tile, int ld, int n0, int k0) {
+    const int lane = threadIdx.x & 31, m = lane >> 3;
+    uint32_t r[4];
+    ldsm_x4(r, tile + (size_t)(n0 + (m >> 1) * 8 + (lane & 7)) * ld + k0 + (m & 1) * 4);
+    b0 = Frag2t{{r[0], r[1]}};
+    b1 = Frag2t{{r[2], r[3]}};
+}
+
 // c += a * b, b exact in tf32 (e.g. bf16 data)
 __device__ __forceinline__ void mma2a(float (&c)[4], const Frag4& a, uint32_t b0, uint32_t b1) {
     mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b0, b1);
