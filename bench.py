@@ -300,6 +300,8 @@ def run_gb300(args, ws, rank, local):
                        "seq_len": w.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
                        "l2": "flushed (512 MiB write) before every timed step"},
             "tflops": tflops, "pct_bf16_peak": tflops / bf16,
+            "fwd_ms": sum(v for k, v in kms.items() if k.startswith("fwd")),
+            "bwd_ms": sum(v for k, v in kms.items() if k.startswith("bwd")),
             "roofline": roof, "clocks": clk, "gpu_launches": 9 * args.steps}
 
     # end to end through the public API with pinned host buffers

@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
             eQ[nt][hh] = *reinterpret_cast<const float2*>(gdQ + row * D + col);
             eKt[nt][hh] = *reinterpret_cast<const float2*>(gdKt + row * D + col);
         }
-    prep_compute(rr, nullptr, a_h, lb, L, 0, s.qe, s.ke, nullptr, s.kp, s.beta, s.inq, s.ink);
+    prep_compute(rr, a_h, lb, L, s.qe, s.ke, s.kp, s.beta, s.inq, s.ink);
     cp_async_wait_all();
     __syncthreads();
     block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);

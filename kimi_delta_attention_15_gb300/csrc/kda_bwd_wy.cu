@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         __syncthreads();
         panels_to_smem_async(s.dU, PS, gdU);
         cp_async_commit();
-        prep_compute(rr, nullptr, a_h, lb, L, 0, nullptr, s.kt, nullptr, s.dW, s.beta, nullptr, nullptr);
+        prep_compute(rr, a_h, lb, L, nullptr, s.kt, s.dW, s.beta, nullptr, nullptr);
     }
     __syncthreads();
     block_products(s.dW, nullptr, s.kt, nullptr, nullptr, &s.fa);

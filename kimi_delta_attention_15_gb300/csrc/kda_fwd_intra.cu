@@ -174,7 +174,7 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         {
             RowRegsT<kIntraWarps> rr;
             prep_load_staged(rr, stg, stg + C * D, stg + 2 * C * D, s.braw, s.dtb, L);
-            prep_compute(rr, nullptr, a_h, lb, L, 0, s.qe, s.ke, nullptr, s.kp, s.beta, nullptr, nullptr);
+            prep_compute(rr, a_h, lb, L, s.qe, s.ke, s.kp, s.beta, nullptr, nullptr);
         }
         __syncthreads();
         block_products(s.kp, s.qe, s.ke, nullptr, nullptr, &s.fa);

@@ -30,63 +30,30 @@ struct Factors {
 };
 
 // Raw bf16 rows of one chunk held in registers: with NW warps, warp w holds
-// rows w + NW b, lane l channels 4l .. 4l+3.
+// rows w + NW b, lane l channels 4l .. 4l+3. The kernels stage a tile's rows in
+// shared memory ahead of use and fill these registers from there.
 template <int NW>
 struct RowRegsT {
     static constexpr int RB = C / NW;
-    uint2 q[RB], k[RB], v[RB], g[RB];
+    uint2 q[RB], k[RB], g[RB];
     float br[RB];
     float dt[4];     // dt_bias[h, 4 lane .. 4 lane + 3]
-    float alog;      // A_log[h]
 };
-using RowRegs = RowRegsT<8>;
 
-// Issues the global loads of a chunk's rows (NW warps). Only the tensors
-// whose pointer is non-null are loaded; the rest stay zero. A_log and dt_bias
-// (nullable) of head h are loaded too.
-template <int NW>
-__device__ __forceinline__ void prep_load(RowRegsT<NW>& rr, const uint16_t* __restrict__ q,
-                                          const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
-                                          const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
-                                          int t0, int L, int H, int h, const float* __restrict__ A_log = nullptr,
-                                          const float* __restrict__ dt_bias = nullptr) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c0 = lane * 4;
-    rr.alog = A_log ? A_log[h] : 0.0f;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) rr.dt[e] = dt_bias ? dt_bias[h * D + c0 + e] : 0.0f;
-#pragma unroll
-    for (int b = 0; b < RowRegsT<NW>::RB; ++b) {
-        const int r = warp + b * NW;
-        rr.q[b] = rr.k[b] = rr.v[b] = rr.g[b] = make_uint2(0u, 0u);
-        rr.br[b] = 0.0f;
-        if (r < L) {
-            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-            if (q) rr.q[b] = *reinterpret_cast<const uint2*>(q + base);
-            if (k) rr.k[b] = *reinterpret_cast<const uint2*>(k + base);
-            if (v) rr.v[b] = *reinterpret_cast<const uint2*>(v + base);
-            if (g_raw) rr.g[b] = *reinterpret_cast<const uint2*>(g_raw + base);
-            if (beta_raw && lane == 0) rr.br[b] = bf2f(beta_raw[(size_t)(t0 + r) * H + h]);
-        }
-    }
-}
-
-// The same rows taken from raw bf16 copies already in shared memory (q, k, g_raw
-// as [64][128], beta_raw [64], dt_bias [128] of the head; any may be null),
-// for kernels that stage a tile's inputs ahead of use. Filling the same
-// registers keeps prep_compute, and so every derived value, unchanged.
+// A chunk's rows from raw bf16 copies in shared memory (q, k, g_raw as
+// [64][128], beta_raw [64], dt_bias [128] of the head; any may be null; rows at
+// or past L read as zero).
 template <int NW>
 __device__ __forceinline__ void prep_load_staged(RowRegsT<NW>& rr, const uint16_t* qs, const uint16_t* ks,
                                                  const uint16_t* gs, const uint16_t* bs, const float* dtb, int L) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = lane * 4;
-    rr.alog = 0.0f;
 #pragma unroll
     for (int e = 0; e < 4; ++e) rr.dt[e] = dtb ? dtb[c0 + e] : 0.0f;
 #pragma unroll
     for (int b = 0; b < RowRegsT<NW>::RB; ++b) {
         const int r = warp + b * NW;
-        rr.q[b] = rr.k[b] = rr.v[b] = rr.g[b] = make_uint2(0u, 0u);
+        rr.q[b] = rr.k[b] = rr.g[b] = make_uint2(0u, 0u);
         rr.br[b] = 0.0f;
         if (r < L) {
             if (qs) rr.q[b] = *reinterpret_cast<const uint2*>(qs + r * D + c0);
@@ -97,18 +64,14 @@ __device__ __forceinline__ void prep_load_staged(RowRegsT<NW>& rr, const uint16_
     }
 }
 
-// Turns loaded rows into q^, k^, v, alpha, beta and 1/sqrt(|x|^2 + eps) in
-// shared memory (any output pointer may be null; rows >= L: zeros, alpha = 1,
-// beta = 0).
+// Turns loaded rows into q^, k^, alpha, beta and 1/sqrt(|x|^2 + eps) in shared
+// memory (any output pointer may be null; rows >= L: zeros, alpha = 1, beta = 0).
 template <int NW>
-__device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, const float* __restrict__ dt_bias, float a_h,
-                                             float lb, int L, int h, float* xq, float* xk, float* xv, float* xa,
-                                             float* beta, float* inq, float* ink) {
+__device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, float a_h, float lb, int L, float* xq,
+                                             float* xk, float* xa, float* beta, float* inq, float* ink) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = lane * 4;
-    float dtv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) dtv[e] = (xa && dt_bias) ? dt_bias[h * D + c0 + e] : rr.dt[e];
+    const float* dtv = rr.dt;
     auto un = [](uint2 w, float* out) {
         out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
         out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
@@ -133,8 +96,8 @@ __device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, const float
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
         const int r = warp + b * NW;
-        float qv[4], kv[4], vv[4], gr[4], al[4] = {1, 1, 1, 1};
-        un(rr.q[b], qv); un(rr.k[b], kv); un(rr.v[b], vv); un(rr.g[b], gr);
+        float qv[4], kv[4], gr[4], al[4] = {1, 1, 1, 1};
+        un(rr.q[b], qv); un(rr.k[b], kv); un(rr.g[b], gr);
         if (xa && r < L) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dtv[e])));
@@ -142,7 +105,6 @@ __device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, const float
         const float iq = rsqrtf(sq[b] + 1e-6f), ik = rsqrtf(sk[b] + 1e-6f);
         if (xq) *reinterpret_cast<float4*>(xq + r * PS + c0) = make_float4(qv[0] * iq, qv[1] * iq, qv[2] * iq, qv[3] * iq);
         if (xk) *reinterpret_cast<float4*>(xk + r * PS + c0) = make_float4(kv[0] * ik, kv[1] * ik, kv[2] * ik, kv[3] * ik);
-        if (xv) *reinterpret_cast<float4*>(xv + r * PS + c0) = make_float4(vv[0], vv[1], vv[2], vv[3]);
         if (xa) *reinterpret_cast<float4*>(xa + r * PS + c0) = make_float4(al[0], al[1], al[2], al[3]);
         if (lane == 0) {
             if (beta) beta[r] = r < L ? sigmoidf(rr.br[b]) : 0.0f;
@@ -150,19 +112,6 @@ __device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, const float
             if (ink) ink[r] = ik;
         }
     }
-}
-
-// Loads and prepares rows of one chunk in one go (NW warps).
-template <int NW = 8>
-__device__ __forceinline__ void prep_rows(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
-                                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
-                                          const uint16_t* __restrict__ beta_raw, const float* __restrict__ dt_bias,
-                                          float a_h, float lb, int t0, int L, int H, int h, float* xq, float* xk,
-                                          float* xv, float* xa, float* beta, float* inq, float* ink) {
-    RowRegsT<NW> rr;
-    prep_load(rr, (xq || inq) ? q : nullptr, (xk || ink) ? k : nullptr, xv ? v : nullptr, xa ? g_raw : nullptr,
-              beta ? beta_raw : nullptr, t0, L, H, h);
-    prep_compute(rr, dt_bias, a_h, lb, L, h, xq, xk, xv, xa, beta, inq, ink);
 }
 
 // Block products. On entry `ap` holds alpha, `xq`/`xk` hold q^/k^ (either may
