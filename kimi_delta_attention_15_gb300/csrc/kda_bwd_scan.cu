@@ -136,18 +136,38 @@ __global__ void __launch_bounds__(256, 1)
         }
         // dS_L: TMEM -> tf32 copy in TMEM (the MMA operand), and dS_L^T [k][v] to the
         // workspace checkpoint; dS_L diag(exp(G_L)) back to TMEM
+        // (both 32-column halves in flight at once: one wait for the loads, one for the stores)
         uint8_t* gDST = ws + lay.ds + tile * kTileDD;
-        for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
-            float r[32], q[32];
-            tmem_ld32(tS + lane_base + c0, r);
+        {
+            const int cb = 64 * half;
+            uint32_t r0[32], r1[32], q0[32], q1[32];
+            tmem_ld32_issue(tS + lane_base + cb, r0);
+            tmem_ld32_issue(tS + lane_base + cb + 32, r1);
+            tmem_wait_ld(r0);
+            tmem_after_wait(r1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) q[j] = tf32_round(r[j]);
-            tmem_st32(tDS + lane_base + c0, q);
+            for (int j = 0; j < 32; ++j) {
+                q0[j] = tf32_round_bits(__uint_as_float(r0[j]));
+                q1[j] = tf32_round_bits(__uint_as_float(r1[j]));
+            }
+            tmem_st32_issue(tDS + lane_base + cb, q0);
+            tmem_st32_issue(tDS + lane_base + cb + 32, q1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(gDST + panel_off(c0 + j, v, D)) = q[j];
+            for (int j = 0; j < 32; ++j) {
+                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + j, v, D)) = q0[j];
+                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + 32 + j, v, D)) = q1[j];
+            }
 #pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] *= s.gam[c0 + j];
-            tmem_st32(tS + lane_base + c0, r);
+            for (int j = 0; j < 32; ++j) {
+                r0[j] = __float_as_uint(__uint_as_float(r0[j]) * s.gam[cb + j]);
+                r1[j] = __float_as_uint(__uint_as_float(r1[j]) * s.gam[cb + 32 + j]);
+            }
+            tmem_st32_issue(tS + lane_base + cb, r0);
+            tmem_st32_issue(tS + lane_base + cb + 32, r1);
+            tmem_wait_st(q0);
+            tmem_after_wait(q1);
+            tmem_after_wait(r0);
+            tmem_after_wait(r1);
         }
         fence_async_smem();
         tc_fence_before();
