@@ -51,8 +51,8 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "07128afc1be66be5",
-    "per_tile": {"fwd_intra": 333475, "fwd_scan": 243898, "bwd_scan": 211308, "bwd_state": 309152, "bwd_wy": 198866, "bwd_pair": 222691},
+    "sources": "2eef516bf60ee346",
+    "per_tile": {"fwd_intra": 333717, "fwd_scan": 244140, "bwd_scan": 211409, "bwd_state": 308902, "bwd_wy": 198832, "bwd_pair": 222677},
 }
 
 
@@ -307,8 +307,8 @@ def run_gb300(args, ws, rank, local):
     # end to end through the public API with pinned host buffers
     if not args.no_e2e:
         line["e2e"] = e2e(args, inp, dev, w)
-    if not args.no_e2e:
-        line["decode"] = decode_bench(dev, hbm)
+    if args.decode_requests > 0:
+        line["decode"] = decode_bench(dev, hbm, n_req=args.decode_requests)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         import oracle
         cores = oracle.default_threads()
@@ -461,6 +461,8 @@ def main():
                     help="name of a workload in kimi_delta_attention_15_gb300.inputs (default: the T=8192, H=96 one)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-requests", type=int, default=256,
+                    help="requests in the decode measurement (x 96 heads; 0 skips it)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
