@@ -145,8 +145,8 @@ kda_status check_shape(const kda_shape* sh, bool packed) {
 
 Layout layout_of(const kda_shape* sh, bool packed) { return make_layout(sh->B, sh->T, sh->H, sh->N, packed); }
 
-// Grid of a persistent per-tile kernel: one CTA per SM (each holds ~220 KB of
-// shared memory), never more CTAs than tiles.
+// Grid of a persistent per-tile kernel: one CTA (or one two-CTA cluster) per SM,
+// never more than tiles.
 unsigned persistent_grid(int64_t tiles) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -242,6 +242,11 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     if ((st = set_smem(kda_bwd_state_kernel, bwd_state_smem_bytes())) != KDA_OK) return st;
     if ((st = set_smem(kda_bwd_wy_kernel, bwd_wy_smem_bytes())) != KDA_OK) return st;
     if ((st = set_smem(kda_bwd_pair_kernel, bwd_pair_smem_bytes())) != KDA_OK) return st;
+    // clusters of two CTAs, two CTAs per SM: all of the unified L1 as shared memory
+    if ((st = cuda_status(cudaFuncSetAttribute(kda_bwd_pair_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                               (int)cudaSharedmemCarveoutMaxShared),
+                          "cudaFuncSetAttribute")) != KDA_OK)
+        return st;
     const dim3 tiles((unsigned)lay.nc_max, (unsigned)H);
     prof(4, s);
     if (shape->N > 0)
@@ -257,7 +262,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
                                                                    ws, lay);
     prof(7, s);
     if (lay.nc_max > 0)
-        kda_bwd_pair_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
+        kda_bwd_pair_kernel<<<2 * persistent_grid(lay.nc_max * H), 256, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
                                                                        dq, dk, dg_raw, dbeta_raw, ws, lay);
     prof(8, s);
     kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);

@@ -1,7 +1,7 @@
-// Backward, last per-chunk stage: one CTA per (chunk, head), all chunks in
-// parallel. Gathers every adjoint of q^, k^ and of the in-chunk cumulative
-// log-decay G, then applies the reverse cumulative sum (g_t = G_t - G_{t-1})
-// and the chains of the gate, the beta sigmoid and the L2 norms:
+// Backward, last per-chunk stage, per (chunk, head) tile. Gathers every adjoint of
+// q^, k^ and of the in-chunk cumulative log-decay G, then applies the reverse
+// cumulative sum (g_t = G_t - G_{t-1}) and the chains of the gate, the beta sigmoid
+// and the L2 norms:
 //   pair terms  B_ij = sum_c k^_ic k^_jc e^{G_ic-G_jc},  Aqk_ij = sum_c q^_ic k^_jc e^{G_ic-G_jc}
 //     with dB (WY kernel) and dAqk (state-products kernel), for column block J:
 //     a = dM[:,J] Kt_J,  b = dM[:,J]^T Xt_J   (Xt_J = x^ e^{G-G_eJ}, Kt_J = k^_J e^{G_eJ-G_J})
@@ -17,9 +17,15 @@
 // which is the same sum without the cancellation of the Kbar terms.
 // Then du = dg lb s (1 - s), dg_raw = du exp(A_log), and the per-chunk
 // partial sums of ddt_bias and dA_log go to the workspace.
-// Persistent over tiles (one CTA per SM). The raw q, k, g_raw rows of the CTA's next
-// tile are staged by cp.async in the dAqk and E+ tiles, which are free from the
-// write-back of the adjoints to the end of the tile.
+//
+// Every term above is per key channel except the row norms of q and k and the row
+// dot products of the L2-norm chains. A cluster of two CTAs takes each tile, CTA r
+// the key channels 64r .. 64r+63; the two exchange those per-row partial sums
+// through distributed shared memory. Half the channels need half the shared memory
+// (about 107 KB), so two CTAs share an SM and the memory phases of one overlap the
+// arithmetic of the other. Persistent over tiles; the raw q, k, g_raw rows of the
+// cluster's next tile are staged by cp.async in the dAqk and dB tiles, which are
+// free from the write-back of the adjoints to the end of the tile.
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
@@ -28,28 +34,73 @@
 namespace kda {
 
 namespace {
-struct PairSmem {
-    float qe[C * PS];   // q^ E-      -> dq^
-    float ke[C * PS];   // k^ E-      -> dk^
-    float kp[C * PS];   // k^ E+      -> dG'
-    float em[C * PS];   // E-         -> dKbar Kbar, then its exclusive prefix over rows
-    float ep[C * PS];   // E+
-    float dB[C * PC];
-    float dA[C * PC];   // dAqk
-    Factors fa;
-    float beta[C], inq[C], ink[C];
-    float red[D];
-    float dtb[D];        // dt_bias of the staged tile's head
-    uint16_t braw[C];    // beta_raw of the current tile
+constexpr int CH = D / 2;   // key channels per CTA
+constexpr int kPairWarps = 8;
+constexpr int kPairThreads = kPairWarps * 32;
+static_assert(CH == C, "the [64][64] tiles share one layout");
+
+// dB and dAqk: [64][64] fp32, rows of 64 floats with the column index XOR-ed by a
+// function of the row, so that the mma fragment loads in both orientations (row by
+// lane / 4 and column by lane % 4, or the transpose) are free of bank conflicts.
+// Aligned groups of four columns stay contiguous (16-byte copies keep working).
+__device__ __forceinline__ int sw(int r, int c) { return r * CH + (c ^ (((r & 3) << 3) | (r & 4))); }
+// [64][64] fp32 channel tiles: rows padded to 68 floats (plain addressing with constant
+// offsets; the fragment loads with rows by lane % 4 see two-way bank conflicts)
+constexpr int PCH = CH + 4;
+__device__ __forceinline__ int pidx(int r, int c) { return r * PCH + c; }
+
+struct PairFactors {
+    float F[NSUB][NSUB][CH];
+    float Pb[NSUB][CH];
+    float Sf[NSUB][CH];
+    float Db[NSUB][CH];
+    float gl[CH];
 };
-static_assert(C * PC * 4 >= C * D * 2 && C * PS * 4 >= 2 * C * D * 2, "the staged rows fit in dA and ep");
+
+struct PairSmem {
+    float qe[C * PCH];   // q^ E-          -> dq^
+    float ke[C * PCH];   // k^ E-          -> dk^
+    float kp[C * PCH];   // alpha, k^ E+   -> dG'
+    float em[C * PCH];   // E-             -> dKbar Kbar, then its exclusive prefix over rows
+    float dB[C * C];    // dB; from the write-back on: dg scratch (4 KB), staged g_raw rows
+    float dA[C * C];    // dAqk; from the write-back on: staged q and k rows
+    PairFactors fa;
+    float beta[C], inq[C], ink[C];
+    float xn[2][2][C];  // partial squared norms per row: [channel half][q, k][row]
+    float xd[2][2][C];  // partial dot products of the L2-norm chains, same layout
+    alignas(16) float dtb[CH];
+    float red[kPairWarps];
+    float go;
+    uint16_t braw[C];
+};
+static_assert(sizeof(PairSmem) <= 113 * 1024, "two CTAs per SM");
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// v to the same shared-memory location in CTA `rank` of the cluster
+__device__ __forceinline__ void st_cluster(const float* local, uint32_t rank, float v) {
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+// v to this CTA's and to the peer's copy of a location
+__device__ __forceinline__ void st_both(float* local, uint32_t peer, float v) {
+    *local = v;
+    st_cluster(local, peer, v);
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 }  // namespace
 
 size_t bwd_pair_smem_bytes() { return sizeof(PairSmem); }
 
-constexpr int kPairWarps = 16;
-
-__global__ void __launch_bounds__(kPairWarps * 32, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     kda_bwd_pair_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                         const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
                         const float* __restrict__ A_log, const float* __restrict__ dt_bias, int H, float lb,
@@ -57,32 +108,48 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
                         uint16_t* __restrict__ dbeta_raw, uint8_t* __restrict__ ws, Layout lay) {
     extern __shared__ uint8_t smem_raw[];
     PairSmem& s = *reinterpret_cast<PairSmem*>(smem_raw);
-    if (read_status(ws) != 0) return;
-    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
-    const int ntiles = (int)lay.nc_max * H;
+    const uint32_t half = cluster_rank(), peer = half ^ 1u;
+    const int cb = (int)half * CH;   // first key channel of this CTA
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gid = lane >> 2, tig = lane & 3;
-    const int step = (int)gridDim.x;
-    // empty chunk records only follow the last real chunk: the first one ends the CTA's work
-    int tile_i = blockIdx.x;
+    constexpr uint32_t kAll = 0xffffffffu;
+
+    // Both CTAs of the cluster run or neither: rank 0 reads the status word and passes
+    // its decision on. The first barrier also makes sure both CTAs have started before
+    // either writes into the other's shared memory; every later step is taken by both
+    // CTAs alike (same tiles, same exits), so every cluster barrier is met by both.
+    cluster_arrive();
+    cluster_wait();
+    if (half == 0 && tid == 0) st_both(&s.go, peer, read_status(ws) == 0 ? 1.0f : 0.0f);
+    cluster_arrive();
+    cluster_wait();
+    if (s.go == 0.0f) return;
+
+    const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
+    const int ntiles = (int)lay.nc_max * H;
+    const int step = (int)(gridDim.x >> 1);
+    // empty chunk records only follow the last real chunk: the first one ends the work
+    int tile_i = (int)(blockIdx.x >> 1);
     ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
     if (ci.L <= 0) return;
-    uint16_t* const stq = reinterpret_cast<uint16_t*>(s.dA);   // staged q rows
-    uint16_t* const stk = reinterpret_cast<uint16_t*>(s.ep);   // staged k rows, then g_raw rows
+    uint16_t* const stq = reinterpret_cast<uint16_t*>(s.dA);   // staged rows, [64][64] bf16 each
+    uint16_t* const stk = stq + C * CH;
+    uint16_t* const stg = reinterpret_cast<uint16_t*>(s.dB + 1024);
+    float* const scr = s.dB;                                     // [4][RG][64] dg scratch
     float alog_next = 0.0f;
     uint16_t braw_next = 0;
-    // raw rows of tile t_i (record cn) -> staging; rows past the chunk read as zero
+    // this CTA's channels of the raw rows of tile t_i (record cn); rows past the chunk read as zero
     auto stage_tile = [&](int t_i, const ChunkInfo& cn) {
         const int hn = t_i % H;
-        for (int seg = tid; seg < 3 * C * (D / 8); seg += kPairWarps * 32) {
-            const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
+        for (int seg = tid; seg < 3 * C * (CH / 8); seg += kPairThreads) {
+            const int which = seg >> 9, rem = seg & 511, r = rem >> 3, c8 = (rem & 7) * 8;
             const uint16_t* src = which == 0 ? q : which == 1 ? k : g_raw;
             const bool valid = r < cn.L;
-            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
-            uint16_t* dst = which == 0 ? stq + r * D + c8 : stk + (which - 1) * C * D + r * D + c8;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + cb + c8;
+            uint16_t* dst = (which == 0 ? stq : which == 1 ? stk : stg) + r * CH + c8;
             cp_async16_zfill(dst, src, valid);
         }
-        if (tid < D / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + 4 * tid);
+        if (tid < CH / 4) cp_async16(s.dtb + 4 * tid, dt_bias + (size_t)hn * D + cb + 4 * tid);
         cp_async_commit();
         alog_next = A_log[hn];
         if (tid < C) braw_next = tid < cn.L ? beta_raw[(size_t)(cn.t0 + tid) * H + hn] : (uint16_t)0;
@@ -93,46 +160,154 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     while (true) {
     const int nxt = tile_i + step;
     const ChunkInfo cn = nxt < ntiles ? chunks[nxt / H] : ChunkInfo{0, 0, 0, 0};
-    const int chunk = tile_i / H, h = tile_i - chunk * H;
+    const int h = tile_i % H;
     const int L = ci.L, t0 = ci.t0;
     const size_t tile = (size_t)tile_i;
     const uint8_t* bg = ws + lay.bg + tile * BgOff::BYTES;
     const uint8_t* wy = ws + lay.wy + tile * WyOff::BYTES;
     const float a_h = __expf(alog);
-    (void)chunk;
 
     if (tid < C) s.braw[tid] = braw;
     cp_async_wait_all();
     __syncthreads();
-    RowRegsT<kPairWarps> rr;
-    prep_load_staged(rr, stq, stk, stk + C * D, s.braw, s.dtb, L);
-    __syncthreads();   // the staged rows are read: dA is reloaded and ep rewritten below
-    tile_to_smem_async(s.dB, PC, reinterpret_cast<const float*>(wy + WyOff::DB), C, C);
-    tile_to_smem_async(s.dA, PC, reinterpret_cast<const float*>(bg + BgOff::DAQK), C, C);
-    cp_async_commit();
-    // each warp owns rows 16rb + {gid, gid+8}, columns 32ch + 8nt + 2tig + {0,1}
-    const int rb = warp & 3, ch = warp >> 2;
+    // ---- rows: a half-warp per row, lane l the channels cb + 4(l % 16) .. +3 of row
+    // 16b + 2w + l / 16 (b = 0 .. 3)
+    constexpr int RB = C / (2 * kPairWarps);
+    const int hl = lane >> 4, c4 = 4 * (lane & 15);
+    uint2 wq[RB], wk[RB], wg[RB];
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+        const int r = 16 * b + 2 * warp + hl;
+        wq[b] = *reinterpret_cast<const uint2*>(stq + r * CH + c4);
+        wk[b] = *reinterpret_cast<const uint2*>(stk + r * CH + c4);
+        wg[b] = *reinterpret_cast<const uint2*>(stg + r * CH + c4);
+    }
+    const float4 dt4 = *reinterpret_cast<const float4*>(s.dtb + c4);
+    __syncthreads();   // the staged rows are read: dB and dAqk are reloaded over them
+    {
+        const float* gB = reinterpret_cast<const float*>(wy + WyOff::DB);
+        const float* gA = reinterpret_cast<const float*>(bg + BgOff::DAQK);
+        for (int i = tid; i < 2 * C * (C / 4); i += kPairThreads) {
+            const int m = i >> 10, r = (i >> 4) & (C - 1), j = (i & 15) * 4;
+            cp_async16((m ? s.dA : s.dB) + sw(r, j), (m ? gA : gB) + r * C + j);
+        }
+        cp_async_commit();
+    }
+    // each warp of the products owns rows 16rb + {gid, gid+8}, columns chw + 8nt + 2tig + {0,1}
+    const int rb = warp & 3, chw = (warp >> 2) * 32;
     constexpr int NT = 4;   // n-tiles of 8 columns per warp
+    const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB) + cb;
+    const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB) + cb;
+    const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT) + cb;
     // operands of the elementwise terms (dQbar, dKt) of this thread's elements: loaded
     // now, so that their latency hides under the row preparation
-    const float* gdQ = reinterpret_cast<const float*>(bg + BgOff::DQB);
-    const float* gdKb = reinterpret_cast<const float*>(bg + BgOff::DKB);
-    const float* gdKt = reinterpret_cast<const float*>(wy + WyOff::DKT);
     float2 eQ[NT][2], eKt[NT][2];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
+            const int row = rb * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2;
             eQ[nt][hh] = *reinterpret_cast<const float2*>(gdQ + row * D + col);
             eKt[nt][hh] = *reinterpret_cast<const float2*>(gdKt + row * D + col);
         }
-    prep_compute(rr, a_h, lb, L, s.qe, s.ke, s.kp, s.beta, s.inq, s.ink);
+
+    // ---- row preparation. Squared norms in the fixed order of the other chunk kernels:
+    // a fused chain over each lane's 4 channels, a butterfly over the 16 lanes of the
+    // row (this half of the channels), then the sum of the two halves' partials
+    auto un4 = [](uint2 w, float (&x)[4]) {
+        x[0] = bf_lo(w.x); x[1] = bf_hi(w.x); x[2] = bf_lo(w.y); x[3] = bf_hi(w.y);
+    };
+    {
+        float sq[RB], sk[RB];
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            float qv[4], kv[4];
+            un4(wq[b], qv); un4(wk[b], kv);
+            sq[b] = sq4(qv[0], qv[1], qv[2], qv[3]);
+            sk[b] = sq4(kv[0], kv[1], kv[2], kv[3]);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+            for (int b = 0; b < RB; ++b) {
+                sq[b] += __shfl_xor_sync(kAll, sq[b], o);
+                sk[b] += __shfl_xor_sync(kAll, sk[b], o);
+            }
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            if ((lane & 15) == 0) st_both(&s.xn[half][0][r], peer, sq[b]);
+            if ((lane & 15) == 1) st_both(&s.xn[half][1][r], peer, sk[b]);
+        }
+    }
+    cluster_arrive();
+    // gates and beta need no norm: computed while the peer's partials arrive
+    {
+        const float dtv[4] = {dt4.x, dt4.y, dt4.z, dt4.w};
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            float gr[4], al[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+            un4(wg[b], gr);
+            if (r < L) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) al[e] = __expf(lb * sigmoidf(a_h * (gr[e] + dtv[e])));
+            }
+            *reinterpret_cast<float4*>(s.kp + pidx(r, c4)) = make_float4(al[0], al[1], al[2], al[3]);
+            if ((lane & 15) == 0) s.beta[r] = r < L ? sigmoidf(bf2f(s.braw[r])) : 0.0f;
+        }
+    }
+    cluster_wait();
+#pragma unroll
+    for (int b = 0; b < RB; ++b) {
+        const int r = 16 * b + 2 * warp + hl;
+        const float iq = rsqrtf(s.xn[0][0][r] + s.xn[1][0][r] + 1e-6f);
+        const float ik = rsqrtf(s.xn[0][1][r] + s.xn[1][1][r] + 1e-6f);
+        float qv[4], kv[4];
+        un4(wq[b], qv); un4(wk[b], kv);
+        *reinterpret_cast<float4*>(s.qe + pidx(r, c4)) = make_float4(qv[0] * iq, qv[1] * iq, qv[2] * iq, qv[3] * iq);
+        *reinterpret_cast<float4*>(s.ke + pidx(r, c4)) = make_float4(kv[0] * ik, kv[1] * ik, kv[2] * ik, kv[3] * ik);
+        if ((lane & 15) == 0) {
+            s.inq[r] = iq;
+            s.ink[r] = ik;
+        }
+    }
     cp_async_wait_all();
     __syncthreads();
-    block_products(s.kp, s.qe, s.ke, s.em, s.ep, &s.fa);
+    // block products: thread (I, c) walks the 16 rows of block I in channel c
+    {
+        const int c = tid & (CH - 1), I = tid >> 6;
+        float al[SUB], e_m[SUB], e_p[SUB];
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) al[i] = s.kp[pidx(I * SUB + i, c)];
+        float pre = 1.0f;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) { pre *= al[i]; e_m[i] = pre; }
+        float suf = 1.0f;
+#pragma unroll
+        for (int i = SUB - 1; i >= 0; --i) { e_p[i] = suf; suf *= al[i]; }
+        s.fa.Db[I][c] = pre;
+#pragma unroll
+        for (int i = 0; i < SUB; ++i) {
+            const int a = pidx(I * SUB + i, c);
+            const float kh = s.ke[a];
+            s.ke[a] = kh * e_m[i];
+            s.kp[a] = kh * e_p[i];
+            s.qe[a] = s.qe[a] * e_m[i];
+            s.em[a] = e_m[i];
+        }
+    }
     __syncthreads();
-    block_factors(&s.fa);
+    if (tid < CH) {   // block factors of channel tid
+        const int c = tid;
+        const float d0 = s.fa.Db[0][c], d1 = s.fa.Db[1][c], d2 = s.fa.Db[2][c], d3 = s.fa.Db[3][c];
+        s.fa.Pb[0][c] = 1.0f; s.fa.Pb[1][c] = d0; s.fa.Pb[2][c] = d0 * d1; s.fa.Pb[3][c] = d0 * d1 * d2;
+        s.fa.gl[c] = d0 * d1 * d2 * d3;
+        s.fa.Sf[3][c] = 1.0f; s.fa.Sf[2][c] = d3; s.fa.Sf[1][c] = d2 * d3; s.fa.Sf[0][c] = d1 * d2 * d3;
+        s.fa.F[0][0][c] = 1.0f / d0; s.fa.F[1][1][c] = 1.0f / d1; s.fa.F[2][2][c] = 1.0f / d2; s.fa.F[3][3][c] = 1.0f / d3;
+        s.fa.F[1][0][c] = 1.0f; s.fa.F[2][1][c] = 1.0f; s.fa.F[3][2][c] = 1.0f;
+        s.fa.F[2][0][c] = d1; s.fa.F[3][1][c] = d2; s.fa.F[3][0][c] = d1 * d2;
+    }
     __syncthreads();
 
     // (c) elementwise terms of Q^*Gamma and K^*Gamma start the accumulators (the Kbar terms
@@ -142,14 +317,19 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
+            const int row = rb * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+            const float2 pb = *reinterpret_cast<const float2*>(&s.fa.Pb[rb][col]);
+            const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
+            const float2 qev = *reinterpret_cast<const float2*>(s.qe + a);
+            const float2 kev = *reinterpret_cast<const float2*>(s.ke + a);
+            const float pbv[2] = {pb.x, pb.y}, emx[2] = {emv.x, emv.y}, qex[2] = {qev.x, qev.y},
+                        kex[2] = {kev.x, kev.y};
             const float dQv[2] = {eQ[nt][hh].x, eQ[nt][hh].y}, dKtv[2] = {eKt[nt][hh].x, eKt[nt][hh].y};
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
-                const int e = hh * 2 + e2, cc = col + e2, I = row >> 4;
-                const float pb = s.fa.Pb[I][cc];
-                const float gam = s.em[row * PS + cc] * pb;
-                const float qb = s.qe[row * PS + cc] * pb, kt = s.ke[row * PS + cc] * pb;
+                const int e = hh * 2 + e2;
+                const float gam = emx[e2] * pbv[e2];
+                const float qb = qex[e2] * pbv[e2], kt = kex[e2] * pbv[e2];
                 adq[nt][e] = dQv[e2] * gam;
                 adk[nt][e] = dKtv[e2] * gam;
                 adg[nt][e] = dQv[e2] * qb + dKtv[e2] * kt;
@@ -170,12 +350,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
-                const Frag4 fb = frag4(s.dB[r0 * PC + j0], s.dB[r1 * PC + j0], s.dB[r0 * PC + j1], s.dB[r1 * PC + j1]);
-                const Frag4 fa = frag4(s.dA[r0 * PC + j0], s.dA[r1 * PC + j0], s.dA[r0 * PC + j1], s.dA[r1 * PC + j1]);
+                const Frag4 fb = frag4(s.dB[sw(r0, j0)], s.dB[sw(r1, j0)], s.dB[sw(r0, j1)], s.dB[sw(r1, j1)]);
+                const Frag4 fa = frag4(s.dA[sw(r0, j0)], s.dA[sw(r1, j0)], s.dA[sw(r0, j1)], s.dA[sw(r1, j1)]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
-                    const int c = ch * 32 + nt * 8 + gid;
-                    const Frag2 kb = frag2(s.kp[j0 * PS + c], s.kp[j1 * PS + c]);
+                    const int c = chw + nt * 8 + gid;
+                    const Frag2 kb = frag2(s.kp[pidx(j0, c)], s.kp[pidx(j1, c)]);
                     mma3(accB[nt], fb, kb);
                     mma3(accA[nt], fa, kb);
                 }
@@ -184,18 +364,29 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int row = I * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
-                    const float fc = f[col];
-                    const float R = s.em[row * PS + col] * fc;
-                    adk[nt][e] += R * accB[nt][e];
-                    adq[nt][e] += R * accA[nt][e];
-                    adg[nt][e] += (s.ke[row * PS + col] * fc) * accB[nt][e];
-                    adg[nt][e] += (s.qe[row * PS + col] * fc) * accA[nt][e];
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int row = I * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+                    const float2 f2 = *reinterpret_cast<const float2*>(f + col);
+                    const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
+                    const float2 kev = *reinterpret_cast<const float2*>(s.ke + a);
+                    const float2 qev = *reinterpret_cast<const float2*>(s.qe + a);
+                    const float fx[2] = {f2.x, f2.y}, emx[2] = {emv.x, emv.y}, kex[2] = {kev.x, kev.y},
+                                qex[2] = {qev.x, qev.y};
+#pragma unroll
+                    for (int e2 = 0; e2 < 2; ++e2) {
+                        const int e = hh * 2 + e2;
+                        const float fc = fx[e2];
+                        const float R = emx[e2] * fc;
+                        adk[nt][e] += R * accB[nt][e];
+                        adq[nt][e] += R * accA[nt][e];
+                        adg[nt][e] += (kex[e2] * fc) * accB[nt][e];
+                        adg[nt][e] += (qex[e2] * fc) * accA[nt][e];
+                    }
                 }
         }
     }
-    // (b) column side: rows j of block J = rb, row blocks I >= J
+    // (b) column side: rows j of block J = rb, row blocks I >= J. E+ of those rows is
+    // D_J / E- (it enters only dk^, no cancelling term)
     {
         const int J = rb;
         float acc[NT][4];
@@ -212,12 +403,12 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
                 for (int kk = 0; kk < 2; ++kk) {
                     const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
                     const int c0 = J * SUB + gid, c1 = c0 + 8;
-                    const Frag4 af = frag4(dM[i0 * PC + c0], dM[i0 * PC + c1], dM[i1 * PC + c0], dM[i1 * PC + c1]);
+                    const Frag4 af = frag4(dM[sw(i0, c0)], dM[sw(i0, c1)], dM[sw(i1, c0)], dM[sw(i1, c1)]);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const int c = ch * 32 + nt * 8 + gid;
+                        const int c = chw + nt * 8 + gid;
                         const float fc = f[c];
-                        mma3(acc[nt], af, frag2(base[i0 * PS + c] * fc, base[i1 * PS + c] * fc));
+                        mma3(acc[nt], af, frag2(base[pidx(i0, c)] * fc, base[pidx(i1, c)] * fc));
                     }
                 }
             }
@@ -225,162 +416,197 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = J * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
-                adk[nt][e] += s.ep[row * PS + col] * acc[nt][e];
-                adg[nt][e] -= s.kp[row * PS + col] * acc[nt][e];
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = J * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+                const float2 db = *reinterpret_cast<const float2*>(&s.fa.Db[J][col]);
+                const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
+                const float2 kpv = *reinterpret_cast<const float2*>(s.kp + a);
+                const float dbx[2] = {db.x, db.y}, emx[2] = {emv.x, emv.y}, kpx[2] = {kpv.x, kpv.y};
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int e = hh * 2 + e2;
+                    adk[nt][e] += __fdividef(dbx[e2], emx[e2]) * acc[nt][e];
+                    adg[nt][e] -= kpx[e2] * acc[nt][e];
+                }
             }
     }
-    // (c) elementwise terms of Kbar
+    // (c) elementwise terms of Kbar (E+ again as D_I / E-)
     float pk[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int row = rb * SUB + gid + hh * 8, col = ch * 32 + nt * 8 + tig * 2;
+            const int row = rb * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
             const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
-            const float dKbv[2] = {dKb2.x, dKb2.y};
+            const float2 sf = *reinterpret_cast<const float2*>(&s.fa.Sf[rb][col]);
+            const float2 db = *reinterpret_cast<const float2*>(&s.fa.Db[rb][col]);
+            const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
+            const float2 kpv = *reinterpret_cast<const float2*>(s.kp + a);
+            const float dKbv[2] = {dKb2.x, dKb2.y}, sfx[2] = {sf.x, sf.y}, dbx[2] = {db.x, db.y},
+                        emx[2] = {emv.x, emv.y}, kpx[2] = {kpv.x, kpv.y};
 #pragma unroll
             for (int e2 = 0; e2 < 2; ++e2) {
-                const int e = hh * 2 + e2, cc = col + e2, I = row >> 4;
-                const float sf = s.fa.Sf[I][cc];
-                const float el = s.ep[row * PS + cc] * sf, kb = s.kp[row * PS + cc] * sf;
+                const int e = hh * 2 + e2;
+                const float el = __fdividef(dbx[e2], emx[e2]) * sfx[e2], kb = kpx[e2] * sfx[e2];
                 adk[nt][e] += dKbv[e2] * el;
                 pk[nt][e] = dKbv[e2] * kb;
             }
         }
-    __syncthreads();   // all reads of qe, ke, kp, em done
+    __syncthreads();   // all reads of qe, ke, kp, em, dB, dA done
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const int row = rb * SUB + gid + (e >> 1) * 8, col = ch * 32 + nt * 8 + tig * 2 + (e & 1);
-            s.qe[row * PS + col] = adq[nt][e];
-            s.ke[row * PS + col] = adk[nt][e];
-            s.kp[row * PS + col] = adg[nt][e];
-            s.em[row * PS + col] = pk[nt][e];
+        for (int hh = 0; hh < 2; ++hh) {
+            const int row = rb * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+            *reinterpret_cast<float2*>(s.qe + a) = make_float2(adq[nt][hh * 2], adq[nt][hh * 2 + 1]);
+            *reinterpret_cast<float2*>(s.ke + a) = make_float2(adk[nt][hh * 2], adk[nt][hh * 2 + 1]);
+            *reinterpret_cast<float2*>(s.kp + a) = make_float2(adg[nt][hh * 2], adg[nt][hh * 2 + 1]);
+            *reinterpret_cast<float2*>(s.em + a) = make_float2(pk[nt][hh * 2], pk[nt][hh * 2 + 1]);
         }
     __syncthreads();
-    // dA and ep are no longer read: the next tile's rows stream in during the chains below
+    // dB and dAqk are no longer read: the next tile's rows stream in during the chains below
     if (cn.L > 0) stage_tile(nxt, cn);
 
-    // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); all rows of a warp loaded at once
-    {
-        const int c0 = lane * 4;
-        uint2 wq[C / kPairWarps], wk[C / kPairWarps];
-#pragma unroll
-        for (int b = 0; b < C / kPairWarps; ++b) {
-            const int r = warp + kPairWarps * b;
-            wq[b] = wk[b] = make_uint2(0u, 0u);
-            if (r < L) {
-                const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-                wq[b] = *reinterpret_cast<const uint2*>(q + base);
-                wk[b] = *reinterpret_cast<const uint2*>(k + base);
-            }
-        }
-#pragma unroll
-        for (int b = 0; b < C / kPairWarps; ++b) {
-            const int r = warp + kPairWarps * b;
-            if (r >= L) break;
-            const size_t base = ((size_t)(t0 + r) * H + h) * D + c0;
-#pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint2 w = which == 0 ? wq[b] : wk[b];
-                const float* dx = which == 0 ? s.qe : s.ke;
-                const float inv = which == 0 ? s.inq[r] : s.ink[r];
-                const float xv[4] = {bf2f((uint16_t)(w.x & 0xffffu)) * inv, bf2f((uint16_t)(w.x >> 16)) * inv,
-                                     bf2f((uint16_t)(w.y & 0xffffu)) * inv, bf2f((uint16_t)(w.y >> 16)) * inv};
-                float dot = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 4; ++e) dot += xv[e] * dx[r * PS + c0 + e];
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-                uint16_t out[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) out[e] = f2bf((dx[r * PS + c0 + e] - xv[e] * dot) * inv);
-                uint16_t* dst = which == 0 ? dq : dk;
-                *reinterpret_cast<uint2*>(dst + base) = make_uint2((uint32_t)out[0] | ((uint32_t)out[1] << 16),
-                                                                   (uint32_t)out[2] | ((uint32_t)out[3] << 16));
-            }
-        }
-    }
-    // thread (row group rg, channel c) owns rows rg + RG b of channel c in the gate chain;
-    // its raw gates are loaded now, all at once
-    constexpr int RG = kPairWarps * 32 / D;   // row groups (threads per channel)
-    const int cc = tid & (D - 1), rg = tid >> 7;
+    // thread (row group rg, channel cc) owns rows rg + RG b of channel cc in the gate chain
+    constexpr int RG = kPairThreads / CH;   // row groups (threads per channel)
+    const int cc = tid & (CH - 1), rg = tid >> 6;
     uint16_t graw[C / RG];
+    float dtc;
+    // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); the row dot products
+    // from both halves of the channels (rows as in the preparation)
+    {
+        uint2 xq[RB], xk[RB];
 #pragma unroll
-    for (int b = 0; b < C / RG; ++b) {
-        const int r = rg + RG * b;
-        graw[b] = r < L ? g_raw[((size_t)(t0 + r) * H + h) * D + cc] : (uint16_t)0;
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            xq[b] = xk[b] = make_uint2(0u, 0u);
+            if (r < L) {
+                const size_t base = ((size_t)(t0 + r) * H + h) * D + cb + c4;
+                xq[b] = *reinterpret_cast<const uint2*>(q + base);
+                xk[b] = *reinterpret_cast<const uint2*>(k + base);
+            }
+        }
+        float pq[RB], pkd[RB];
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            const float iq = s.inq[r], ik = s.ink[r];
+            const float4 gq = *reinterpret_cast<const float4*>(s.qe + pidx(r, c4));
+            const float4 gk = *reinterpret_cast<const float4*>(s.ke + pidx(r, c4));
+            float qv[4], kv[4];
+            un4(xq[b], qv); un4(xk[b], kv);
+            pq[b] = (qv[0] * iq) * gq.x + (qv[1] * iq) * gq.y + (qv[2] * iq) * gq.z + (qv[3] * iq) * gq.w;
+            pkd[b] = (kv[0] * ik) * gk.x + (kv[1] * ik) * gk.y + (kv[2] * ik) * gk.z + (kv[3] * ik) * gk.w;
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1)
+#pragma unroll
+            for (int b = 0; b < RB; ++b) {
+                pq[b] += __shfl_xor_sync(kAll, pq[b], o);
+                pkd[b] += __shfl_xor_sync(kAll, pkd[b], o);
+            }
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            if ((lane & 15) == 0) st_both(&s.xd[half][0][r], peer, pq[b]);
+            if ((lane & 15) == 1) st_both(&s.xd[half][1][r], peer, pkd[b]);
+        }
+        cluster_arrive();
+        // the raw gates of the gate chain load while the peer's partials arrive
+#pragma unroll
+        for (int b = 0; b < C / RG; ++b) {
+            const int r = rg + RG * b;
+            graw[b] = r < L ? g_raw[((size_t)(t0 + r) * H + h) * D + cb + cc] : (uint16_t)0;
+        }
+        dtc = dt_bias[h * D + cb + cc];
+        cluster_wait();
+#pragma unroll
+        for (int b = 0; b < RB; ++b) {
+            const int r = 16 * b + 2 * warp + hl;
+            if (r < L) {
+                const size_t base = ((size_t)(t0 + r) * H + h) * D + cb + c4;
+#pragma unroll
+                for (int which = 0; which < 2; ++which) {
+                    float xv[4];
+                    un4(which == 0 ? xq[b] : xk[b], xv);
+                    const float inv = which == 0 ? s.inq[r] : s.ink[r];
+                    const float dot = s.xd[0][which][r] + s.xd[1][which][r];
+                    const float4 g = *reinterpret_cast<const float4*>((which == 0 ? s.qe : s.ke) + pidx(r, c4));
+                    const float gv[4] = {g.x, g.y, g.z, g.w};
+                    uint16_t o[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) o[e] = f2bf((gv[e] - (xv[e] * inv) * dot) * inv);
+                    *reinterpret_cast<uint2*>((which == 0 ? dq : dk) + base) =
+                        make_uint2((uint32_t)o[0] | ((uint32_t)o[1] << 16), (uint32_t)o[2] | ((uint32_t)o[3] << 16));
+                }
+            }
+        }
     }
-    const float dtc = dt_bias[h * D + cc];
     // dg: sums over rows per key channel, written back as dg_t
     //   dg_t = sum_{i>=t} dG'_i + sum_{i<t} dKbar_i Kbar_i + dgam exp(G_L)
-    // blocked over RG contiguous row segments of SEG rows: segment sums first (scratch in
-    // the dB tile, which is no longer read), then each segment from its offsets
+    // blocked over RG contiguous row segments of SEG rows: segment sums first, then each
+    // segment from its offsets
     float* part = reinterpret_cast<float*>(ws + lay.part) + tile * (D + 4);
     {
         constexpr int SEG = C / RG;
-        float* segE = s.dB;            // [RG][128] sums of the dKbar Kbar terms
-        float* segK = s.dB + RG * D;   // [RG][128] sums of dG'
+        float* segE = scr;             // [RG][64] sums of the dKbar Kbar terms
+        float* segK = scr + RG * CH;   // [RG][64] sums of dG'
         const int r0 = rg * SEG, r1 = min(r0 + SEG, L);
         float se = 0.0f, sk = 0.0f;
-        for (int r = r0; r < r1; ++r) { se += s.em[r * PS + cc]; sk += s.kp[r * PS + cc]; }
-        segE[rg * D + cc] = se;
-        segK[rg * D + cc] = sk;
+        for (int r = r0; r < r1; ++r) { se += s.em[pidx(r, cc)]; sk += s.kp[pidx(r, cc)]; }
+        segE[rg * CH + cc] = se;
+        segK[rg * CH + cc] = sk;
         __syncthreads();
-        float run = 0.0f, rev = reinterpret_cast<const float*>(bg + BgOff::DGAM)[cc] * s.fa.gl[cc];
-        for (int g2 = 0; g2 < rg; ++g2) run += segE[g2 * D + cc];
-        for (int g2 = RG - 1; g2 > rg; --g2) rev += segK[g2 * D + cc];
+        float run = 0.0f, rev = reinterpret_cast<const float*>(bg + BgOff::DGAM)[cb + cc] * s.fa.gl[cc];
+        for (int g2 = 0; g2 < rg; ++g2) run += segE[g2 * CH + cc];
+        for (int g2 = RG - 1; g2 > rg; --g2) rev += segK[g2 * CH + cc];
         for (int r = r0; r < r1; ++r) {
-            const float p = s.em[r * PS + cc];
-            s.em[r * PS + cc] = run;
+            const int a = pidx(r, cc);
+            const float p = s.em[a];
+            s.em[a] = run;
             run += p;
         }
         for (int r = r1 - 1; r >= r0; --r) {
-            rev += s.kp[r * PS + cc];
-            s.kp[r * PS + cc] = rev + s.em[r * PS + cc];
+            const int a = pidx(r, cc);
+            rev += s.kp[a];
+            s.kp[a] = rev + s.em[a];
         }
     }
     __syncthreads();
-    // gate chain, every thread: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
+    // gate chain: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
     {
-        const int c = cc, r0 = rg;
         float ddt = 0.0f, dA = 0.0f;
 #pragma unroll
         for (int b = 0; b < C / RG; ++b) {
-            const int r = r0 + RG * b;
+            const int r = rg + RG * b;
             if (r >= L) break;
-            const size_t gi = ((size_t)(t0 + r) * H + h) * D + c;
+            const size_t gi = ((size_t)(t0 + r) * H + h) * D + cb + cc;
             const float x = bf2f(graw[b]) + dtc;
-            const float dgr = s.kp[r * PS + c] * lb * dsigmoidf(a_h * x) * a_h;
+            const float dgr = s.kp[pidx(r, cc)] * lb * dsigmoidf(a_h * x) * a_h;
             dg_raw[gi] = f2bf(dgr);
             ddt += dgr;
             dA += dgr * x;
         }
-        // RG threads per channel (rows r = r0 mod RG); combined below in a fixed order
-        s.dB[(2 * RG + r0) * D + c] = ddt;
-        s.dB[(3 * RG + r0) * D + c] = dA;
+        // RG threads per channel (rows r = rg mod RG); combined below in a fixed order
+        scr[(2 * RG + rg) * CH + cc] = ddt;
+        scr[(3 * RG + rg) * CH + cc] = dA;
     }
     __syncthreads();
-    if (tid < D) {
+    if (tid < CH) {
         float a = 0.0f, b = 0.0f;
 #pragma unroll
-        for (int g = 0; g < RG; ++g) { a += s.dB[(2 * RG + g) * D + tid]; b += s.dB[(3 * RG + g) * D + tid]; }
-        part[tid] = a;
-        s.red[tid] = b;
+        for (int g = 0; g < RG; ++g) { a += scr[(2 * RG + g) * CH + tid]; b += scr[(3 * RG + g) * CH + tid]; }
+        part[cb + tid] = a;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) b += __shfl_xor_sync(kAll, b, o);
+        if (lane == 0) s.red[warp] = b;
     }
-    if (tid < L) {
+    if (half == 0 && tid < L) {
         const float db = reinterpret_cast<const float*>(wy + WyOff::DBETA)[tid];
         dbeta_raw[(size_t)(t0 + tid) * H + h] = f2bf(db * dsigmoidf(bf2f(beta_raw[(size_t)(t0 + tid) * H + h])));
     }
     __syncthreads();
-    for (int off = D / 2; off > 0; off >>= 1) {
-        if (tid < off) s.red[tid] += s.red[tid + off];
-        __syncthreads();
-    }
-    if (tid == 0) part[D] = s.red[0];
+    if (tid == 0) part[D + half] = s.red[0] + s.red[1];
     if (cn.L <= 0) break;
     tile_i = nxt;
     ci = cn;
@@ -390,8 +616,9 @@ __global__ void __launch_bounds__(kPairWarps * 32, 1)
 }
 
 // Deterministic sum of the per-chunk parameter partials, per head: eight running sums
-// over the chunks (chunk index mod 8), then combined in a fixed order. Empty chunk
-// records only follow the last real chunk.
+// over the chunks (chunk index mod 8), then combined in a fixed order. Each chunk
+// holds one ddt_bias partial per channel and two dA_log partials (one per channel
+// half). Empty chunk records only follow the last real chunk.
 __global__ void __launch_bounds__(128)
     kda_param_reduce_kernel(int H, float* __restrict__ dA_log, float* __restrict__ ddt_bias,
                             uint8_t* __restrict__ ws, Layout lay) {
@@ -420,13 +647,13 @@ __global__ void __launch_bounds__(128)
         for (int u = 0; u < 8; ++u) {
             const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
             acc[u] += p[c];
-            if (c == 0) accA[u] += p[D];
+            if (c == 0) accA[u] += p[D] + p[D + 1];
         }
     }
     for (int u = 0; ch + u < n; ++u) {
         const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
         acc[u] += p[c];
-        if (c == 0) accA[u] += p[D];
+        if (c == 0) accA[u] += p[D] + p[D + 1];
     }
     float tot = 0.0f, totA = 0.0f;
 #pragma unroll

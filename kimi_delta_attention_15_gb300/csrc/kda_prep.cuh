@@ -29,6 +29,11 @@ struct Factors {
     float gl[D];
 };
 
+// Sum of squares of four consecutive channels, in one fixed fused order.
+__device__ __forceinline__ float sq4(float a, float b, float c, float d) {
+    return fmaf(d, d, fmaf(c, c, fmaf(b, b, a * a)));
+}
+
 // Raw bf16 rows of one chunk held in registers: with NW warps, warp w holds
 // rows w + NW b, lane l channels 4l .. 4l+3. The kernels stage a tile's rows in
 // shared memory ahead of use and fill these registers from there.
@@ -76,23 +81,28 @@ __device__ __forceinline__ void prep_compute(const RowRegsT<NW>& rr, float a_h, 
         out[0] = bf2f((uint16_t)(w.x & 0xffffu)); out[1] = bf2f((uint16_t)(w.x >> 16));
         out[2] = bf2f((uint16_t)(w.y & 0xffffu)); out[3] = bf2f((uint16_t)(w.y >> 16));
     };
-    // squared norms of all rows first, then the reductions interleaved across rows
+    // squared norms of all rows first, then the reductions interleaved across rows.
+    // Fixed order: a fused chain over each lane's 4 channels, a butterfly over the 16
+    // lanes of each 64-channel half, then the two halves (the pair-term kernel, which
+    // splits the channels between two CTAs, forms the same sums bit for bit)
     constexpr int RB = RowRegsT<NW>::RB;
     float sq[RB], sk[RB];
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
         float qv[4], kv[4];
         un(rr.q[b], qv); un(rr.k[b], kv);
-        sq[b] = qv[0] * qv[0] + qv[1] * qv[1] + qv[2] * qv[2] + qv[3] * qv[3];
-        sk[b] = kv[0] * kv[0] + kv[1] * kv[1] + kv[2] * kv[2] + kv[3] * kv[3];
+        sq[b] = sq4(qv[0], qv[1], qv[2], qv[3]);
+        sk[b] = sq4(kv[0], kv[1], kv[2], kv[3]);
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
+    for (int i = 0; i < 5; ++i) {
+        const int o = i < 4 ? 8 >> i : 16;
 #pragma unroll
         for (int b = 0; b < RB; ++b) {
             sq[b] += __shfl_xor_sync(0xffffffffu, sq[b], o);
             sk[b] += __shfl_xor_sync(0xffffffffu, sk[b], o);
         }
+    }
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
         const int r = warp + b * NW;
