@@ -6,9 +6,9 @@
 //     with dB (WY kernel) and dAqk (state-products kernel), for column block J:
 //     a = dM[:,J] Kt_J,  b = dM[:,J]^T Xt_J   (Xt_J = x^ e^{G-G_eJ}, Kt_J = k^_J e^{G_eJ-G_J})
 //     dx += e^{G-G_eJ} a,  dk_J += e^{G_eJ-G_J} b,  dG += Xt_J a,  dG_J -= Kt_J b
-//     (split-tf32 products, about fp32 accurate, and both dG terms multiply by
-//      the same fp32 operand values, so the pairs inside [t, L) cancel in the
-//      reverse cumulative sum as they must);
+//     (split-tf32 products, about fp32 accurate, and both dG terms multiply the
+//      same factors k^, E-, E+ and f_IJ, rounded to fp32 at most once apart, so the
+//      pairs inside [t, L) cancel in the reverse cumulative sum to fp32 accuracy);
 //   dq^ += dQbar Gamma, dk^ += dKt Gamma + dKbar e^{G_L-G},
 //   dG  += dQbar Q^Gamma + dKt K^Gamma - dKbar Kbar,
 //   dG_L = sum_i dKbar_i Kbar_i + dgam exp(G_L).
@@ -336,17 +336,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             }
         }
 
-    // (a) row side: rows of block I = rb, column blocks J <= I; the products with dB
-    // and with dAqk share their B fragments (k^ E+ of block J) and the decay R
+    // (a) row side: rows of block I = rb, column blocks J <= I. The decay factor f_IJ of
+    // each column block is folded into the shared B operand (k^ E+ of block J, times f_IJ
+    // per channel), so the products with dB and with dAqk accumulate over all J and the
+    // epilogue, with E- of the rows, runs once
     {
         const int I = rb;
         const int r0 = I * SUB + gid, r1 = r0 + 8;
+        float accB[NT][4], accA[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) accB[nt][e] = accA[nt][e] = 0.0f;
         for (int J = 0; J <= I; ++J) {
-            float accB[NT][4], accA[NT][4];
+            const float* f = s.fa.F[I][J];
+            float fc[NT];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) accB[nt][e] = accA[nt][e] = 0.0f;
+            for (int nt = 0; nt < NT; ++nt) fc[nt] = f[chw + nt * 8 + gid];
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
@@ -355,35 +361,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int c = chw + nt * 8 + gid;
-                    const Frag2 kb = frag2(s.kp[pidx(j0, c)], s.kp[pidx(j1, c)]);
+                    const Frag2 kb = frag2(s.kp[pidx(j0, c)] * fc[nt], s.kp[pidx(j1, c)] * fc[nt]);
                     mma3(accB[nt], fb, kb);
                     mma3(accA[nt], fa, kb);
                 }
             }
-            const float* f = s.fa.F[I][J];
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int row = I * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
-                    const float2 f2 = *reinterpret_cast<const float2*>(f + col);
-                    const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
-                    const float2 kev = *reinterpret_cast<const float2*>(s.ke + a);
-                    const float2 qev = *reinterpret_cast<const float2*>(s.qe + a);
-                    const float fx[2] = {f2.x, f2.y}, emx[2] = {emv.x, emv.y}, kex[2] = {kev.x, kev.y},
-                                qex[2] = {qev.x, qev.y};
-#pragma unroll
-                    for (int e2 = 0; e2 < 2; ++e2) {
-                        const int e = hh * 2 + e2;
-                        const float fc = fx[e2];
-                        const float R = emx[e2] * fc;
-                        adk[nt][e] += R * accB[nt][e];
-                        adq[nt][e] += R * accA[nt][e];
-                        adg[nt][e] += (kex[e2] * fc) * accB[nt][e];
-                        adg[nt][e] += (qex[e2] * fc) * accA[nt][e];
-                    }
-                }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = I * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+                const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
+                const float2 kev = *reinterpret_cast<const float2*>(s.ke + a);
+                const float2 qev = *reinterpret_cast<const float2*>(s.qe + a);
+                const float emx[2] = {emv.x, emv.y}, kex[2] = {kev.x, kev.y}, qex[2] = {qev.x, qev.y};
+#pragma unroll
+                for (int e2 = 0; e2 < 2; ++e2) {
+                    const int e = hh * 2 + e2;
+                    adk[nt][e] += emx[e2] * accB[nt][e];
+                    adq[nt][e] += emx[e2] * accA[nt][e];
+                    adg[nt][e] += kex[e2] * accB[nt][e];
+                    adg[nt][e] += qex[e2] * accA[nt][e];
+                }
+            }
     }
     // (b) column side: rows j of block J = rb, row blocks I >= J. E+ of those rows is
     // D_J / E- (it enters only dk^, no cancelling term)
