@@ -136,6 +136,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     uint16_t* const stk = stq + C * CH;
     uint16_t* const stg = reinterpret_cast<uint16_t*>(s.dB + 1024);
     float* const scr = s.dB;                                     // [4][RG][64] dg scratch
+    uint16_t* const stgc = reinterpret_cast<uint16_t*>(s.qe);   // the tile's raw gate rows, in the gate chain
     float alog_next = 0.0f;
     uint16_t braw_next = 0;
     // this CTA's channels of the raw rows of tile t_i (record cn); rows past the chunk read as zero
@@ -471,8 +472,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     // thread (row group rg, channel cc) owns rows rg + RG b of channel cc in the gate chain
     constexpr int RG = kPairThreads / CH;   // row groups (threads per channel)
     const int cc = tid & (CH - 1), rg = tid >> 6;
-    uint16_t graw[C / RG];
-    float dtc;
+    const float dtc = dt_bias[h * D + cb + cc];
     // L2-norm chains: dx = (dx^ - x^ (x^ . dx^)) / sqrt(|x|^2 + eps); the row dot products
     // from both halves of the channels (rows as in the preparation)
     {
@@ -513,13 +513,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             if ((lane & 15) == 1) st_both(&s.xd[half][1][r], peer, pkd[b]);
         }
         cluster_arrive();
-        // the raw gates of the gate chain load while the peer's partials arrive
-#pragma unroll
-        for (int b = 0; b < C / RG; ++b) {
-            const int r = rg + RG * b;
-            graw[b] = r < L ? g_raw[((size_t)(t0 + r) * H + h) * D + cb + cc] : (uint16_t)0;
-        }
-        dtc = dt_bias[h * D + cb + cc];
         cluster_wait();
 #pragma unroll
         for (int b = 0; b < RB; ++b) {
@@ -558,6 +551,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
         segE[rg * CH + cc] = se;
         segK[rg * CH + cc] = sk;
         __syncthreads();
+        // the chains have read dq^ and dk^: this CTA's channels of the raw gate rows of the
+        // tile stream into the dq^ tile during the scan (rows past the chunk are not read)
+        for (int seg = tid; seg < C * (CH / 8); seg += kPairThreads) {
+            const int r = seg >> 3, c8 = (seg & 7) * 8;
+            if (r < L) cp_async16(stgc + r * CH + c8, g_raw + ((size_t)(t0 + r) * H + h) * D + cb + c8);
+        }
+        cp_async_commit();
         float run = 0.0f, rev = reinterpret_cast<const float*>(bg + BgOff::DGAM)[cb + cc] * s.fa.gl[cc];
         for (int g2 = 0; g2 < rg; ++g2) run += segE[g2 * CH + cc];
         for (int g2 = RG - 1; g2 > rg; --g2) rev += segK[g2 * CH + cc];
@@ -573,6 +573,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             s.kp[a] = rev + s.em[a];
         }
     }
+    cp_async_wait_all();
     __syncthreads();
     // gate chain: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
     {
@@ -582,7 +583,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             const int r = rg + RG * b;
             if (r >= L) break;
             const size_t gi = ((size_t)(t0 + r) * H + h) * D + cb + cc;
-            const float x = bf2f(graw[b]) + dtc;
+            const float x = bf2f(stgc[r * CH + cc]) + dtc;
             const float dgr = s.kp[pidx(r, cc)] * lb * dsigmoidf(a_h * x) * a_h;
             dg_raw[gi] = f2bf(dgr);
             ddt += dgr;
