@@ -536,18 +536,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             }
         }
     }
-    // dg: sums over rows per key channel, written back as dg_t
+    // dg: sums over rows per key channel
     //   dg_t = sum_{i>=t} dG'_i + sum_{i<t} dKbar_i Kbar_i + dgam exp(G_L)
-    // blocked over RG contiguous row segments of SEG rows: segment sums first, then each
-    // segment from its offsets
+    // blocked over RG contiguous row segments of SEG rows, one per thread of the channel:
+    // segment sums first, then each segment from its offsets, in registers; the gate chain
+    // follows on the same rows
     float* part = reinterpret_cast<float*>(ws + lay.part) + tile * (D + 4);
     {
         constexpr int SEG = C / RG;
         float* segE = scr;             // [RG][64] sums of the dKbar Kbar terms
         float* segK = scr + RG * CH;   // [RG][64] sums of dG'
-        const int r0 = rg * SEG, r1 = min(r0 + SEG, L);
+        const int r0 = rg * SEG;
+        float pe[SEG], pg[SEG];
+#pragma unroll
+        for (int i = 0; i < SEG; ++i) {
+            const bool v = r0 + i < L;
+            pe[i] = v ? s.em[pidx(r0 + i, cc)] : 0.0f;
+            pg[i] = v ? s.kp[pidx(r0 + i, cc)] : 0.0f;
+        }
         float se = 0.0f, sk = 0.0f;
-        for (int r = r0; r < r1; ++r) { se += s.em[pidx(r, cc)]; sk += s.kp[pidx(r, cc)]; }
+#pragma unroll
+        for (int i = 0; i < SEG; ++i) { se += pe[i]; sk += pg[i]; }
         segE[rg * CH + cc] = se;
         segK[rg * CH + cc] = sk;
         __syncthreads();
@@ -561,35 +570,33 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
         float run = 0.0f, rev = reinterpret_cast<const float*>(bg + BgOff::DGAM)[cb + cc] * s.fa.gl[cc];
         for (int g2 = 0; g2 < rg; ++g2) run += segE[g2 * CH + cc];
         for (int g2 = RG - 1; g2 > rg; --g2) rev += segK[g2 * CH + cc];
-        for (int r = r0; r < r1; ++r) {
-            const int a = pidx(r, cc);
-            const float p = s.em[a];
-            s.em[a] = run;
+#pragma unroll
+        for (int i = 0; i < SEG; ++i) {   // exclusive prefix of the Kbar terms
+            const float p = pe[i];
+            pe[i] = run;
             run += p;
         }
-        for (int r = r1 - 1; r >= r0; --r) {
-            const int a = pidx(r, cc);
-            rev += s.kp[a];
-            s.kp[a] = rev + s.em[a];
+#pragma unroll
+        for (int i = SEG - 1; i >= 0; --i) {   // dg of row r0 + i
+            rev += pg[i];
+            pg[i] = rev + pe[i];
         }
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    // gate chain: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
-    {
+        cp_async_wait_all();
+        __syncthreads();
+        // gate chain: du = dg lb sigmoid'(a (g_raw + dt_bias)), dg_raw = du a
         float ddt = 0.0f, dA = 0.0f;
 #pragma unroll
-        for (int b = 0; b < C / RG; ++b) {
-            const int r = rg + RG * b;
-            if (r >= L) break;
-            const size_t gi = ((size_t)(t0 + r) * H + h) * D + cb + cc;
-            const float x = bf2f(stgc[r * CH + cc]) + dtc;
-            const float dgr = s.kp[pidx(r, cc)] * lb * dsigmoidf(a_h * x) * a_h;
-            dg_raw[gi] = f2bf(dgr);
-            ddt += dgr;
-            dA += dgr * x;
+        for (int i = 0; i < SEG; ++i) {
+            const int r = r0 + i;
+            if (r < L) {
+                const float x = bf2f(stgc[r * CH + cc]) + dtc;
+                const float dgr = pg[i] * lb * dsigmoidf(a_h * x) * a_h;
+                dg_raw[((size_t)(t0 + r) * H + h) * D + cb + cc] = f2bf(dgr);
+                ddt += dgr;
+                dA += dgr * x;
+            }
         }
-        // RG threads per channel (rows r = rg mod RG); combined below in a fixed order
+        // RG threads per channel (row segments); combined below in a fixed order
         scr[(2 * RG + rg) * CH + cc] = ddt;
         scr[(3 * RG + rg) * CH + cc] = dA;
     }
