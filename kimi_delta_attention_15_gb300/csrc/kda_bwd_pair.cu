@@ -391,30 +391,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     // D_J / E- (it enters only dk^, no cancelling term)
     {
         const int J = rb;
-        float acc[NT][4];
+        float acc[NT][4], acc2[NT][4];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[nt][e] = 0.0f;
-        for (int m = 0; m < 2; ++m) {
-            const float* dM = m == 0 ? s.dB : s.dA;
-            const float* base = m == 0 ? s.ke : s.qe;
-            for (int I = J; I < NSUB; ++I) {
-                const float* f = s.fa.F[I][J];
+            for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.0f;
+        for (int I = J; I < NSUB; ++I) {
+            const float* f = s.fa.F[I][J];
+            float fc[NT];
 #pragma unroll
-                for (int kk = 0; kk < 2; ++kk) {
-                    const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
-                    const int c0 = J * SUB + gid, c1 = c0 + 8;
-                    const Frag4 af = frag4(dM[sw(i0, c0)], dM[sw(i0, c1)], dM[sw(i1, c0)], dM[sw(i1, c1)]);
+            for (int nt = 0; nt < NT; ++nt) fc[nt] = f[chw + nt * 8 + gid];
 #pragma unroll
-                    for (int nt = 0; nt < NT; ++nt) {
-                        const int c = chw + nt * 8 + gid;
-                        const float fc = f[c];
-                        mma3(acc[nt], af, frag2(base[pidx(i0, c)] * fc, base[pidx(i1, c)] * fc));
-                    }
+            for (int kk = 0; kk < 2; ++kk) {
+                const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
+                const int c0 = J * SUB + gid, c1 = c0 + 8;
+                const Frag4 ab = frag4(s.dB[sw(i0, c0)], s.dB[sw(i0, c1)], s.dB[sw(i1, c0)], s.dB[sw(i1, c1)]);
+                const Frag4 aa = frag4(s.dA[sw(i0, c0)], s.dA[sw(i0, c1)], s.dA[sw(i1, c0)], s.dA[sw(i1, c1)]);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const int c = chw + nt * 8 + gid;
+                    mma3(acc[nt], ab, frag2(s.ke[pidx(i0, c)] * fc[nt], s.ke[pidx(i1, c)] * fc[nt]));
+                    mma3(acc2[nt], aa, frag2(s.qe[pidx(i0, c)] * fc[nt], s.qe[pidx(i1, c)] * fc[nt]));
                 }
             }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

@@ -197,11 +197,18 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     __syncthreads();
     // k^, v and dU are no longer read: the next tile's rows stream in
     if (cn.L > 0) stage_tile(nxt, cn, s.vb[par ^ 1]);
-    // dbeta from T = X diag(beta); M = dT T^T into the dW buffer
-    if (tid < C) {
+    // dbeta from T = X diag(beta), sum_{i >= j} dT_ij X_ij: eight threads per column j
+    // (rows i = p mod 8), combined by shuffles in a fixed order; M = dT T^T into the dW buffer
+    {
+        const int j = tid >> 3, p = tid & 7;
         float acc = 0.0f;
-        for (int i = tid; i < C; ++i) acc += s.dT[i * PC + tid] * s.X[i * PC + tid];
-        s.dbeta[tid] = acc;
+#pragma unroll
+        for (int i = p; i < C; i += 8)
+            if (i >= j) acc += s.dT[i * PC + j] * s.X[i * PC + j];
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (p == 0) s.dbeta[j] = acc;
     }
     float* M = s.dW;
     {
@@ -260,10 +267,16 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
         const int r = idx >> 6, c = idx & 63;
         gdB[idx] = s.beta[r] * s.dT[r * PC + c];
     }
-    if (tid < C) {
-        float acc = s.dbeta[tid];
-        for (int j = 0; j < tid; ++j) acc += s.dT[tid * PC + j] * s.B[tid * PC + j];
-        reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] = acc;
+    {   // dbeta_i += sum_{j < i} dA_ij B_ij: eight threads per row i, as above
+        const int i = tid >> 3, p = tid & 7;
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = p; j < C; j += 8)
+            if (j < i) acc += s.dT[i * PC + j] * s.B[i * PC + j];
+        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        if (p == 0) reinterpret_cast<float*>(wy + WyOff::DBETA)[i] = s.dbeta[i] + acc;
     }
     if (cn.L <= 0) break;
     tile_i = nxt;
