@@ -134,9 +134,9 @@ __global__ void __launch_bounds__(256, 1)
             *reinterpret_cast<float4*>(s.DOT + panel_off(v, 32 * half + ii, D)) =
                 make_float4(bf2f(col[0]), bf2f(col[D]), bf2f(col[2 * D]), bf2f(col[3 * D]));
         }
-        // dS_L: TMEM -> tf32 copy in TMEM (the MMA operand), and dS_L^T [k][v] to the
-        // workspace checkpoint; dS_L diag(exp(G_L)) back to TMEM
-        // (both 32-column halves in flight at once: one wait for the loads, one for the stores)
+        // dS_L: TMEM -> tf32 copy in TMEM (the MMA operand); dS_L diag(exp(G_L)) back to TMEM
+        // (both 32-column halves in flight at once: one wait for the loads, one for the stores).
+        // The checkpoint dS_L^T [k][v] is written from the tf32 copy once the MMAs run.
         uint8_t* gDST = ws + lay.ds + tile * kTileDD;
         {
             const int cb = 64 * half;
@@ -152,11 +152,6 @@ __global__ void __launch_bounds__(256, 1)
             }
             tmem_st32_issue(tDS + lane_base + cb, q0);
             tmem_st32_issue(tDS + lane_base + cb + 32, q1);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + j, v, D)) = q0[j];
-                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + 32 + j, v, D)) = q1[j];
-            }
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 r0[j] = __float_as_uint(__uint_as_float(r0[j]) * s.gam[cb + j]);
@@ -186,6 +181,20 @@ __global__ void __launch_bounds__(256, 1)
                     umma_tf32(tU, desc_kmajor(smem_u32(s.DOT), D, ks), desc_kmajor(smem_u32(s.AQ), C + D, ks),
                               idN192, 1);
                 umma_commit(&s.barM1);
+            }
+        }
+        // the checkpoint dS_L^T, read back from its tf32 copy while the MMAs read the same copy
+        {
+            const int cb = 64 * half;
+            uint32_t q0[32], q1[32];
+            tmem_ld32_issue(tDS + lane_base + cb, q0);
+            tmem_ld32_issue(tDS + lane_base + cb + 32, q1);
+            tmem_wait_ld(q0);
+            tmem_after_wait(q1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + j, v, D)) = q0[j];
+                *reinterpret_cast<uint32_t*>(gDST + panel_off(cb + 32 + j, v, D)) = q1[j];
             }
         }
         ok = mbar_wait(&s.barM1, par) && ok;
