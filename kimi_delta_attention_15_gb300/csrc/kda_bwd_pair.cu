@@ -6,7 +6,8 @@
 //     with dB (WY kernel) and dAqk (state-products kernel), for column block J:
 //     a = dM[:,J] Kt_J,  b = dM[:,J]^T Xt_J   (Xt_J = x^ e^{G-G_eJ}, Kt_J = k^_J e^{G_eJ-G_J})
 //     dx += e^{G-G_eJ} a,  dk_J += e^{G_eJ-G_J} b,  dG += Xt_J a,  dG_J -= Kt_J b
-//     (split-tf32 products, about fp32 accurate, and both dG terms multiply the
+//     (products about fp32 accurate: tf32 high parts plus bf16 cross terms,
+//      mma_sync.cuh; both dG terms multiply the
 //      same factors k^, E-, E+ and f_IJ, rounded to fp32 at most once apart, so the
 //      pairs inside [t, L) cancel in the reverse cumulative sum to fp32 accuracy);
 //   dq^ += dQbar Gamma, dk^ += dKt Gamma + dKbar e^{G_L-G},
@@ -357,14 +358,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
             for (int kk = 0; kk < 2; ++kk) {
                 const int j0 = J * SUB + kk * 8 + tig, j1 = j0 + 4;
-                const Frag4 fb = frag4(s.dB[sw(r0, j0)], s.dB[sw(r1, j0)], s.dB[sw(r0, j1)], s.dB[sw(r1, j1)]);
-                const Frag4 fa = frag4(s.dA[sw(r0, j0)], s.dA[sw(r1, j0)], s.dA[sw(r0, j1)], s.dA[sw(r1, j1)]);
+                const Frag4x fb = frag4x(s.dB[sw(r0, j0)], s.dB[sw(r1, j0)], s.dB[sw(r0, j1)], s.dB[sw(r1, j1)]);
+                const Frag4x fa = frag4x(s.dA[sw(r0, j0)], s.dA[sw(r1, j0)], s.dA[sw(r0, j1)], s.dA[sw(r1, j1)]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int c = chw + nt * 8 + gid;
-                    const Frag2 kb = frag2(s.kp[pidx(j0, c)] * fc[nt], s.kp[pidx(j1, c)] * fc[nt]);
-                    mma3(accB[nt], fb, kb);
-                    mma3(accA[nt], fa, kb);
+                    const Frag2x kb = frag2x(s.kp[pidx(j0, c)] * fc[nt], s.kp[pidx(j1, c)] * fc[nt]);
+                    mma2x(accB[nt], fb, kb);
+                    mma2x(accA[nt], fa, kb);
                 }
             }
         }
@@ -405,13 +406,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             for (int kk = 0; kk < 2; ++kk) {
                 const int i0 = I * SUB + kk * 8 + tig, i1 = i0 + 4;
                 const int c0 = J * SUB + gid, c1 = c0 + 8;
-                const Frag4 ab = frag4(s.dB[sw(i0, c0)], s.dB[sw(i0, c1)], s.dB[sw(i1, c0)], s.dB[sw(i1, c1)]);
-                const Frag4 aa = frag4(s.dA[sw(i0, c0)], s.dA[sw(i0, c1)], s.dA[sw(i1, c0)], s.dA[sw(i1, c1)]);
+                const Frag4x ab = frag4x(s.dB[sw(i0, c0)], s.dB[sw(i0, c1)], s.dB[sw(i1, c0)], s.dB[sw(i1, c1)]);
+                const Frag4x aa = frag4x(s.dA[sw(i0, c0)], s.dA[sw(i0, c1)], s.dA[sw(i1, c0)], s.dA[sw(i1, c1)]);
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     const int c = chw + nt * 8 + gid;
-                    mma3(acc[nt], ab, frag2(s.ke[pidx(i0, c)] * fc[nt], s.ke[pidx(i1, c)] * fc[nt]));
-                    mma3(acc2[nt], aa, frag2(s.qe[pidx(i0, c)] * fc[nt], s.qe[pidx(i1, c)] * fc[nt]));
+                    mma2x(acc[nt], ab, frag2x(s.ke[pidx(i0, c)] * fc[nt], s.ke[pidx(i1, c)] * fc[nt]));
+                    mma2x(acc2[nt], aa, frag2x(s.qe[pidx(i0, c)] * fc[nt], s.qe[pidx(i1, c)] * fc[nt]));
                 }
             }
         }

@@ -8,7 +8,8 @@
 //   T = (I + A)^{-1} diag(beta) by blocked forward substitution,
 //   W = T (K^ * Gamma), U = T V,
 // and stores the images the two state scans consume (kda_internal.cuh).
-// W and U use split-tf32 operands (mma_sync.cuh): the final state and the gate
+// W and U use about fp32-accurate products (mma_sync.cuh: tf32 high parts plus bf16
+// cross terms for W, both halves of T against the exact v for U): the final state and the gate
 // gradient of the backward need them. The pairwise products of A and Aqk and the
 // off-diagonal blocks of the solve use single tf32 products (the measured output
 // errors stay well inside their tolerances).
@@ -361,12 +362,12 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
             const int ra = rb * SUB + gid, rbb = ra + 8;
             for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
                 const int j0 = ks * 8 + tig, j1 = j0 + 4;
-                const Frag4 tf = frag4(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
+                const Frag4x tf = frag4x(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
                 const float* pb = s.fa.Pb[j0 >> 4];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     const int c = ch * 32 + nt * 8 + gid;
-                    mma3(aw[nt], tf, frag2(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
+                    mma2x(aw[nt], tf, frag2x(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
                     // v is bf16 data: its fp32 bit pattern is exact in tf32
                     mma2a(au[nt], tf, (uint32_t)vv[j0 * VP + c] << 16, (uint32_t)vv[j1 * VP + c] << 16);
                 }

@@ -29,33 +29,11 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&c)[4], uint32_t a0, uint
 
 namespace kda {
 
-// Split-tf32 ("3xTF32") products: x = hi + lo exactly, hi = x with the 13 mantissa
-// bits below tf32 cleared, lo = x - hi (exact in fp32; the tensor core reads its top
-// 19 bits), and a*b ~ a_hi b_hi + a_hi b_lo + a_lo b_hi, which keeps about 20 bits of
-// the fp32 operands instead of 10. Used where the gate gradient needs more than tf32.
-struct Frag4 { uint32_t hi[4], lo[4]; };
-struct Frag2 { uint32_t hi[2], lo[2]; };
-
+// Operands split exactly by masking: x = hi + lo, hi = x with the 13 mantissa bits below
+// tf32 cleared, lo = x - hi (exact in fp32).
 __device__ __forceinline__ void split_tf32(float x, uint32_t& hi, uint32_t& lo) {
     hi = __float_as_uint(x) & 0xffffe000u;
     lo = __float_as_uint(x - __uint_as_float(hi));
-}
-__device__ __forceinline__ Frag4 frag4(float a0, float a1, float a2, float a3) {
-    Frag4 f;
-    split_tf32(a0, f.hi[0], f.lo[0]); split_tf32(a1, f.hi[1], f.lo[1]);
-    split_tf32(a2, f.hi[2], f.lo[2]); split_tf32(a3, f.hi[3], f.lo[3]);
-    return f;
-}
-__device__ __forceinline__ Frag2 frag2(float b0, float b1) {
-    Frag2 f;
-    split_tf32(b0, f.hi[0], f.lo[0]); split_tf32(b1, f.hi[1], f.lo[1]);
-    return f;
-}
-// c += a * b, both operands split
-__device__ __forceinline__ void mma3(float (&c)[4], const Frag4& a, const Frag2& b) {
-    mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b.hi[0], b.hi[1]);
-    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.lo[0], b.lo[1]);
-    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.hi[0], b.hi[1]);
 }
 // Single tf32 products, for products whose outputs stay well inside their tolerances
 // without the split (measured against the fp64 reference): the fp32 operands go in
@@ -101,10 +79,61 @@ __device__ __forceinline__ void ldsm_b2(Frag2t& b0, Frag2t& b1, const float* til
     b1 = Frag2t{{r[2], r[3]}};
 }
 
-// c += a * b, b exact in tf32 (e.g. bf16 data)
-__device__ __forceinline__ void mma2a(float (&c)[4], const Frag4& a, uint32_t b0, uint32_t b1) {
+
+}  // namespace kda
+
+#include <cuda_bf16.h>
+namespace kda {
+// About fp32-accurate products in two MMAs ("tf32 + bf16 cross terms"), where the gate
+// gradient needs more than tf32: with the masked split a = a_hi + a_lo, b = b_hi + b_lo,
+//   a b ~ a_hi b_hi            (one tf32 m16n8k8 product, exact operands)
+//       + a b_lo + a_lo b      (one bf16 m16n8k16 product: the two cross terms side by side
+//                               along k, a and b_lo in the first 8 slots, a_lo and b in the
+//                               last 8)
+// The cross terms are 2^-11 of the product, so their bf16 operands (8 bits) leave an error
+// of about 2^-20 of a b, the accuracy of the three-product "3xTF32" split (hi hi + hi lo +
+// lo hi) at two thirds of its MMAs; the measured output errors against the fp64 reference
+// are the same. The bf16 k slots are permuted so that each thread's bf16 pairs are exactly
+// the values of its tf32 fragments: slot 2t <-> k = t, slot 2t+1 <-> k = t+4 (fragment
+// layouts of mma.m16n8k16 .bf16, PTX ISA).
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+struct Frag4x { uint32_t hi[4], lo[4], bf[4]; };
+struct Frag2x { uint32_t hi[2], bf[2]; };
+__device__ __forceinline__ Frag4x frag4x(float a0, float a1, float a2, float a3) {
+    Frag4x f;
+    split_tf32(a0, f.hi[0], f.lo[0]); split_tf32(a1, f.hi[1], f.lo[1]);
+    split_tf32(a2, f.hi[2], f.lo[2]); split_tf32(a3, f.hi[3], f.lo[3]);
+    f.bf[0] = pack_bf16(a0, a2);
+    f.bf[1] = pack_bf16(a1, a3);
+    f.bf[2] = pack_bf16(__uint_as_float(f.lo[0]), __uint_as_float(f.lo[2]));
+    f.bf[3] = pack_bf16(__uint_as_float(f.lo[1]), __uint_as_float(f.lo[3]));
+    return f;
+}
+__device__ __forceinline__ Frag2x frag2x(float b0, float b1) {
+    Frag2x f;
+    uint32_t l[2];
+    split_tf32(b0, f.hi[0], l[0]); split_tf32(b1, f.hi[1], l[1]);
+    f.bf[0] = pack_bf16(__uint_as_float(l[0]), __uint_as_float(l[1]));
+    f.bf[1] = pack_bf16(b0, b1);
+    return f;
+}
+__device__ __forceinline__ void mma_bf16_16x8x16(float (&c)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+__device__ __forceinline__ void mma2x(float (&c)[4], const Frag4x& a, const Frag2x& b) {
+    mma_bf16_16x8x16(c, a.bf, b.bf);
+    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.hi[0], b.hi[1]);
+}
+// c += a * b, b exact in tf32 (e.g. bf16 data): a's high and low parts in two tf32 products
+__device__ __forceinline__ void mma2a(float (&c)[4], const Frag4x& a, uint32_t b0, uint32_t b1) {
     mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b0, b1);
     mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b0, b1);
 }
-
 }  // namespace kda
