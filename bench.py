@@ -295,7 +295,7 @@ def run_gb300(args, ws, rank, local):
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16 io, tf32 mma, fp32 accum/state", "data": "synthetic",
+            "vs_baseline": None, "dtype": "bf16 io, tf32 mma (bf16 mma for the cross terms of fp32-accurate products), fp32 accum/state", "data": "synthetic",
             "config": {"workload": w.name, "T": w.T, "H": w.H, "K": 128, "V": 128, "global_batch": 1,
                        "seq_len": w.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
                        "l2": "flushed (512 MiB write) before every timed step"},
