@@ -388,6 +388,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
                 }
             }
     }
+    float pk[NT][4];   // dKbar Kbar of this thread's elements
     // (b) column side: rows j of block J = rb, row blocks I >= J. E+ of those rows is
     // D_J / E- (it enters only dk^, no cancelling term)
     {
@@ -420,45 +421,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+        // the column-side epilogue and the elementwise Kbar terms act on the same elements
+        // (rows of block J = rb): E+ = D_J / E- once per element
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
                 const int row = J * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
+                const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
+                const float2 sf = *reinterpret_cast<const float2*>(&s.fa.Sf[J][col]);
                 const float2 db = *reinterpret_cast<const float2*>(&s.fa.Db[J][col]);
                 const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
                 const float2 kpv = *reinterpret_cast<const float2*>(s.kp + a);
-                const float dbx[2] = {db.x, db.y}, emx[2] = {emv.x, emv.y}, kpx[2] = {kpv.x, kpv.y};
+                const float dKbv[2] = {dKb2.x, dKb2.y}, sfx[2] = {sf.x, sf.y}, dbx[2] = {db.x, db.y},
+                            emx[2] = {emv.x, emv.y}, kpx[2] = {kpv.x, kpv.y};
 #pragma unroll
                 for (int e2 = 0; e2 < 2; ++e2) {
                     const int e = hh * 2 + e2;
-                    adk[nt][e] += __fdividef(dbx[e2], emx[e2]) * acc[nt][e];
+                    const float ep = __fdividef(dbx[e2], emx[e2]);
+                    adk[nt][e] += ep * acc[nt][e];
                     adg[nt][e] -= kpx[e2] * acc[nt][e];
+                    adk[nt][e] += dKbv[e2] * (ep * sfx[e2]);   // (c) elementwise terms of Kbar
+                    pk[nt][e] = dKbv[e2] * (kpx[e2] * sfx[e2]);
                 }
             }
     }
-    // (c) elementwise terms of Kbar (E+ again as D_I / E-)
-    float pk[NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int row = rb * SUB + gid + hh * 8, col = chw + nt * 8 + tig * 2, a = pidx(row, col);
-            const float2 dKb2 = *reinterpret_cast<const float2*>(gdKb + row * D + col);
-            const float2 sf = *reinterpret_cast<const float2*>(&s.fa.Sf[rb][col]);
-            const float2 db = *reinterpret_cast<const float2*>(&s.fa.Db[rb][col]);
-            const float2 emv = *reinterpret_cast<const float2*>(s.em + a);
-            const float2 kpv = *reinterpret_cast<const float2*>(s.kp + a);
-            const float dKbv[2] = {dKb2.x, dKb2.y}, sfx[2] = {sf.x, sf.y}, dbx[2] = {db.x, db.y},
-                        emx[2] = {emv.x, emv.y}, kpx[2] = {kpv.x, kpv.y};
-#pragma unroll
-            for (int e2 = 0; e2 < 2; ++e2) {
-                const int e = hh * 2 + e2;
-                const float el = __fdividef(dbx[e2], emx[e2]) * sfx[e2], kb = kpx[e2] * sfx[e2];
-                adk[nt][e] += dKbv[e2] * el;
-                pk[nt][e] = dKbv[e2] * kb;
-            }
-        }
     __syncthreads();   // all reads of qe, ke, kp, em, dB, dA done
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)

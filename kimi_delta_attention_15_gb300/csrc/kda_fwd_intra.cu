@@ -9,7 +9,8 @@
 //   W = T (K^ * Gamma), U = T V,
 // and stores the images the two state scans consume (kda_internal.cuh).
 // W and U use about fp32-accurate products (mma_sync.cuh: tf32 high parts plus bf16
-// cross terms for W, both halves of T against the exact v for U): the final state and the gate
+// cross terms for W; for U, T's high part in tf32 and its low part in bf16 against the
+// exact bf16 v, two k-steps per bf16 product): the final state and the gate
 // gradient of the backward need them. The pairwise products of A and Aqk and the
 // off-diagonal blocks of the solve use single tf32 products (the measured output
 // errors stay well inside their tolerances).
@@ -360,16 +361,31 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) { aw[nt][e] = 0.0f; au[nt][e] = 0.0f; }
             const int ra = rb * SUB + gid, rbb = ra + 8;
-            for (int ks = 0; ks < 2 * (rb + 1); ++ks) {
-                const int j0 = ks * 8 + tig, j1 = j0 + 4;
-                const Frag4x tf = frag4x(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
-                const float* pb = s.fa.Pb[j0 >> 4];
+            // k-steps in pairs (the triangle spans an even number): U's low-part products of
+            // both steps run as one bf16 m16n8k16 product (v is exact in bf16)
+            for (int kq = 0; kq < rb + 1; ++kq) {
+                Frag4x tf[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const int j0 = (2 * kq + u) * 8 + tig, j1 = j0 + 4;
+                    tf[u] = frag4x(s.T[ra * PA + j0], s.T[rbb * PA + j0], s.T[ra * PA + j1], s.T[rbb * PA + j1]);
+                }
+                const uint32_t alo[4] = {tf[0].bf[2], tf[0].bf[3], tf[1].bf[2], tf[1].bf[3]};
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
                     const int c = ch * 32 + nt * 8 + gid;
-                    mma2x(aw[nt], tf, frag2x(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
-                    // v is bf16 data: its fp32 bit pattern is exact in tf32
-                    mma2a(au[nt], tf, (uint32_t)vv[j0 * VP + c] << 16, (uint32_t)vv[j1 * VP + c] << 16);
+                    uint32_t vb2[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int j0 = (2 * kq + u) * 8 + tig, j1 = j0 + 4;
+                        const float* pb = s.fa.Pb[j0 >> 4];
+                        mma2x(aw[nt], tf[u], frag2x(s.ke[j0 * P + c] * pb[c], s.ke[j1 * P + c] * pb[c]));
+                        const uint32_t v0 = vv[j0 * VP + c], v1 = vv[j1 * VP + c];
+                        // v is bf16 data: its fp32 bit pattern is exact in tf32
+                        mma_tf32_16x8x8(au[nt], tf[u].hi[0], tf[u].hi[1], tf[u].hi[2], tf[u].hi[3], v0 << 16, v1 << 16);
+                        vb2[u] = v0 | (v1 << 16);
+                    }
+                    mma_bf16_16x8x16(au[nt], alo, vb2);
                 }
             }
             float* gU = reinterpret_cast<float*>(img + ImgOff::U);

@@ -100,7 +100,7 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&v);
 }
-struct Frag4x { uint32_t hi[4], lo[4], bf[4]; };
+struct Frag4x { uint32_t hi[4], lo[4], bf[4]; };   // bf: [a | a_lo] pairs (k = t, t + 4)
 struct Frag2x { uint32_t hi[2], bf[2]; };
 __device__ __forceinline__ Frag4x frag4x(float a0, float a1, float a2, float a3) {
     Frag4x f;
@@ -130,10 +130,5 @@ __device__ __forceinline__ void mma_bf16_16x8x16(float (&c)[4], const uint32_t (
 __device__ __forceinline__ void mma2x(float (&c)[4], const Frag4x& a, const Frag2x& b) {
     mma_bf16_16x8x16(c, a.bf, b.bf);
     mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b.hi[0], b.hi[1]);
-}
-// c += a * b, b exact in tf32 (e.g. bf16 data): a's high and low parts in two tf32 products
-__device__ __forceinline__ void mma2a(float (&c)[4], const Frag4x& a, uint32_t b0, uint32_t b1) {
-    mma_tf32_16x8x8(c, a.lo[0], a.lo[1], a.lo[2], a.lo[3], b0, b1);
-    mma_tf32_16x8x8(c, a.hi[0], a.hi[1], a.hi[2], a.hi[3], b0, b1);
 }
 }  // namespace kda
