@@ -88,29 +88,53 @@ def _peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle sampling during the timed region."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clock / throttle sampling during the timed region: sampling starts (and its
+    first sample has arrived) before the region, every sample carries nvidia-smi's timestamp,
+    and only the samples inside the region [mark_start, mark_end] count (the one nearest to it
+    when the region is shorter than the sampling period)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 50
 
     def __init__(self, index):
         self.index = index
         self.rows = []
         self.proc = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                                          "-i", str(self.index), "-lms", "200"],
+                                          "-i", str(self.index), "-lms", str(self.PERIOD_MS)],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 5.0
+            while not self.rows and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def _read(self):
         for line in self.proc.stdout:
             self.rows.append([x.strip() for x in line.split(",")])
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        for fmt in ("%Y/%m/%d %H:%M:%S.%f", "%Y-%m-%d %H:%M:%S.%f"):
+            try:
+                return datetime.datetime.strptime(stamp, fmt).timestamp()
+            except ValueError:
+                pass
+        return None
 
     def stop(self):
         if self.proc is None:
@@ -120,16 +144,26 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except Exception:
             self.proc.kill()
-        sm = [float(r[1]) for r in self.rows if len(r) > 2 and r[1].replace(".", "").isdigit()]
-        mx = [float(r[2]) for r in self.rows if len(r) > 2 and r[2].replace(".", "").isdigit()]
+        rows = [r for r in self.rows if len(r) >= 10 and r[2].replace(".", "").isdigit()]
+        inside = rows
+        if self.t0 is not None and self.t1 is not None and rows:
+            stamped = [(self._when(r[0]), r) for r in rows]
+            stamped = [(t, r) for t, r in stamped if t is not None]
+            if stamped:
+                inside = [r for t, r in stamped if self.t0 <= t <= self.t1]
+                if not inside:   # region shorter than the period: the sample nearest to it
+                    mid = 0.5 * (self.t0 + self.t1)
+                    inside = [min(stamped, key=lambda tr: abs(tr[0] - mid))[1]]
+        sm = [float(r[2]) for r in inside]
+        mx = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in self.rows:
+        for r in inside:
             for i, nme in enumerate(names):
-                if len(r) > 5 + i and r[5 + i].lower().startswith("active"):
+                if r[6 + i].lower().startswith("active"):
                     reasons.add(nme)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm), "period_ms": self.PERIOD_MS}
 
 
 def _dist():
@@ -245,27 +279,45 @@ def run_gb300(args, ws, rank, local):
         raise RuntimeError("device status after warm-up: %d" % ops.device_status(wsp))
 
     timer = ops.KernelTimer()
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    per_kernel = {k: 0.0 for k in ops.KERNEL_SLOTS}
-    clocks = ClockSampler(local)
-    if ws > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks.start()
-    for i in range(args.steps):
-        flush.zero_()                      # evict L2 between steps
-        starts[i].record(stream)
-        with timer:
-            step()
-        ends[i].record(stream)
-        ends[i].synchronize()
-        for k, v in timer.times_ms().items():
-            per_kernel[k] += v
-    torch.cuda.synchronize()
-    if ws > 1:
-        dist.barrier()
-    clk = clocks.stop()
+
+    def timed_region():
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        per_kernel = {k: 0.0 for k in ops.KERNEL_SLOTS}
+        clocks = ClockSampler(local)
+        if ws > 1:
+            dist.barrier()
+        clocks.start()
+        torch.cuda.synchronize()
+        clocks.mark_start()
+        for i in range(args.steps):
+            flush.zero_()                      # evict L2 between steps
+            starts[i].record(stream)
+            with timer:
+                step()
+            ends[i].record(stream)
+            ends[i].synchronize()
+            for k, v in timer.times_ms().items():
+                per_kernel[k] += v
+        torch.cuda.synchronize()
+        clocks.mark_end()
+        if ws > 1:
+            dist.barrier()
+        return starts, ends, per_kernel, clocks.stop()
+
+    def clocks_rejected(c):
+        """thermal or hardware slowdown, or SM clocks well below their maximum with no reason
+        reported (a clock lock left by someone else): the measurement is taken once more"""
+        if not c or c.get("sm_mhz") is None or not c.get("sm_max_mhz"):
+            return False
+        bad = {"hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown"}
+        return bool(bad & set(c["reasons"])) or (c["sm_mhz"] < 0.9 * c["sm_max_mhz"] and not c["reasons"])
+
+    starts, ends, per_kernel, clk = timed_region()
+    if ws == 1 and clocks_rejected(clk):
+        first = clk
+        starts, ends, per_kernel, clk = timed_region()
+        clk = dict(clk, remeasured_after=first)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     total_ms = reduce_max(sum(step_ms), ws, dev)
     ms_per_step = total_ms / args.steps
