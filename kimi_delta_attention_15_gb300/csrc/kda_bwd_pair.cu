@@ -461,7 +461,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     // dB and dAqk are no longer read: the next tile's rows stream in during the chains below
     if (cn.L > 0) stage_tile(nxt, cn);
 
-    // thread (row group rg, channel cc) owns rows rg + RG b of channel cc in the gate chain
+    // thread (row group rg, channel cc) owns rows 16 rg .. 16 rg + 15 of channel cc in the dg scan and gate chain
     constexpr int RG = kPairThreads / CH;   // row groups (threads per channel)
     const int cc = tid & (CH - 1), rg = tid >> 6;
     const float dtc = dt_bias[h * D + cb + cc];
