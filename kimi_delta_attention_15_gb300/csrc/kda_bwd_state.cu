@@ -13,8 +13,12 @@
 //
 // Persistent and warp-specialised. Every product contracts over the value
 // channel v, so a tile streams through shared memory as four 32-column value
-// panels in a two-stage ring:
-//   warp 0        bulk copies of the panels (and the tile's dO rows)
+// panels, in two rings: the S0^T and dS_L^T panels (two thirds of the bytes) in
+// three stages, Ut, dUt and their split parts in two; a stage stays in use from its
+// copy to the end of the MMAs that read it, so the deeper ring keeps more bytes in
+// flight:
+//   warp 0        bulk copies of the panels: lane 0 the three-stage ring, lane 1
+//                 the two-stage ring and, one tile ahead, the next tile's dO rows
 //   warps 4..7    split Ut, dUt into tf32 high + low parts, dO to fp32, and the
 //                 diagonal dgam on the CUDA cores
 //   warp 1        the MMAs of a panel into one of two TMEM accumulator sets
@@ -31,21 +35,27 @@ constexpr uint32_t kPanelDD = D * 128;   // one 32-column panel of a 128-row til
 constexpr uint32_t kPanelCD = C * 128;   // one 32-column panel of a 64-row tile (8 KB)
 constexpr int kDoPitch = 2 * D + 64;     // bytes per staged dO row (padded against bank conflicts)
 
-struct StStage {
+constexpr int kStA = 3, kStB = 2;        // stages of the two rings
+struct StageA {
     uint8_t S0T[kPanelDD];   // S0^T   [128 k][32 v]
     uint8_t DST[kPanelDD];   // dS_L^T [128 k][32 v]
+};
+struct StageB {
     uint8_t STK[kPanelDD];   // rows 0..63 dO [c][32 v] (fp32), rows 64..127 dUt high part
     uint8_t DUL[kPanelCD];   // dUt low part [64 c][32 v]
     uint8_t UH[kPanelCD];    // Ut as copied, then its high part [64 c][32 v]
     uint8_t UL[kPanelCD];    // Ut low part
 };
 struct BStateSmem {
-    StStage st[2];
+    StageA sa[kStA];
+    StageB sb[kStB];
     uint8_t dos[2][C * kDoPitch];   // dO rows of a tile as stored (bf16), by tile parity
-    uint64_t full[2], ready[2], empty[2], tfull[2], tempty[2], fin;
+    uint64_t fullA[kStA], emptyA[kStA], fullB[kStB], emptyB[kStB], ready[kStB], tfull[2], tempty[2], fin;
+    uint64_t dfull[2];              // dO rows of a tile landed, by tile parity
     uint32_t tmem;
     int abort;
 };
+static_assert(sizeof(BStateSmem) + 1024 <= 227 * 1024, "shared memory");
 }  // namespace
 
 size_t bwd_state_smem_bytes() { return sizeof(BStateSmem) + 1024; }
@@ -64,12 +74,19 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
         tmem_relinquish();
     }
     if (tid == 0) {
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s.full[i], 1);
+        for (int i = 0; i < kStA; ++i) {
+            mbar_init(&s.fullA[i], 1);
+            mbar_init(&s.emptyA[i], 1);
+        }
+        for (int i = 0; i < kStB; ++i) {
+            mbar_init(&s.fullB[i], 1);
+            mbar_init(&s.emptyB[i], 1);
             mbar_init(&s.ready[i], 128);
-            mbar_init(&s.empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
             mbar_init(&s.tempty[i], 256);
+            mbar_init(&s.dfull[i], 1);
         }
         mbar_init(&s.fin, 1);
         s.abort = 0;
@@ -83,9 +100,25 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
-            int it = 0;
+        // lane 0: the S0^T / dS_L^T ring, lane 1: the Ut / dUt ring (and the dO rows); the
+        // two lanes run the same tile sequence independently
+        if (lane < 2) {
+            const bool ring_a = lane == 0;
+            int it = 0, d_issued = 0;
             bool ok = true;
+            // dO rows of tile t_i (the n-th of this CTA) into dos[n & 1], completing dfull[n & 1]
+            auto issue_dO = [&](int t_i, int nn) {
+                if (t_i >= ntiles) return;
+                const int chunk = t_i / H, h = t_i - chunk * H;
+                const ChunkInfo cn = chunks[chunk];
+                if (cn.L <= 0) return;
+                mbar_arrive_expect_tx(&s.dfull[nn & 1], (uint32_t)cn.L * 2 * D);
+                for (int c = 0; c < cn.L; ++c)
+                    bulk_g2s(s.dos[nn & 1] + c * kDoPitch, dO + ((size_t)(cn.t0 + c) * H + h) * D, 2 * D,
+                             &s.dfull[nn & 1]);
+                ++d_issued;
+            };
+            if (!ring_a) issue_dO(blockIdx.x, 0);
             for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
                 const int chunk = tile / H, h = tile - chunk * H;
                 const ChunkInfo ci = chunks[chunk];
@@ -96,25 +129,40 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 const uint8_t* gUt = ws + lay.ut + t * kTileCK;
                 const uint8_t* gdU = ws + lay.dut + t * kTileCK;
                 for (int p = 0; p < 4; ++p, ++it) {
-                    const int sg = it & 1;
-                    if (!mbar_wait(&s.empty[sg], ((it >> 1) & 1) ^ 1) || *abort_flag) { ok = false; break; }
-                    StStage& g = s.st[sg];
-                    const uint32_t bytes = 2 * kPanelDD + 2 * kPanelCD + (p == 0 ? (uint32_t)ci.L * 2 * D : 0u);
-                    mbar_arrive_expect_tx(&s.full[sg], bytes);
-                    bulk_g2s(g.S0T, gS0 + p * kPanelDD, kPanelDD, &s.full[sg]);
-                    bulk_g2s(g.DST, gDS + p * kPanelDD, kPanelDD, &s.full[sg]);
-                    bulk_g2s(g.UH, gUt + p * kPanelCD, kPanelCD, &s.full[sg]);
-                    bulk_g2s(g.STK + kPanelCD, gdU + p * kPanelCD, kPanelCD, &s.full[sg]);
-                    if (p == 0)
-                        for (int c = 0; c < ci.L; ++c)
-                            bulk_g2s(s.dos[n & 1] + c * kDoPitch, dO + ((size_t)(ci.t0 + c) * H + h) * D, 2 * D,
-                                     &s.full[sg]);
+                    if (ring_a) {
+                        const int sa = it % kStA;
+                        if (!mbar_wait(&s.emptyA[sa], (uint32_t)(((it / kStA) & 1) ^ 1)) || *abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&s.fullA[sa], 2 * kPanelDD);
+                        bulk_g2s(s.sa[sa].S0T, gS0 + p * kPanelDD, kPanelDD, &s.fullA[sa]);
+                        bulk_g2s(s.sa[sa].DST, gDS + p * kPanelDD, kPanelDD, &s.fullA[sa]);
+                    } else {
+                        const int sb = it & 1;
+                        if (!mbar_wait(&s.emptyB[sb], (uint32_t)(((it >> 1) & 1) ^ 1)) || *abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(&s.fullB[sb], 2 * kPanelCD);
+                        bulk_g2s(s.sb[sb].UH, gUt + p * kPanelCD, kPanelCD, &s.fullB[sb]);
+                        bulk_g2s(s.sb[sb].STK + kPanelCD, gdU + p * kPanelCD, kPanelCD, &s.fullB[sb]);
+                        // the next tile's dO rows: the splitter is done with the tile before this
+                        // one once panel 2's stage was free (its previous use was panel 0 here)
+                        if (p == 2) issue_dO(tile + (int)gridDim.x, n + 1);
+                    }
                 }
                 ++n;
             }
             if (!ok) *abort_flag = 1;
             // copies still in flight (only after an abort): the last issue of each stage
-            for (int j = it - 1; j >= 0 && j >= it - 2; --j) mbar_wait(&s.full[j & 1], (j >> 1) & 1);
+            if (ring_a)
+                for (int j = it - 1; j >= 0 && j >= it - kStA; --j) mbar_wait(&s.fullA[j % kStA], (uint32_t)((j / kStA) & 1));
+            else {
+                for (int j = it - 1; j >= 0 && j >= it - kStB; --j) mbar_wait(&s.fullB[j & 1], (uint32_t)((j >> 1) & 1));
+                for (int j = d_issued - 1; j >= 0 && j >= d_issued - 2; --j)
+                    mbar_wait(&s.dfull[j & 1], (uint32_t)((j >> 1) & 1));
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -128,15 +176,17 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 const int tb = n & 1;
                 const uint32_t acc = tm + 256u * tb;
                 for (int p = 0; p < 4; ++p, ++it) {
-                    const int sg = it & 1;
-                    if (!mbar_wait(&s.ready[sg], (it >> 1) & 1) ||
+                    const int sa = it % kStA, sb = it & 1;
+                    // the splitter has seen both rings' copies of this panel land
+                    if (!mbar_wait(&s.ready[sb], (it >> 1) & 1) ||
                         (p == 0 && !mbar_wait(&s.tempty[tb], ((n >> 1) & 1) ^ 1)) || *abort_flag) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const StStage& g = s.st[sg];
-                    const uint32_t aS = smem_u32(g.S0T), aD = smem_u32(g.DST), aK = smem_u32(g.STK);
+                    const StageA& ga = s.sa[sa];
+                    const StageB& g = s.sb[sb];
+                    const uint32_t aS = smem_u32(ga.S0T), aD = smem_u32(ga.DST), aK = smem_u32(g.STK);
                     const uint32_t bDL = smem_u32(g.DUL), bUH = smem_u32(g.UH), bUL = smem_u32(g.UL);
                     // [dQbar / scale | dUt S0]^T = S0^T [dO ; dUt]^T     -> cols 0..127
                     for (int ks = 0; ks < 4; ++ks)
@@ -153,7 +203,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                         umma_tf32(acc + 192, desc_kmajor(aK, D, ks), desc_kmajor(bUH, C, ks), id64, (p | ks) != 0);
                     for (int ks = 0; ks < 4; ++ks)
                         umma_tf32(acc + 192, desc_kmajor(aK, D, ks), desc_kmajor(bUL, C, ks), id64, 1);
-                    umma_commit(&s.empty[sg]);
+                    umma_commit(&s.emptyA[sa]);
+                    umma_commit(&s.emptyB[sb]);
                     if (p == 3) umma_commit(&s.tfull[tb]);
                 }
                 ++n;
@@ -175,15 +226,21 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             const uint8_t* dos = s.dos[n & 1];
             float dg = 0.0f;
             for (int p = 0; p < 4; ++p, ++it) {
-                const int sg = it & 1;
-                if (!mbar_wait(&s.full[sg], (it >> 1) & 1) || *abort_flag) { ok = false; break; }
-                StStage& g = s.st[sg];
+                const int sa = it % kStA, sg = it & 1;
+                if (!mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) ||
+                    !mbar_wait(&s.fullB[sg], (uint32_t)((it >> 1) & 1)) ||
+                    (p == 0 && !mbar_wait(&s.dfull[n & 1], (uint32_t)((n >> 1) & 1))) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const StageA& ga = s.sa[sa];
+                StageB& g = s.sb[sg];
                 // dgam: row k of S0^T and dS_L^T
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                     const uint32_t off = t * 128u + ((j4 ^ (t & 7)) << 4);
-                    const float4 a = *reinterpret_cast<const float4*>(g.S0T + off);
-                    const float4 b = *reinterpret_cast<const float4*>(g.DST + off);
+                    const float4 a = *reinterpret_cast<const float4*>(ga.S0T + off);
+                    const float4 b = *reinterpret_cast<const float4*>(ga.DST + off);
                     dg = fmaf(a.x, b.x, dg); dg = fmaf(a.y, b.y, dg);
                     dg = fmaf(a.z, b.z, dg); dg = fmaf(a.w, b.w, dg);
                 }
