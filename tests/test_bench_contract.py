@@ -63,3 +63,33 @@ def test_gpu_arm_line():
     clk = line["clocks"]
     assert clk["sm_max_mhz"] > 0 and isinstance(clk["reasons"], list)
     assert line["decode"]["ms_per_step"] > 0
+
+
+def test_clock_samples_are_taken_inside_the_timed_region():
+    """The sampler keeps the samples whose nvidia-smi timestamp falls inside the timed region
+    (or the nearest one when none does), and reports their median clock and the reasons."""
+    import bench
+
+    class FinishedProcess:   # stands in for the nvidia-smi process at stop()
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    cs = bench.ClockSampler(0)
+    cs.proc = FinishedProcess()
+    samples = [("2026/12/03 10:00:00.000", "1200", "Not Active"),
+               ("2026/12/03 10:00:00.500", "2070", "Not Active"),
+               ("2026/12/03 10:00:00.600", "2060", "Active"),
+               ("2026/12/03 10:00:01.500", "900", "Not Active")]
+    cs.rows = [[stamp, "0", mhz, "2070", "1000.0", "0x0", "Not Active", "Not Active", "Not Active", cap]
+               for stamp, mhz, cap in samples]
+    t0 = cs._when("2026/12/03 10:00:00.400")
+    cs.t0, cs.t1 = t0, t0 + 0.3
+    out = cs.stop()
+    assert out["samples"] == 2 and out["sm_mhz"] == 2065.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"]
+    cs.t0 = cs.t1 = cs._when("2026/12/03 10:00:01.400")
+    out = cs.stop()
+    assert out["samples"] == 1 and out["sm_mhz"] == 900.0
