@@ -10,6 +10,9 @@ This module builds it with gcc on first use and exposes:
   forward(inp, ...)   -> dict(o, hT)           fp64 numpy arrays
   backward(inp, ...)  -> dict(dq, dk, dv, dg_raw, dbeta_raw, dA_log, ddt_bias, dh0)
 
+Grouped value heads: q and k may hold fewer heads than v (H_v = G H_qk); value
+head h then reads query/key head h // G, and dq, dk are summed over each group.
+
 ``inp`` holds fp64 numpy arrays (or anything ``np.asarray`` takes) in the
 packed layouts of ``kimi_delta_attention_15_gb300.inputs``. In ``core`` mode
 q and k are used as given (no L2 norm), ``g_raw`` is taken as the log-decay g
@@ -49,6 +52,7 @@ class _Args(ctypes.Structure):
         ("dO", _P), ("dhT", _P),
         ("dq", _P), ("dk", _P), ("dv", _P), ("dgx", _P), ("dbx", _P),
         ("dA_log_unit", _P), ("ddt_bias_unit", _P), ("dh0", _P),
+        ("G", ctypes.c_int64),
     ]
 
 
@@ -123,8 +127,9 @@ def _ptr(x):
 
 def _prepare(inp, mode, nthreads):
     q, k, v = _f64(inp["q"]), _f64(inp["k"]), _f64(inp["v"])
-    T, H, K = q.shape
-    V = v.shape[2]
+    T, Hk, K = q.shape
+    H, V = v.shape[1], v.shape[2]
+    assert H % Hk == 0, "value heads must be a multiple of query/key heads"
     cu = np.ascontiguousarray(np.asarray(inp["cu_seqlens"], dtype=np.int64))
     N = cu.shape[0] - 1
     keep = dict(q=q, k=k, v=v, gx=_f64(inp["g_raw"]), bx=_f64(inp["beta_raw"]), cu=cu,
@@ -134,6 +139,7 @@ def _prepare(inp, mode, nthreads):
         keep["dt_bias"] = _f64(inp["dt_bias"])
     a = _Args()
     a.N, a.H, a.K, a.V = N, H, K, V
+    a.G = H // Hk
     a.cu = cu.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
     a.scale = float(inp.get("scale", SCALE))
     a.lb = float(inp.get("lower_bound", LOWER_BOUND))
@@ -175,6 +181,14 @@ def backward(inp, mode: str = "raw", nthreads: int | None = None):
     a.dgx, a.dbx, a.dh0 = _ptr(out["dg_raw"]), _ptr(out["dbeta_raw"]), _ptr(out["dh0"])
     a.dA_log_unit, a.ddt_bias_unit = _ptr(dA_unit), _ptr(ddt_unit)
     _load().kda_oracle_backward(ctypes.byref(a))
+    G = a.G
+    if G > 1:   # dq, dk per value head -> per query/key head, summed over the group in order
+        for name in ("dq", "dk"):
+            per = out[name].reshape(T, H // G, G, K)
+            acc = per[:, :, 0, :].copy()
+            for j in range(1, G):
+                acc += per[:, :, j, :]
+            out[name] = acc
     dA = np.zeros(H)
     ddt = np.zeros((H, K))
     for n in range(N):          # fixed summation order

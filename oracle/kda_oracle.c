@@ -38,6 +38,12 @@
  * Units (sequence, head) are independent and run on POSIX threads. The
  * parameter gradients are written per unit and summed by the caller in a
  * fixed order.
+ *
+ * Grouped value heads (the FlashKDA CPU-reference proposal lists them): with
+ * G value heads per query/key head, value head h reads q, k of head h / G
+ * (q, k hold H / G heads); every other tensor is per value head. dq and dk are
+ * written per value head and summed over each group by the caller, in a fixed
+ * order. G = 1 is the plain layout.
  */
 #include <math.h>
 #include <pthread.h>
@@ -52,7 +58,7 @@ typedef struct {
     int mode;                   /* 1 raw, 0 core */
     int nthreads;
     /* forward inputs, packed over tokens */
-    const double *q, *k;        /* [T,H,K] */
+    const double *q, *k;        /* [T,H/G,K] */
     const double *v;            /* [T,H,V] */
     const double *gx;           /* raw: g_raw [T,H,K]; core: log-decay g [T,H,K] */
     const double *bx;           /* raw: beta_raw [T,H]; core: beta [T,H] */
@@ -66,13 +72,14 @@ typedef struct {
     const double *dO;           /* [T,H,V] */
     const double *dhT;          /* [N,H,V,K] or NULL (= 0) */
     /* backward outputs */
-    double *dq, *dk;            /* [T,H,K] (raw: wrt q,k; core: wrt q^,k^) */
+    double *dq, *dk;            /* [T,H,K] per value head (raw: wrt q,k; core: wrt q^,k^) */
     double *dv;                 /* [T,H,V] */
     double *dgx;                /* raw: wrt g_raw; core: wrt g. [T,H,K] */
     double *dbx;                /* raw: wrt beta_raw; core: wrt beta. [T,H] */
     double *dA_log_unit;        /* [N,H] per-unit partial (raw) */
     double *ddt_bias_unit;      /* [N,H,K] per-unit partial (raw) */
     double *dh0;                /* [N,H,V,K] or NULL */
+    int64_t G;                  /* value heads per query/key head (q, k: [T,H/G,K]); 1 = none */
 } kda_oracle_args;
 
 enum { SEG = 64 };
@@ -96,9 +103,10 @@ static double sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 /* Gate, beta and L2 norm of token t, head h (flashinfer page, contract). */
 static void prep_token(const kda_oracle_args *a, int64_t t, int64_t h, tok_t *x)
 {
-    const int64_t K = a->K, H = a->H;
-    const double *q = a->q + (t * H + h) * K;
-    const double *k = a->k + (t * H + h) * K;
+    const int64_t K = a->K, H = a->H, G = a->G > 0 ? a->G : 1;
+    const int64_t hk = MUT(11) ? h % (H / G) : h / G;   /* the query/key head of value head h */
+    const double *q = a->q + (t * (H / G) + hk) * K;
+    const double *k = a->k + (t * (H / G) + hk) * K;
     const double *gx = a->gx + (t * H + h) * K;
     const double bx = a->bx[t * H + h];
     if (a->mode == 1) {

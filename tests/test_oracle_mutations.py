@@ -20,6 +20,7 @@ MUTATIONS = {
     8: "dA_log without the exp(A_log) factor",
     9: "L2-norm chain without the projection",
     10: "residual with a wrong (transposed) state term",
+    11: "grouped value heads mapped to query/key heads round robin",
 }
 
 PIN_TESTS = [
@@ -35,6 +36,8 @@ PIN_TESTS = [
     pins.test_parameter_gradient_identities,
     pins.test_l2_norm_invariances,
     lambda: pins.test_chunk_form_equals_recurrence(16),
+    pins.test_grouped_heads_equal_repeated_query_key_heads,
+    pins.test_grouped_heads_central_differences,
 ]
 
 

@@ -322,3 +322,71 @@ def test_strong_decay_chunk_is_finite():
         assert np.all(np.isfinite(v))
     fc = chunk_model.forward(inp, 64)
     np.testing.assert_allclose(fc["o"], fo["o"], rtol=0, atol=1e-11 * np.abs(fo["o"]).max())
+
+
+def _grouped_inputs(lengths, Hk, G, seed):
+    """fp64 inputs with G value heads per query/key head (q, k: Hk heads; the rest Hk G)."""
+    inp = _rand_inputs(lengths, Hk * G, seed)
+    rng = np.random.default_rng(seed + 100)
+    T = sum(lengths)
+    inp["q"] = rng.standard_normal((T, Hk, K))
+    inp["k"] = rng.standard_normal((T, Hk, K))
+    return inp
+
+
+def test_grouped_heads_central_differences():
+    """Grouped value heads: the gradients of the shared q, k (summed over each group) and of
+    the per-value-head tensors against central differences of the forward."""
+    inp = _grouped_inputs((3, 2), Hk=2, G=2, seed=21)
+    g = oracle.backward(inp)
+    assert g["dq"].shape == inp["q"].shape and g["dv"].shape == inp["v"].shape
+    rng = np.random.default_rng(7)
+    h = 1e-6
+    for name, gname in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g_raw", "dg_raw"), ("A_log", "dA_log")):
+        x0 = inp[name]
+        d = rng.standard_normal(x0.shape)
+        plus = dict(inp); plus[name] = x0 + h * d
+        minus = dict(inp); minus[name] = x0 - h * d
+        fd = (_loss(plus) - _loss(minus)) / (2 * h)
+        an = float((g[gname] * d).sum())
+        assert abs(fd - an) <= 1e-7 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_grouped_heads_equal_repeated_query_key_heads():
+    """Value head h reading query/key head h // G is the plain layout with q, k repeated G
+    times along the head axis (numpy), and dq, dk are the group sums of that run's."""
+    Hk, G = 2, 3
+    inp = _grouped_inputs((5, 3), Hk=Hk, G=G, seed=22)
+    rep = dict(inp)
+    rep["q"] = np.repeat(inp["q"], G, axis=1)
+    rep["k"] = np.repeat(inp["k"], G, axis=1)
+    fg, fr = oracle.forward(inp), oracle.forward(rep)
+    assert np.array_equal(fg["o"], fr["o"]) and np.array_equal(fg["hT"], fr["hT"])
+    bg, br = oracle.backward(inp), oracle.backward(rep)
+    for key in ("dv", "dg_raw", "dbeta_raw", "dA_log", "ddt_bias", "dh0"):
+        assert np.array_equal(bg[key], br[key]), key
+    T = inp["q"].shape[0]
+    for key in ("dq", "dk"):
+        summed = br[key].reshape(T, Hk, G, K).sum(axis=2)
+        np.testing.assert_allclose(bg[key], summed, rtol=1e-13, atol=1e-13)
+
+
+def test_grouped_heads_identical_members_scale_the_shared_gradient():
+    """A group of G identical value heads (same v, gates, beta, parameters, states and
+    adjoints) gives G copies of the single-head outputs and G times its dq, dk."""
+    G = 4
+    one = _rand_inputs((6,), 1, seed=23)
+    grp = dict(one)
+    for name in ("v", "g_raw", "beta_raw", "do"):
+        grp[name] = np.repeat(one[name], G, axis=1)
+    for name in ("A_log", "dt_bias", "h0", "dhT"):
+        grp[name] = np.repeat(one[name], G, axis=0 if name in ("A_log", "dt_bias") else 1)
+    f1, fg = oracle.forward(one), oracle.forward(grp)
+    for j in range(G):
+        assert np.array_equal(fg["o"][:, j], f1["o"][:, 0])
+    b1, bg = oracle.backward(one), oracle.backward(grp)
+    np.testing.assert_allclose(bg["dq"], G * b1["dq"], rtol=1e-14, atol=0)
+    np.testing.assert_allclose(bg["dk"], G * b1["dk"], rtol=1e-14, atol=0)
+    for j in range(G):
+        assert np.array_equal(bg["dv"][:, j], b1["dv"][:, 0])
+        assert bg["dA_log"][j] == b1["dA_log"][0]
