@@ -21,7 +21,8 @@
  *  - bf16 tensors are passed as raw 16-bit patterns (kda_bf16).
  *  - Token tensors are contiguous [B*T, H, 128] (fixed-length batches, B rows
  *    of T tokens) or [T_total, H, 128] with B = 1 when packed. beta_raw and
- *    dbeta_raw are [B*T, H].
+ *    dbeta_raw are [B*T, H]. With grouped value heads (kda_shape.groups = G),
+ *    q, k, dq, dk are [B*T, H/G, 128] and every other token tensor has H heads.
  *  - A_log, dA_log: [H] fp32. dt_bias, ddt_bias: [H, 128] fp32 (one bias per
  *    key channel of the gate).
  *  - States h0, hT, dhT, dh0: [N, H, V, K] fp32, value-first.
@@ -77,6 +78,12 @@ typedef struct {
     int32_t V;           /* value dimension, must be 128 */
     float scale;         /* output scale, finite and > 0 (the pages fix 1/sqrt(128)) */
     float lower_bound;   /* gate lower bound lb, in [-5, 0) (FLA chunk_kda lower_bound) */
+    int32_t groups;      /* grouped value heads (the FlashKDA CPU-reference proposal): value
+                            heads per query/key head, G >= 1 dividing H (0 is read as 1).
+                            H counts value heads; q, k, dq, dk hold H / G heads and value
+                            head h reads query/key head h / G; dq, dk are the sums over
+                            each group (fixed order). Every other tensor is per value head. */
+    int32_t reserved;    /* must be 0 */
 } kda_shape;
 
 /* Bytes of workspace kda_fwd and kda_bwd need for this shape (the same buffer
@@ -96,7 +103,7 @@ kda_status kda_fwd(const kda_shape* shape,
 
 /* Backward of the kda_fwd call that filled `workspace`, with the same inputs.
  * do_ is the output adjoint [B*T, H, 128] bf16; dhT the final-state adjoint
- * (NULL = 0). Writes dq, dk, dv, dg_raw [B*T, H, 128] bf16, dbeta_raw
+ * (NULL = 0). Writes dq, dk [B*T, H/G, 128], dv, dg_raw [B*T, H, 128] bf16, dbeta_raw
  * [B*T, H] bf16, dA_log [H] fp32, ddt_bias [H, 128] fp32 (written, not
  * accumulated) and, if dh0 != NULL, dh0 [N, H, 128, 128] fp32. The parameter
  * gradients are summed over all tokens of all sequences in a fixed order

@@ -13,18 +13,14 @@ size_t bwd_state_smem_bytes();
 size_t bwd_wy_smem_bytes();
 size_t bwd_pair_smem_bytes();
 
-__global__ void kda_fwd_intra_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
-                                     const uint16_t*, const float*, const float*, int, float, float, uint8_t*,
-                                     Layout);
+FwdIntraKernel fwd_intra_kernel(bool grouped);
 __global__ void kda_fwd_scan_kernel(const float*, uint16_t*, float*, int, float, uint8_t*, Layout);
 __global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, uint8_t*, Layout);
 __global__ void kda_bwd_state_kernel(const uint16_t*, int, float, uint8_t*, Layout);
-__global__ void kda_bwd_wy_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*, const float*,
-                                  const float*, int, float, uint16_t*, uint8_t*, Layout);
-__global__ void kda_bwd_pair_kernel(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
-                                    const float*, const float*, int, float, uint16_t*, uint16_t*, uint16_t*,
-                                    uint16_t*, uint8_t*, Layout);
+BwdWyKernel bwd_wy_kernel(bool grouped);
+BwdPairKernel bwd_pair_kernel(bool grouped);
 __global__ void kda_param_reduce_kernel(int, float*, float*, uint8_t*, Layout);
+__global__ void kda_qk_group_reduce_kernel(uint16_t*, uint16_t*, uint8_t*, int64_t, Layout);
 
 // Chunk table from the offsets: validates cu_seqlens (cu[0] = 0, non-decreasing,
 // cu[N] = T_total), lists the chunks of every sequence in order (a chunk never
@@ -140,10 +136,16 @@ kda_status check_shape(const kda_shape* sh, bool packed) {
         if (sh->N != sh->B || sh->B > 65535) return KDA_ERR_SHAPE;
     }
     if (sh->B * sh->T * sh->H >= (int64_t(1) << 31)) return KDA_ERR_SHAPE;
+    if (sh->groups < 0 || sh->reserved != 0) return KDA_ERR_SHAPE;
+    if (sh->groups > 1 && sh->H % sh->groups != 0) return KDA_ERR_SHAPE;
     return KDA_OK;
 }
 
-Layout layout_of(const kda_shape* sh, bool packed) { return make_layout(sh->B, sh->T, sh->H, sh->N, packed); }
+int64_t groups_of(const kda_shape* sh) { return sh->groups > 1 ? sh->groups : 1; }
+
+Layout layout_of(const kda_shape* sh, bool packed) {
+    return make_layout(sh->B, sh->T, sh->H, sh->N, packed, groups_of(sh));
+}
 
 // Grid of a persistent per-tile kernel: one CTA (or one two-CTA cluster) per SM,
 // never more than tiles.
@@ -178,8 +180,8 @@ extern "C" size_t kda_workspace_size(const kda_shape* shape) {
     // the same shape may be used with or without offsets; cover both layouts
     const bool ok_p = check_shape(shape, true) == KDA_OK, ok_f = check_shape(shape, false) == KDA_OK;
     if (!ok_p && !ok_f) return 0;
-    const size_t a = ok_p ? make_layout(shape->B, shape->T, shape->H, shape->N, true).total : 0;
-    const size_t b = ok_f ? make_layout(shape->B, shape->T, shape->H, shape->N, false).total : 0;
+    const size_t a = ok_p ? layout_of(shape, true).total : 0;
+    const size_t b = ok_f ? layout_of(shape, false).total : 0;
     return a > b ? a : b;
 }
 
@@ -199,7 +201,8 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     const int H = (int)shape->H;
     const int64_t T_total = shape->B * shape->T;
-    if ((st = set_smem(kda_fwd_intra_kernel, fwd_intra_smem_bytes())) != KDA_OK) return st;
+    const FwdIntraKernel intra = fwd_intra_kernel(lay.G > 1);
+    if ((st = set_smem(intra, fwd_intra_smem_bytes())) != KDA_OK) return st;
     if ((st = set_smem(kda_fwd_scan_kernel, fwd_scan_smem_bytes())) != KDA_OK) return st;
 
     prof(0, s);
@@ -207,7 +210,7 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
-        kda_fwd_intra_kernel<<<persistent_grid(lay.nc_max * H), 512, fwd_intra_smem_bytes(), s>>>(
+        intra<<<persistent_grid(lay.nc_max * H), 512, fwd_intra_smem_bytes(), s>>>(
             q, k, v, g_raw, beta_raw, A_log, dt_bias, H, shape->lower_bound, shape->scale, ws, lay);
     prof(2, s);
     if (shape->N > 0)
@@ -240,10 +243,12 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     const float lb = shape->lower_bound, scale = shape->scale;
     if ((st = set_smem(kda_bwd_scan_kernel, bwd_scan_smem_bytes())) != KDA_OK) return st;
     if ((st = set_smem(kda_bwd_state_kernel, bwd_state_smem_bytes())) != KDA_OK) return st;
-    if ((st = set_smem(kda_bwd_wy_kernel, bwd_wy_smem_bytes())) != KDA_OK) return st;
-    if ((st = set_smem(kda_bwd_pair_kernel, bwd_pair_smem_bytes())) != KDA_OK) return st;
+    const BwdWyKernel wy = bwd_wy_kernel(lay.G > 1);
+    const BwdPairKernel pair = bwd_pair_kernel(lay.G > 1);
+    if ((st = set_smem(wy, bwd_wy_smem_bytes())) != KDA_OK) return st;
+    if ((st = set_smem(pair, bwd_pair_smem_bytes())) != KDA_OK) return st;
     // clusters of two CTAs, two CTAs per SM: all of the unified L1 as shared memory
-    if ((st = cuda_status(cudaFuncSetAttribute(kda_bwd_pair_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+    if ((st = cuda_status(cudaFuncSetAttribute(pair, cudaFuncAttributePreferredSharedMemoryCarveout,
                                                (int)cudaSharedmemCarveoutMaxShared),
                           "cudaFuncSetAttribute")) != KDA_OK)
         return st;
@@ -258,12 +263,17 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
                                                                                                   lay);
     prof(6, s);
     if (lay.nc_max > 0)
-        kda_bwd_wy_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,
+        wy<<<persistent_grid(lay.nc_max * H), 512, bwd_wy_smem_bytes(), s>>>(k, v, g_raw, beta_raw, A_log, dt_bias, H, lb, dv,
                                                                    ws, lay);
     prof(7, s);
     if (lay.nc_max > 0)
-        kda_bwd_pair_kernel<<<2 * persistent_grid(lay.nc_max * H), 256, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
+        pair<<<2 * persistent_grid(lay.nc_max * H), 256, bwd_pair_smem_bytes(), s>>>(q, k, g_raw, beta_raw, A_log, dt_bias, H, lb,
                                                                        dq, dk, dg_raw, dbeta_raw, ws, lay);
+    const int64_t tokens = shape->B * shape->T;
+    if (lay.G > 1 && tokens > 0) {   // grouped value heads: dq, dk summed over each group
+        const int64_t rows = tokens * (lay.H / lay.G);   // (token, query/key head) rows of 128 channels
+        kda_qk_group_reduce_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(dq, dk, ws, tokens, lay);
+    }
     prof(8, s);
     kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);
     prof(9, s);

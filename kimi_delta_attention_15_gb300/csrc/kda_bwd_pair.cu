@@ -101,6 +101,10 @@ __device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 
 
 size_t bwd_pair_smem_bytes() { return sizeof(PairSmem); }
 
+// kGrouped: q, k, dq, dk hold H / G heads (grouped value heads) and the kernel writes each
+// value head's fp32 share of dq, dk to the workspace; the plain layout is its own
+// instantiation, writing bf16 dq, dk directly.
+template <bool kGrouped>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     kda_bwd_pair_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                         const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
@@ -129,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
     const int ntiles = (int)lay.nc_max * H;
     const int step = (int)(gridDim.x >> 1);
+    const int G = kGrouped ? (int)lay.G : 1, Hqk = H / G;   // q, k, dq, dk have Hqk heads
     // empty chunk records only follow the last real chunk: the first one ends the work
     int tile_i = (int)(blockIdx.x >> 1);
     ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
@@ -142,12 +147,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     uint16_t braw_next = 0;
     // this CTA's channels of the raw rows of tile t_i (record cn); rows past the chunk read as zero
     auto stage_tile = [&](int t_i, const ChunkInfo& cn) {
-        const int hn = t_i % H;
+        const int hn = t_i % H, hq = hn / G;   // value head, its query/key head
         for (int seg = tid; seg < 3 * C * (CH / 8); seg += kPairThreads) {
             const int which = seg >> 9, rem = seg & 511, r = rem >> 3, c8 = (rem & 7) * 8;
             const uint16_t* src = which == 0 ? q : which == 1 ? k : g_raw;
             const bool valid = r < cn.L;
-            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + cb + c8;
+            // q, k belong to query/key head hq (grouped value heads), g_raw to value head hn
+            const int hs = which < 2 ? hq : hn, Hs = which < 2 ? Hqk : H;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * Hs + hs) * D + cb + c8;
             uint16_t* dst = (which == 0 ? stq : which == 1 ? stk : stg) + r * CH + c8;
             cp_async16_zfill(dst, src, valid);
         }
@@ -474,7 +481,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             const int r = 16 * b + 2 * warp + hl;
             xq[b] = xk[b] = make_uint2(0u, 0u);
             if (r < L) {
-                const size_t base = ((size_t)(t0 + r) * H + h) * D + cb + c4;
+                const size_t base = ((size_t)(t0 + r) * Hqk + h / G) * D + cb + c4;
                 xq[b] = *reinterpret_cast<const uint2*>(q + base);
                 xk[b] = *reinterpret_cast<const uint2*>(k + base);
             }
@@ -510,7 +517,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
         for (int b = 0; b < RB; ++b) {
             const int r = 16 * b + 2 * warp + hl;
             if (r < L) {
-                const size_t base = ((size_t)(t0 + r) * H + h) * D + cb + c4;
 #pragma unroll
                 for (int which = 0; which < 2; ++which) {
                     float xv[4];
@@ -519,11 +525,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
                     const float dot = s.xd[0][which][r] + s.xd[1][which][r];
                     const float4 g = *reinterpret_cast<const float4*>((which == 0 ? s.qe : s.ke) + pidx(r, c4));
                     const float gv[4] = {g.x, g.y, g.z, g.w};
-                    uint16_t o[4];
+                    float dx[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) o[e] = f2bf((gv[e] - (xv[e] * inv) * dot) * inv);
-                    *reinterpret_cast<uint2*>((which == 0 ? dq : dk) + base) =
-                        make_uint2((uint32_t)o[0] | ((uint32_t)o[1] << 16), (uint32_t)o[2] | ((uint32_t)o[3] << 16));
+                    for (int e = 0; e < 4; ++e) dx[e] = (gv[e] - (xv[e] * inv) * dot) * inv;
+                    if (!kGrouped) {
+                        const size_t base = ((size_t)(t0 + r) * H + h) * D + cb + c4;
+                        *reinterpret_cast<uint2*>((which == 0 ? dq : dk) + base) =
+                            make_uint2((uint32_t)f2bf(dx[0]) | ((uint32_t)f2bf(dx[1]) << 16),
+                                       (uint32_t)f2bf(dx[2]) | ((uint32_t)f2bf(dx[3]) << 16));
+                    } else {   // this value head's share of dq, dk; summed per group afterwards
+                        float* share = reinterpret_cast<float*>(ws + qk_share_offset(lay));
+                        share += (((size_t)(t0 + r) * H + h) * 2 + which) * D + cb + c4;
+                        *reinterpret_cast<float4*>(share) = make_float4(dx[0], dx[1], dx[2], dx[3]);
+                    }
                 }
             }
         }
@@ -613,6 +627,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     ci = cn;
     alog = alog_next;
     braw = braw_next;
+    }
+}
+
+
+// The instantiation for the plain or the grouped head layout (template kernels are not
+// visible outside this file).
+BwdPairKernel bwd_pair_kernel(bool grouped) {
+    return grouped ? kda_bwd_pair_kernel<true> : kda_bwd_pair_kernel<false>;
+}
+
+// Grouped value heads: dq, dk of query/key head g at a token = the sum of the shares of its
+// value heads g G .. g G + G - 1 (fp32, in that order), rounded once to bf16. The shares
+// are [tokens][H][2][128] (dq, dk); each thread takes 4 channels of one (token,
+// query/key head) row, 8 rows per CTA.
+__global__ void __launch_bounds__(256)
+    kda_qk_group_reduce_kernel(uint16_t* __restrict__ dq, uint16_t* __restrict__ dk, uint8_t* __restrict__ ws,
+                               int64_t tokens, Layout lay) {
+    if (read_status(ws) != 0) return;
+    const int G = (int)lay.G, H = (int)lay.H, Hqk = H / G;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= tokens * Hqk) return;
+    const int64_t t = row / Hqk;
+    const int g = (int)(row - t * Hqk), c4 = 4 * (threadIdx.x & 31);
+    const float* share = reinterpret_cast<const float*>(ws + qk_share_offset(lay));
+#pragma unroll
+    for (int which = 0; which < 2; ++which) {
+        const float* src = share + (((size_t)t * H + (size_t)g * G) * 2 + which) * D + c4;
+        float4 a = *reinterpret_cast<const float4*>(src);
+        for (int j = 1; j < G; ++j) {
+            const float4 b = *reinterpret_cast<const float4*>(src + (size_t)j * 2 * D);
+            a.x += b.x; a.y += b.y; a.z += b.z; a.w += b.w;
+        }
+        uint16_t* dst = (which == 0 ? dq : dk) + ((size_t)t * Hqk + g) * D + c4;
+        *reinterpret_cast<uint2*>(dst) = make_uint2((uint32_t)f2bf(a.x) | ((uint32_t)f2bf(a.y) << 16),
+                                                    (uint32_t)f2bf(a.z) | ((uint32_t)f2bf(a.w) << 16));
     }
 }
 

@@ -45,6 +45,9 @@ size_t bwd_wy_smem_bytes() { return sizeof(WySmem); }
 
 constexpr int kWyWarps = 16;
 
+// kGrouped: k holds H / G heads (grouped value heads); the plain layout is its own
+// instantiation so that it carries no head-group arithmetic.
+template <bool kGrouped>
 __global__ void __launch_bounds__(kWyWarps * 32, 1)
     kda_bwd_wy_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                       const uint16_t* __restrict__ g_raw, const uint16_t* __restrict__ beta_raw,
@@ -60,6 +63,7 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     // Persistent over tiles (tile = chunk * H + h). Empty chunk records only
     // follow the last real chunk, so the first empty tile ends the CTA's work.
     const int step = (int)gridDim.x;
+    const int G = kGrouped ? (int)lay.G : 1, Hqk = H / G;   // k has Hqk heads
     int tile_i = blockIdx.x;
     ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
     if (ci.L <= 0) return;
@@ -68,12 +72,14 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     uint16_t braw_next = 0;
     // raw rows of tile t_i (record cn) -> staging and vdst; rows past the chunk read as zero
     auto stage_tile = [&](int t_i, const ChunkInfo& cn, uint16_t* vdst) {
-        const int hn = t_i % H;
+        const int hn = t_i % H, hq = hn / G;   // value head, its query/key head
         for (int seg = tid; seg < 3 * C * (D / 8); seg += kWyWarps * 32) {
             const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
             const uint16_t* src = which == 0 ? k : which == 1 ? g_raw : v;
             const bool valid = r < cn.L;
-            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
+            // k belongs to query/key head hq (grouped value heads), the rest to value head hn
+            const int hs = which == 0 ? hq : hn, Hs = which == 0 ? Hqk : H;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * Hs + hs) * D + c8;
             uint16_t* dst = which < 2 ? stg + which * C * D + r * D + c8 : vdst + r * VP + c8;
             cp_async16_zfill(dst, src, valid);
         }
@@ -286,5 +292,9 @@ __global__ void __launch_bounds__(kWyWarps * 32, 1)
     braw = braw_next;
     }
 }
+
+// The instantiation for the plain or the grouped head layout (template kernels are not
+// visible outside this file).
+BwdWyKernel bwd_wy_kernel(bool grouped) { return grouped ? kda_bwd_wy_kernel<true> : kda_bwd_wy_kernel<false>; }
 
 }  // namespace kda

@@ -68,6 +68,9 @@ __device__ __forceinline__ void bar_solve() { asm volatile("bar.sync 1, 128;" ::
 
 constexpr int kIntraWarps = 16;
 
+// kGrouped: q, k hold H / G heads (grouped value heads); the plain layout is its own
+// instantiation so that it carries no head-group arithmetic.
+template <bool kGrouped>
 __global__ void __launch_bounds__(kIntraWarps * 32, 1)
     kda_fwd_intra_kernel(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k,
                          const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
@@ -85,6 +88,7 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
     // Empty chunk records only follow the last real chunk, so the first empty
     // tile ends the CTA's work.
     const int step = (int)gridDim.x;
+    const int G = kGrouped ? (int)lay.G : 1, Hqk = H / G;   // q, k have Hqk heads
     int tile_i = blockIdx.x;
     ChunkInfo ci = tile_i < ntiles ? chunks[tile_i / H] : ChunkInfo{0, 0, 0, 0};
     if (ci.L <= 0) return;
@@ -94,12 +98,14 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
     uint16_t braw_next = 0;
     // raw rows of tile t_i (record cn) -> staging and vdst; rows past the chunk read as zero
     auto stage_tile = [&](int t_i, const ChunkInfo& cn, uint16_t* vdst) {
-        const int hn = t_i % H;
+        const int hn = t_i % H, hq = hn / G;   // value head, its query/key head
         for (int seg = tid; seg < 4 * C * (D / 8); seg += kIntraWarps * 32) {
             const int which = seg >> 10, rem = seg & 1023, r = rem >> 4, c8 = (rem & 15) * 8;
             const uint16_t* src = which == 0 ? q : which == 1 ? k : which == 2 ? g_raw : v;
             const bool valid = r < cn.L;
-            src += ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8;
+            // q, k belong to query/key head hq (grouped value heads), the rest to value head hn
+            const int hs = which < 2 ? hq : hn, Hs = which < 2 ? Hqk : H;
+            src += ((size_t)(cn.t0 + (valid ? r : 0)) * Hs + hs) * D + c8;
             uint16_t* dst = which < 3 ? stg + which * C * D + r * D + c8 : vdst + r * VP + c8;
             cp_async16_zfill(dst, src, valid);
         }
@@ -409,6 +415,12 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         alog = alog_next;
         braw = braw_next;
     }
+}
+
+// The instantiation for the plain or the grouped head layout (template kernels are not
+// visible outside this file).
+FwdIntraKernel fwd_intra_kernel(bool grouped) {
+    return grouped ? kda_fwd_intra_kernel<true> : kda_fwd_intra_kernel<false>;
 }
 
 size_t fwd_intra_smem_bytes() { return sizeof(IntraSmem); }

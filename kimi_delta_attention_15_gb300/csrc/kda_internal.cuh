@@ -83,10 +83,12 @@ struct ChunkInfo {
 
 struct Layout {
     int64_t nc_max;      // chunk slots
-    int64_t H;
+    int64_t H;           // value heads
     size_t status, chunks, seq_first, seq_order;
     size_t img, s0, ut, ds, dut, bg, wy, part;
     size_t total;
+    int64_t G;           // value heads per query/key head
+    // (kept at 14 fields: kernels that take the layout by value spill registers once it grows)
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -95,10 +97,12 @@ __host__ __device__ inline int64_t chunk_slots(int64_t B, int64_t T, int64_t N, 
     return packed ? (B * T) / C + N + 1 : B * ((T + C - 1) / C);
 }
 
-__host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, int64_t N, bool packed) {
+__host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
+                                              int64_t G = 1) {
     Layout l;
     l.nc_max = chunk_slots(B, T, N, packed);
     l.H = H;
+    l.G = G;
     const int64_t tiles = l.nc_max * H;
     size_t o = 0;
     l.status = o;      o = align_up(o + 256, 1024);
@@ -113,9 +117,27 @@ __host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, i
     l.bg = o;          o += (size_t)tiles * BgOff::BYTES;
     l.wy = o;          o += (size_t)tiles * WyOff::BYTES;
     l.part = o;        o = align_up(o + (size_t)tiles * (D + 4) * 4, 1024);
+    // G > 1: every value head's fp32 share of dq and dk, [B T][H][2][128], summed per group
+    o = align_up(o + (G > 1 ? (size_t)(B * T) * H * 2 * D * 4 : 0), 1024);
     l.total = o;
     return l;
 }
+
+// Kernels with a plain and a grouped-head instantiation, handed out by host accessors
+// in the files that define them.
+using FwdIntraKernel = void (*)(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*,
+                                const uint16_t*, const float*, const float*, int, float, float, uint8_t*, Layout);
+using BwdWyKernel = void (*)(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*, const float*,
+                             const float*, int, float, uint16_t*, uint8_t*, Layout);
+using BwdPairKernel = void (*)(const uint16_t*, const uint16_t*, const uint16_t*, const uint16_t*, const float*,
+                               const float*, int, float, uint16_t*, uint16_t*, uint16_t*, uint16_t*, uint8_t*,
+                               Layout);
+
+// Offset of the grouped-head dq, dk shares: the region right after the parameter partials.
+__host__ __device__ inline size_t qk_share_offset(const Layout& l) {
+    return align_up(l.part + (size_t)(l.nc_max * l.H) * (D + 4) * 4, 1024);
+}
+
 
 // Device status word helpers (first int32 of the workspace).
 __device__ __forceinline__ int read_status(const uint8_t* ws) {

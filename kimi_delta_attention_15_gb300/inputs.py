@@ -10,8 +10,9 @@ fixed B=1,T=4096,H=32; fixed B=1,T=8192,H=96; packed lengths
 [1300,547,2048,963,271,3063] at H=96. Extra admitted shapes (B=1,T=17,H=16;
 B=1,T=1024,H=4; eight packed sequences of 1024 at H=96) are listed too.
 
-Layouts (packed, B=1):
-  q, k, g_raw, do   [T, H, 128]  bf16
+Layouts (packed, B=1; H counts value heads, q and k hold H / groups heads):
+  q, k              [T, H / groups, 128]  bf16
+  g_raw, do         [T, H, 128]  bf16
   v                 [T, H, 128]  bf16
   beta_raw          [T, H]       bf16
   A_log             [H]          fp32   log(U[1,16])
@@ -44,6 +45,7 @@ class Workload:
     h0: bool = False        # draw h0 ~ 0.1 N(0,1)
     dhT: bool = False       # draw dhT ~ 0.1 N(0,1)
     packed: bool = False    # inputs given as packed varlen with offsets
+    groups: int = 1         # value heads per query/key head (q, k: H // groups heads)
 
     @property
     def T(self) -> int:
@@ -78,11 +80,12 @@ EXTRA_WORKLOADS = [
 HEADLINE = 3   # index of fixed_T8192_H96 in WORKLOADS
 
 
-def custom(lengths, H, g_std=1.0, h0=False, dhT=False, name=None) -> Workload:
+def custom(lengths, H, g_std=1.0, h0=False, dhT=False, name=None, groups=1) -> Workload:
     """A workload of arbitrary packed lengths (tests of edge cases)."""
     lengths = tuple(int(x) for x in lengths)
-    return Workload(name or f"custom_{'_'.join(map(str, lengths))}_H{H}", lengths, H,
-                    g_std=g_std, h0=h0, dhT=dhT, packed=len(lengths) > 1)
+    tag = f"_G{groups}" if groups > 1 else ""
+    return Workload(name or f"custom_{'_'.join(map(str, lengths))}_H{H}{tag}", lengths, H,
+                    g_std=g_std, h0=h0, dhT=dhT, packed=len(lengths) > 1, groups=groups)
 
 
 def cu_seqlens(lengths) -> torch.Tensor:
@@ -103,8 +106,9 @@ def make_inputs(w: Workload, seed: Optional[int] = None) -> dict:
     def randn(*shape):
         return torch.randn(*shape, generator=gen, dtype=torch.float32)
 
-    q = randn(T, H, D)
-    k = randn(T, H, D)
+    Hqk = H // w.groups          # grouped value heads: fewer query/key heads
+    q = randn(T, Hqk, D)
+    k = randn(T, Hqk, D)
     v = randn(T, H, D)
     g_raw = randn(T, H, D) * w.g_std
     beta_raw = randn(T, H)

@@ -37,7 +37,8 @@ class KdaError(RuntimeError):
 class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
-                ("scale", ctypes.c_float), ("lower_bound", ctypes.c_float)]
+                ("scale", ctypes.c_float), ("lower_bound", ctypes.c_float),
+                ("groups", ctypes.c_int32), ("reserved", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -95,8 +96,10 @@ def _stream_handle(stream=None):
 
 
 def make_shape(T: int, H: int, N: int, B: int = 1, scale: float = SCALE,
-               lower_bound: float = LOWER_BOUND) -> Shape:
-    return Shape(B=B, T=T, H=H, N=N, K=128, V=128, scale=scale, lower_bound=lower_bound)
+               lower_bound: float = LOWER_BOUND, groups: int = 1) -> Shape:
+    """H counts value heads; groups = value heads per query/key head."""
+    return Shape(B=B, T=T, H=H, N=N, K=128, V=128, scale=scale, lower_bound=lower_bound, groups=groups,
+                 reserved=0)
 
 
 def workspace_size(shape: Shape) -> int:
@@ -111,15 +114,18 @@ def _check(code, where):
         raise KdaError(code, where + detail)
 
 
-def _shape_of(q, cu_seqlens, B, scale, lower_bound):
+def _shape_of(q, v, cu_seqlens, B, scale, lower_bound):
+    """Shape from the token tensors: H = value heads (v); q, k may hold H / groups heads."""
+    H, Hqk = v.shape[-2], q.shape[-2]
+    if Hqk <= 0 or H % Hqk != 0:
+        raise ValueError(f"value heads ({H}) must be a multiple of query/key heads ({Hqk})")
+    G = H // Hqk
     if cu_seqlens is not None:
-        T, H = q.shape[0], q.shape[1]
-        return make_shape(T, H, cu_seqlens.numel() - 1, 1, scale, lower_bound)
+        return make_shape(q.shape[0], H, cu_seqlens.numel() - 1, 1, scale, lower_bound, G)
     if q.dim() == 4:
-        B_, T, H = q.shape[0], q.shape[1], q.shape[2]
-        return make_shape(T, H, B_, B_, scale, lower_bound)
-    T, H = q.shape[0], q.shape[1]
-    return make_shape(T // B, H, B, B, scale, lower_bound)
+        B_, T = q.shape[0], q.shape[1]
+        return make_shape(T, H, B_, B_, scale, lower_bound, G)
+    return make_shape(q.shape[0] // B, H, B, B, scale, lower_bound, G)
 
 
 def alloc_workspace(shape: Shape, device) -> torch.Tensor:
@@ -131,7 +137,7 @@ def fwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B
         hT=None, want_hT: bool = True, stream=None):
     """kda_fwd. Token tensors [T, H, 128] bf16 (or [B, T, H, 128]); returns (o, hT, workspace)."""
     lib = load()
-    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
     if o is None:
@@ -155,7 +161,7 @@ def fwd_static_scratch(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seq
     callers that cannot allocate device memory (the scratch is a fixed array
     inside the library). Returns (o, hT)."""
     lib = load()
-    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound)
     if o is None:
         o = torch.empty_like(v)
     if hT is None and want_hT:
@@ -174,7 +180,7 @@ def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seq
         grads=None, want_dh0: bool = True, stream=None):
     """kda_bwd with the workspace filled by ``fwd``. Returns a dict of gradients."""
     lib = load()
-    shape = _shape_of(q, cu_seqlens, B, scale, lower_bound)
+    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound)
     if grads is None:
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                      dg_raw=torch.empty_like(g_raw), dbeta_raw=torch.empty_like(beta_raw),

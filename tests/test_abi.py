@@ -66,6 +66,22 @@ def test_host_validation_codes(lib):
     u = ops.make_shape(64, 2, 3)                             # packed with B = 1, N = 3 needs offsets
     assert _call_fwd(lib, u) == 3
     assert lib.kda_status_string(6) == b"KDA_ERR_OFFSETS"
+    u = ops.make_shape(64, 6, 1, groups=4)
+    assert _call_fwd(lib, u) == 3                            # groups must divide H
+    u = ops.make_shape(64, 6, 1, groups=-1)
+    assert _call_fwd(lib, u) == 3
+    u = ops.make_shape(64, 2, 1); u.reserved = 1
+    assert _call_fwd(lib, u) == 3                            # reserved field must be zero
+
+
+def test_grouped_heads_workspace(lib):
+    """groups = 0 reads as 1; grouped heads add the fp32 dq, dk partials of every value head."""
+    plain = ops.workspace_size(ops.make_shape(1000, 8, 1))
+    assert ops.workspace_size(ops.make_shape(1000, 8, 1, groups=0)) == plain
+    assert ops.workspace_size(ops.make_shape(1000, 8, 1, groups=1)) == plain
+    grouped = ops.workspace_size(ops.make_shape(1000, 8, 1, groups=4))
+    assert grouped >= plain + 2 * 1000 * 8 * 128 * 4
+    assert ops.workspace_size(ops.make_shape(1000, 8, 1, groups=3)) == 0
 
 
 def test_selftest_rejects_bad_shapes(lib):
