@@ -125,15 +125,19 @@ kda_status kda_bwd(const kda_shape* shape,
  * and H heads, one token of q, k, v, g_raw [n_req, H, 128] bf16 and beta_raw
  * [n_req, H] bf16 advances the value-first state [n_req, H, 128, 128] fp32
  * IN PLACE and writes o [n_req, H, 128] bf16 (read from the updated state).
+ * groups > 1: grouped value heads as in kda_shape.groups (q, k are
+ * [n_req, H / groups, 128]; value head h reads query/key head h / groups);
+ * 0 or 1: the plain layout.
  * A_log [H] and dt_bias [H, 128] fp32 as in kda_fwd. No workspace; the caller
  * owns every buffer. The result is that of kda_fwd over sequences of one token
  * with h0 = the state before and hT = the state after.
- * Errors: n_req < 0, H <= 0 or n_req * H >= 2^31 -> KDA_ERR_SHAPE; scale not
+ * Errors: n_req < 0, H <= 0, n_req * H >= 2^31, groups < 0 or groups > 1 not
+ * dividing H -> KDA_ERR_SHAPE; scale not
  * finite and > 0, or lower_bound outside [-5, 0) -> KDA_ERR_UNSUPPORTED; a NULL
  * pointer (n_req > 0) -> KDA_ERR_NULL; a pointer not 16-byte aligned ->
  * KDA_ERR_ALIGN; a failed launch -> KDA_ERR_CUDA (text in kda_last_error()).
  * n_req = 0 does nothing. */
-kda_status kda_decode(long long n_req, long long H, float scale, float lower_bound,
+kda_status kda_decode(long long n_req, long long H, long long groups, float scale, float lower_bound,
                       const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
                       const kda_bf16* g_raw, const kda_bf16* beta_raw,
                       const float* A_log, const float* dt_bias,

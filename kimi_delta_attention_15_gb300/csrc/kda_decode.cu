@@ -30,9 +30,11 @@ __global__ void __launch_bounds__(256)
                       const uint16_t* __restrict__ v, const uint16_t* __restrict__ g_raw,
                       const uint16_t* __restrict__ beta_raw, const float* __restrict__ A_log,
                       const float* __restrict__ dt_bias, float* __restrict__ state, uint16_t* __restrict__ o,
-                      int H, float scale, float lb) {
+                      int H, int G, float scale, float lb) {
     const int64_t unit = blockIdx.x;   // n * H + h
     const int h = (int)(unit % H);
+    // q, k of query/key head h / G (grouped value heads; G = 1: the plain layout)
+    const size_t qk = ((size_t)(unit / H) * (H / G) + h / G) * D;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int c0 = 4 * lane;
     float* S = state + unit * D * D;
@@ -44,8 +46,8 @@ __global__ void __launch_bounds__(256)
         s[i] = *reinterpret_cast<const float4*>(S + (size_t)(warp * kDecRows + i) * D + c0);
 
     const size_t tok = (size_t)unit * D;
-    const uint2 qw = *reinterpret_cast<const uint2*>(q + tok + c0);
-    const uint2 kw = *reinterpret_cast<const uint2*>(k + tok + c0);
+    const uint2 qw = *reinterpret_cast<const uint2*>(q + qk + c0);
+    const uint2 kw = *reinterpret_cast<const uint2*>(k + qk + c0);
     const uint2 gw = *reinterpret_cast<const uint2*>(g_raw + tok + c0);
     const float4 dtb = *reinterpret_cast<const float4*>(dt_bias + (size_t)h * D + c0);
     const float a_h = __expf(A_log[h]);
@@ -108,11 +110,13 @@ __global__ void __launch_bounds__(256)
 
 }  // namespace kda
 
-extern "C" kda_status kda_decode(long long n_req, long long H, float scale, float lower_bound,
+extern "C" kda_status kda_decode(long long n_req, long long H, long long groups, float scale, float lower_bound,
                                  const kda_bf16* q, const kda_bf16* k, const kda_bf16* v, const kda_bf16* g_raw,
                                  const kda_bf16* beta_raw, const float* A_log, const float* dt_bias, float* state,
                                  kda_bf16* o, void* stream) {
     if (n_req < 0 || H <= 0 || H > (1 << 20) || n_req * H > (1LL << 31) - 1) return KDA_ERR_SHAPE;
+    if (groups < 0 || (groups > 1 && H % groups != 0)) return KDA_ERR_SHAPE;
+    const int G = groups > 1 ? (int)groups : 1;
     if (!(scale > 0.0f) || !(scale < 1e30f)) return KDA_ERR_UNSUPPORTED;
     if (!(lower_bound >= -5.0f && lower_bound < 0.0f)) return KDA_ERR_UNSUPPORTED;
     if (n_req == 0) return KDA_OK;
@@ -124,7 +128,7 @@ extern "C" kda_status kda_decode(long long n_req, long long H, float scale, floa
         reinterpret_cast<const uint16_t*>(q), reinterpret_cast<const uint16_t*>(k),
         reinterpret_cast<const uint16_t*>(v), reinterpret_cast<const uint16_t*>(g_raw),
         reinterpret_cast<const uint16_t*>(beta_raw), A_log, dt_bias, state, reinterpret_cast<uint16_t*>(o),
-        (int)H, scale, lower_bound);
+        (int)H, G, scale, lower_bound);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) {
         char msg[160];

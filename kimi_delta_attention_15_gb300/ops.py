@@ -78,7 +78,7 @@ def load(build_if_missing: bool = True):
         lib.kda_diag_wait_timeout.restype = ctypes.c_int
         lib.kda_diag_umma_selftest.argtypes = [ctypes.c_int] * 4 + [P, P, P, P]
         lib.kda_diag_umma_selftest.restype = ctypes.c_int
-        lib.kda_decode.argtypes = [ctypes.c_longlong, ctypes.c_longlong, ctypes.c_float, ctypes.c_float] + [P] * 10
+        lib.kda_decode.argtypes = [ctypes.c_longlong] * 3 + [ctypes.c_float, ctypes.c_float] + [P] * 10
         lib.kda_decode.restype = ctypes.c_int
         lib.kda_diag_tf32_round.argtypes = [P, P, P, ctypes.c_longlong, P]
         lib.kda_diag_tf32_round.restype = ctypes.c_int
@@ -199,13 +199,16 @@ def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seq
 
 def decode(q, k, v, g_raw, beta_raw, A_log, dt_bias, state, *, o=None, scale: float = SCALE,
            lower_bound: float = LOWER_BOUND, stream=None):
-    """kda_decode: one token per request. q, k, v, g_raw [n_req, H, 128] bf16,
-    beta_raw [n_req, H] bf16; `state` [n_req, H, 128, 128] fp32 is updated in
+    """kda_decode: one token per request. v, g_raw [n_req, H, 128] bf16,
+    beta_raw [n_req, H] bf16, q, k [n_req, H / groups, 128] bf16 (groups taken
+    from the head counts); `state` [n_req, H, 128, 128] fp32 is updated in
     place. Returns o [n_req, H, 128] bf16."""
-    n_req, H = int(q.shape[0]), int(q.shape[1])
+    n_req, H, Hqk = int(v.shape[0]), int(v.shape[1]), int(q.shape[1])
+    if Hqk <= 0 or H % Hqk != 0:
+        raise ValueError(f"value heads ({H}) must be a multiple of query/key heads ({Hqk})")
     if o is None:
         o = torch.empty_like(v)
-    code = load().kda_decode(n_req, H, scale, lower_bound, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+    code = load().kda_decode(n_req, H, H // Hqk, scale, lower_bound, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
                              _ptr(A_log), _ptr(dt_bias), _ptr(state), _ptr(o), _stream_handle(stream))
     _check(code, "kda_decode")
     return o

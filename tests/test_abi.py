@@ -91,11 +91,13 @@ def test_selftest_rejects_bad_shapes(lib):
 
 
 def test_decode_host_validation_codes(lib):
-    def call(n=2, H=3, scale=0.088, lb=-5.0, ptr=16, bad=None):
+    def call(n=2, H=3, scale=0.088, lb=-5.0, ptr=16, bad=None, groups=1):
         ps = [ctypes.c_void_p(ptr) for _ in range(9)]
         if bad is not None:
             ps[bad] = ctypes.c_void_p(ptr + 8)
-        return lib.kda_decode(n, H, scale, lb, *ps, None)
+        return lib.kda_decode(n, H, groups, scale, lb, *ps, None)
+    assert call(groups=2) == 3                # groups must divide H
+    assert call(groups=-1) == 3
     assert call(n=-1) == 3                    # negative batch
     assert call(H=0) == 3
     assert call(n=1 << 30, H=8) == 3          # more than 2^31 - 1 units

@@ -53,3 +53,23 @@ def test_decode_matches_forward_of_one_token_sequences():
     torch.cuda.synchronize()
     check("o", o_d, o_f.float().double().cpu())
     check("hT", state, hT_f.double().cpu())
+
+
+@pytest.mark.parametrize("n_req,H,G", [(37, 8, 4), (5, 6, 3)])
+def test_grouped_decode_matches_the_oracle(n_req, H, G):
+    """Grouped value heads: q, k hold H / G heads; value head h reads query/key head h // G."""
+    inp = I.make_inputs(I.custom((1,) * n_req, H, h0=True, groups=G), seed=24 + G)
+    d = to_dev(inp)
+    assert d["q"].shape[1] == H // G
+    state = d["h0"].clone()
+    o = ops.decode(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], state)
+    torch.cuda.synchronize()
+    ref = oracle.forward(inp)
+    check("o", o, ref["o"])
+    check("hT", state, ref["hT"])
+    # the same as the grouped forward over one-token sequences
+    o_f, hT_f, _ = ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"],
+                           h0=d["h0"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    check("o", o, o_f.float().double().cpu())
+    check("hT", state, hT_f.double().cpu())
