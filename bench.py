@@ -29,6 +29,12 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 FLOP_PER_TH = 421_888           # fwd 140,629 + bwd 281,259 per token*head (C = 64, d = 128)
+# secondary count, reported beside the primary one: triangular products counted as full
+# tiles, fwd 6d^2 + 10Cd + C^2/3 = 181,589 + bwd 12d^2 + 20Cd + 2C^2/3 = 363,179
+FLOP_PER_TH_DENSE_TILE = 544_768
+# algorithmic minimum of HBM bytes: fwd reads q, k, v, g_raw, beta_raw and writes o
+# (1,282 B); bwd reads the same with dO and writes dq, dk, dv, dg_raw, dbeta_raw (2,308 B)
+BYTES_PER_TH = 3_590
 METRIC = "fwd+bwd tokens·heads/s and TFLOP/s (% of bf16 TC peak) at T=8192,H=96,K=V=128"
 UNIT = "tokens*heads/s"
 L2_FLUSH_BYTES = 512 << 20
@@ -359,6 +365,8 @@ def run_gb300(args, ws, rank, local):
                        "seq_len": w.T, "parallelism": f"replicas{ws}" if ws > 1 else "single",
                        "l2": "flushed (512 MiB write) before every timed step"},
             "tflops": tflops, "pct_bf16_peak": tflops / bf16,
+            "tflops_dense_tile": tflops * FLOP_PER_TH_DENSE_TILE / FLOP_PER_TH,
+            "gbs": value * BYTES_PER_TH / 1e9, "pct_hbm_peak": value * BYTES_PER_TH / 1e9 / hbm,
             "fwd_ms": sum(v for k, v in kms.items() if k.startswith("fwd")),
             "bwd_ms": sum(v for k, v in kms.items() if k.startswith("bwd")),
             "roofline": roof, "clocks": clk, "gpu_launches": 9 * args.steps}

@@ -58,6 +58,8 @@ def test_gpu_arm_line():
     assert abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-9
     assert set(rf["kernel_ms"]) >= {"fwd_intra", "fwd_scan", "bwd_scan", "bwd_state", "bwd_wy", "bwd_pair"}
     assert line["gpu_launches"] > 0
+    assert line["tflops_dense_tile"] > line["tflops"] > 0
+    assert abs(line["gbs"] - line["value"] * 3590 / 1e9) < 1e-6 * line["gbs"] and 0 < line["pct_hbm_peak"] < 1
     assert line["e2e"]["h2d_bytes_per_step"] > 0 and line["e2e"]["d2h_bytes_per_step"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] > 0
     clk = line["clocks"]
