@@ -12,12 +12,13 @@ def run_fwd_bwd(inp, want_bwd=True):
     d = to_dev(inp)
     packed = len(inp["lengths"]) > 1
     cu = d["cu_seqlens"] if packed else None
+    lb = float(inp.get("lower_bound", ops.LOWER_BOUND))   # the oracle reads the same key
     o, hT, ws = ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"],
-                        h0=d.get("h0"), cu_seqlens=cu)
+                        h0=d.get("h0"), cu_seqlens=cu, lower_bound=lb)
     out = dict(o=o, hT=hT)
     if want_bwd:
         g = ops.bwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], d["do"], ws,
-                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"))
+                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"), lower_bound=lb)
         out.update(g)
     status = ops.device_status(ws)
     torch.cuda.synchronize()

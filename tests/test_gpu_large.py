@@ -72,3 +72,19 @@ def test_other_admitted_shapes(name, hs):
         for k in ("dA_log", "ddt_bias"):
             x = out[k] if hs is None else out[k][hs]
             check(k, x, ref[k])
+
+
+# One long chain: 1,024 chunks through each scan at the default lower bound, and a weak
+# decay (lb = -0.1, gates in (-0.1, 0): a state with a long memory) over 256 chunks, so that
+# a growth of the error along the chain of tf32 state products would show.
+@pytest.mark.parametrize("T,lb", [(65536, -5.0), (16384, -0.1)])
+def test_long_single_sequence(T, lb):
+    w = I.custom((T,), 1, h0=True, dhT=True, name=f"long_T{T}")
+    inp = I.make_inputs(w, seed=61)
+    inp["lower_bound"] = lb
+    out = run_fwd_bwd(inp)
+    assert out["status"] == 0
+    ref = dict(oracle.forward(inp))
+    ref.update(oracle.backward(inp))
+    for k in ("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "dA_log", "ddt_bias"):
+        check(k, out[k], ref[k])
