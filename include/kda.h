@@ -29,7 +29,8 @@
  *  - cu_seqlens: DEVICE pointer to N+1 int64 offsets (0 = cu[0] <= ... <=
  *    cu[N] = T_total) for packed variable-length input; NULL for B fixed
  *    sequences of T tokens (then N = B). Empty sequences are allowed.
- *  - All device pointers must be 16-byte aligned.
+ *  - All device pointers must be 16-byte aligned. When B*T = 0 (every sequence
+ *    empty) the token tensors are empty and their pointers may be NULL.
  *  - Nullable inputs (h0, dhT) mean zero. Nullable outputs (hT, dh0) are
  *    skipped.
  *  - `stream` is a cudaStream_t. Calls are asynchronous: nothing is

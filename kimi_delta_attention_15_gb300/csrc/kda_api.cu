@@ -192,7 +192,9 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     Layout lay;
     kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay);
     if (st != KDA_OK) return st;
-    if (!q || !k || !v || !g_raw || !beta_raw || !A_log || !dt_bias || !o) return KDA_ERR_NULL;
+    // with no tokens at all (every sequence empty) the token tensors are empty and may be NULL
+    const bool has_tokens = shape->B * shape->T > 0;
+    if ((has_tokens && (!q || !k || !v || !g_raw || !beta_raw || !o)) || !A_log || !dt_bias) return KDA_ERR_NULL;
     const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, o};
     for (const void* p : ptrs)
         if (!aligned16(p)) return KDA_ERR_ALIGN;
@@ -230,8 +232,10 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
     Layout lay;
     kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay);
     if (st != KDA_OK) return st;
-    if (!q || !k || !v || !g_raw || !beta_raw || !A_log || !dt_bias || !do_ || !dq || !dk || !dv || !dg_raw ||
-        !dbeta_raw || !dA_log || !ddt_bias)
+    // with no tokens at all (every sequence empty) the token tensors are empty and may be NULL
+    const bool has_tokens = shape->B * shape->T > 0;
+    if ((has_tokens && (!q || !k || !v || !g_raw || !beta_raw || !do_ || !dq || !dk || !dv || !dg_raw || !dbeta_raw)) ||
+        !A_log || !dt_bias || !dA_log || !ddt_bias)
         return KDA_ERR_NULL;
     const void* ptrs[] = {q, k, v, g_raw, beta_raw, A_log, dt_bias, do_, dq, dk, dv, dg_raw, dbeta_raw, dA_log, ddt_bias};
     for (const void* p : ptrs)

@@ -49,6 +49,20 @@ def test_fwd_bwd_packed_with_empty_and_tiny_sequences():
         np.testing.assert_array_equal(out["dh0"][n].cpu().numpy(), dhT[n])
 
 
+@pytest.mark.parametrize("lengths,G", [((0, 0, 0), 1), ((0,), 1), ((0, 0), 2)])
+def test_no_tokens_at_all(lengths, G):
+    """Every sequence empty: the token tensors are empty (NULL data pointers), the states pass
+    through unchanged (hT = h0, dh0 = dhT) and the parameter gradients are zero."""
+    inp = I.make_inputs(I.custom(lengths, 4, h0=True, dhT=True, groups=G), seed=15)
+    assert inp["q"].numel() == 0
+    out = run_fwd_bwd(inp)
+    assert out["status"] == 0
+    np.testing.assert_array_equal(out["hT"].cpu().numpy(), inp["h0"].numpy())
+    np.testing.assert_array_equal(out["dh0"].cpu().numpy(), inp["dhT"].numpy())
+    assert not out["dA_log"].any() and not out["ddt_bias"].any()
+    assert out["o"].shape == inp["v"].shape and out["dq"].shape == inp["q"].shape
+
+
 def test_fwd_bwd_many_short_packed_sequences():
     # 200 sequences of 0..70 tokens: more chunk x head tiles than SMs, so the
     # persistent kernels run several tiles each and reach the empty chunk slots
