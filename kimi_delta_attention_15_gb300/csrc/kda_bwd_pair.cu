@@ -27,6 +27,9 @@
 // arithmetic of the other. Persistent over tiles; the raw q, k, g_raw rows of the
 // cluster's next tile are staged by cp.async in the dAqk and dB tiles, which are
 // free from the write-back of the adjoints to the end of the tile.
+// Grouped value heads (G value heads per query/key head): the q, k rows come from
+// query/key head h / G, and dq, dk leave as each value head's fp32 share, summed per
+// group by kda_qk_group_reduce_kernel (end of this file).
 #include "kda_internal.cuh"
 #include "kda_prep.cuh"
 #include "mma_sync.cuh"
