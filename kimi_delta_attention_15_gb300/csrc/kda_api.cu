@@ -27,6 +27,8 @@ __global__ void kda_qk_group_reduce_kernel(uint16_t*, uint16_t*, uint8_t*, int64
 // crosses a sequence boundary), the first chunk of each sequence, and the
 // sequences ordered by decreasing chunk count (longest first, for the scans).
 // One CTA; N is small next to the token count.
+constexpr int kOrderKeys = 4096;   // distinct chunk counts the scan order tells apart
+
 __global__ void __launch_bounds__(1024)
     kda_chunk_table_kernel(const int64_t* __restrict__ cu, int64_t N, int64_t T_total, int64_t T_fixed,
                            uint8_t* __restrict__ ws, Layout lay) {
@@ -84,16 +86,40 @@ __global__ void __launch_bounds__(1024)
         }
     }
     for (int64_t i = total + tid; i < lay.nc_max; i += blockDim.x) chunks[i] = ChunkInfo{0, 0, 0, 0};
-    // longest first: rank of sequence n by (chunk count desc, index asc)
-    for (int64_t n = tid; n < N; n += blockDim.x) {
-        const int cn = first[n + 1] - first[n];
-        int rank = 0;
-        for (int64_t m = 0; m < N; ++m) {
-            const int cm = first[m + 1] - first[m];
-            rank += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
-        }
-        order[rank] = (int)n;
+    // Scan order, longest sequence first: a counting sort on the chunk count (capped at
+    // kOrderKeys - 1), linear in N. Sequences with the same key take any order among
+    // themselves: the order only schedules the scans' CTAs, every (sequence, head)
+    // result is computed alone, so the outputs do not depend on it.
+    __shared__ int slot[kOrderKeys];
+    for (int k = tid; k < kOrderKeys; k += blockDim.x) slot[k] = 0;
+    __syncthreads();
+    auto key_of = [&](int64_t n) { return min(first[n + 1] - first[n], kOrderKeys - 1); };
+    for (int64_t n = tid; n < N; n += blockDim.x) atomicAdd(&slot[key_of(n)], 1);
+    __syncthreads();
+    // slot[k] <- sequences with a larger key (exclusive prefix over descending keys):
+    // thread t sums keys 4t .. 4t+3 from the top, then a block scan over the threads
+    constexpr int kPer = kOrderKeys / 1024;
+    static_assert(kOrderKeys % 1024 == 0, "keys per thread");
+    int part[kPer], sum = 0;
+    for (int j = 0; j < kPer; ++j) {
+        part[j] = slot[kOrderKeys - 1 - (kPer * tid + j)];
+        sum += part[j];
     }
+    scan[tid] = sum;
+    __syncthreads();
+    for (int off = 1; off < 1024; off <<= 1) {
+        const int x = tid >= off ? scan[tid - off] : 0;
+        __syncthreads();
+        scan[tid] += x;
+        __syncthreads();
+    }
+    int run = scan[tid] - sum;
+    for (int j = 0; j < kPer; ++j) {
+        slot[kOrderKeys - 1 - (kPer * tid + j)] = run;
+        run += part[j];
+    }
+    __syncthreads();
+    for (int64_t n = tid; n < N; n += blockDim.x) order[atomicAdd(&slot[key_of(n)], 1)] = (int)n;
 }
 
 __global__ void kda_clear_status_kernel(uint8_t* ws) { *reinterpret_cast<int*>(ws) = 0; }

@@ -74,6 +74,16 @@ def test_fwd_bwd_many_short_packed_sequences():
     _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
 
 
+def test_thousands_of_packed_sequences():
+    # 3,000 sequences of 0..40 tokens: many share a chunk count, so the longest-first scan
+    # order (a counting sort with ties in any order) must still be a permutation
+    rng = np.random.default_rng(16)
+    lengths = tuple(int(x) for x in rng.integers(0, 41, size=3000))
+    inp = I.make_inputs(I.custom(lengths, 2, h0=True, dhT=True), seed=16)
+    out = run_fwd_bwd(inp)
+    _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
+
+
 def test_strong_decay_gate():
     inp = I.make_inputs(I.custom((256,), 2, g_std=4.0, h0=True, dhT=True), seed=12)
     inp["A_log"] = torch.full((2,), float(np.log(16.0)))
