@@ -108,3 +108,28 @@ def test_decode_host_validation_codes(lib):
     for i in range(9):
         assert call(bad=i) == 2               # each pointer must be 16-byte aligned
     assert call(n=0, ptr=0) == 0              # empty batch: nothing to do
+
+
+def test_product_path_fails_loudly_without_the_library():
+    """No CPU fallback: with the library missing and no way to build it, the binding raises
+    instead of computing (run in a fresh interpreter so the loaded library stays untouched)."""
+    import subprocess
+    import sys
+    code = r'''
+import sys, torch
+sys.path.insert(0, ROOT)
+from kimi_delta_attention_15_gb300 import build as B, ops
+B.LIB = "/nonexistent/libkda.so"
+def no_build(*a, **k):
+    raise RuntimeError("nvcc unavailable")
+B.build = no_build
+x = torch.zeros(64, 2, 128, dtype=torch.bfloat16)
+try:
+    ops.fwd(x, x, x, x, torch.zeros(64, 2, dtype=torch.bfloat16), torch.zeros(2), torch.zeros(2, 128))
+except RuntimeError as e:
+    print("raised:", e)
+    sys.exit(0)
+sys.exit(3)
+'''.replace("ROOT", repr(os.path.dirname(os.path.dirname(os.path.abspath(__file__)))))
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and "raised" in r.stdout, r.stdout + r.stderr
