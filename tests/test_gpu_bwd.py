@@ -84,6 +84,23 @@ def test_thousands_of_packed_sequences():
     _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
 
 
+def test_degenerate_rows():
+    """Zero q, k and v rows (padding tokens: q^ = k^ = 0 through the eps of the norm, whose
+    gradient is 1/sqrt(eps) times the adjoint), beta ~ 0 (beta_raw = -30) and saturated gates
+    (g_raw = +-50), at positions inside, at the start and at the end of chunks."""
+    inp = I.make_inputs(I.custom((200,), 3, h0=True, dhT=True), seed=17)
+    for r in (0, 5, 64, 130, 199):
+        inp["q"][r] = 0
+    for r in (7, 63, 65):
+        inp["k"][r] = 0
+    inp["v"][100:111] = 0
+    inp["beta_raw"][10:21] = -30.0
+    inp["g_raw"][150:155] = 50.0
+    inp["g_raw"][160:165] = -50.0
+    out = run_fwd_bwd(inp)
+    _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
+
+
 def test_strong_decay_gate():
     inp = I.make_inputs(I.custom((256,), 2, g_std=4.0, h0=True, dhT=True), seed=12)
     inp["A_log"] = torch.full((2,), float(np.log(16.0)))
