@@ -12,13 +12,14 @@ def run_fwd_bwd(inp, want_bwd=True):
     d = to_dev(inp)
     packed = len(inp["lengths"]) > 1
     cu = d["cu_seqlens"] if packed else None
-    lb = float(inp.get("lower_bound", ops.LOWER_BOUND))   # the oracle reads the same key
+    lb = float(inp.get("lower_bound", ops.LOWER_BOUND))   # the oracle reads the same keys
+    scale = float(inp.get("scale", ops.SCALE))
     o, hT, ws = ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"],
-                        h0=d.get("h0"), cu_seqlens=cu, lower_bound=lb)
+                        h0=d.get("h0"), cu_seqlens=cu, lower_bound=lb, scale=scale)
     out = dict(o=o, hT=hT)
     if want_bwd:
         g = ops.bwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], d["do"], ws,
-                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"), lower_bound=lb)
+                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"), lower_bound=lb, scale=scale)
         out.update(g)
     status = ops.device_status(ws)
     torch.cuda.synchronize()

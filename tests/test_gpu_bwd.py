@@ -101,6 +101,16 @@ def test_degenerate_rows():
     _compare(inp, out, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
 
 
+@pytest.mark.parametrize("scale,h0_mult", [(1.0, 1.0), (0.01, 1.0), (0.0883883476, 10.0)])
+def test_other_scales_and_a_large_initial_state(scale, h0_mult):
+    """Any finite positive output scale is accepted (the pages fix 1/sqrt(128)); an initial
+    state ten times the usual size."""
+    inp = I.make_inputs(I.custom((150, 40), 2, h0=True, dhT=True), seed=18)
+    inp["scale"] = scale
+    inp["h0"] = inp["h0"] * h0_mult
+    _compare(inp, run_fwd_bwd(inp), keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
+
+
 def test_strong_decay_gate():
     inp = I.make_inputs(I.custom((256,), 2, g_std=4.0, h0=True, dhT=True), seed=12)
     inp["A_log"] = torch.full((2,), float(np.log(16.0)))
