@@ -73,3 +73,17 @@ def test_grouped_decode_matches_the_oracle(n_req, H, G):
     torch.cuda.synchronize()
     check("o", o, o_f.float().double().cpu())
     check("hT", state, hT_f.double().cpu())
+
+
+def test_decode_other_lower_bound_and_scale():
+    """A weak decay (lb = -0.1) and an output scale of 1: the values the oracle reads."""
+    inp = I.make_inputs(I.custom((1,) * 40, 4, h0=True), seed=26)
+    inp["lower_bound"], inp["scale"] = -0.1, 1.0
+    d = to_dev(inp)
+    state = d["h0"].clone()
+    o = ops.decode(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], state,
+                   scale=1.0, lower_bound=-0.1)
+    torch.cuda.synchronize()
+    ref = oracle.forward(inp)
+    check("o", o, ref["o"])
+    check("hT", state, ref["hT"])

@@ -14,12 +14,16 @@ from kimi_delta_attention_15_gb300 import inputs as I, ops
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("idx", [1, 2])
-def test_capture_and_replay_matches_eager(idx):
-    w = I.WORKLOADS[idx]
+# packed [17, 33, 65] at H=4, T=4096 at H=32, and grouped value heads (a tenth kernel, the
+# group reduction of dq, dk, inside the captured step)
+WORKLOADS = [I.WORKLOADS[1], I.WORKLOADS[2], I.custom((100, 37, 64), 8, h0=True, dhT=True, groups=4)]
+
+
+@pytest.mark.parametrize("w", WORKLOADS, ids=[w.name for w in WORKLOADS])
+def test_capture_and_replay_matches_eager(w):
     d = to_dev(I.make_inputs(w))
     cu = d["cu_seqlens"] if w.packed else None
-    shape = ops.make_shape(w.T, w.H, w.N)
+    shape = ops.make_shape(w.T, w.H, w.N, groups=w.groups)
     ws = ops.alloc_workspace(shape, d["q"].device)
     o = torch.empty_like(d["v"])
     hT = torch.empty(w.N, w.H, 128, 128, dtype=torch.float32, device=o.device)
