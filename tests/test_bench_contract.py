@@ -95,3 +95,24 @@ def test_clock_samples_are_taken_inside_the_timed_region():
     cs.t0 = cs.t1 = cs._when("2026/12/03 10:00:01.400")
     out = cs.stop()
     assert out["samples"] == 1 and out["sm_mhz"] == 900.0
+
+
+@pytest.mark.timeout(300)
+def test_reference_arm_under_torchrun_two_ranks():
+    """Launched as for a 2-GPU run: rank 0 alone times the oracle and prints one line; the
+    other rank exits 0 without work."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    r = subprocess.run([sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
+                        "--master-addr", "127.0.0.1", "--master-port", str(port),
+                        os.path.join(ROOT, "bench.py"), "--impl", "reference", "--gpus", "2", "--steps", "1",
+                        "--warmup", "3", "--workload", "fixed_T17_H1"],
+                       capture_output=True, text=True, timeout=280, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
