@@ -133,3 +133,33 @@ sys.exit(3)
 '''.replace("ROOT", repr(os.path.dirname(os.path.dirname(os.path.abspath(__file__)))))
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300)
     assert r.returncode == 0 and "raised" in r.stdout, r.stdout + r.stderr
+
+
+def test_header_is_plain_c():
+    """include/kda.h compiles as C99 (the boundary is a C ABI, not only C++)."""
+    import shutil
+    import subprocess
+    import tempfile
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not available")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    src = r'''
+#include "kda.h"
+int main(void) {
+    kda_shape sh = {1, 64, 2, 1, 128, 128, 0.088f, -5.0f, 1, 0};
+    size_t (*ws)(const kda_shape*) = kda_workspace_size;
+    kda_status (*fwd)(const kda_shape*, const kda_bf16*, const kda_bf16*, const kda_bf16*, const kda_bf16*,
+                      const kda_bf16*, const float*, const float*, const float*, const int64_t*, kda_bf16*,
+                      float*, void*, size_t, void*) = kda_fwd;
+    (void)sh; (void)ws; (void)fwd; (void)kda_bwd; (void)kda_decode; (void)kda_get_device_status;
+    return KDA_OK;
+}
+'''
+    with tempfile.TemporaryDirectory() as d:
+        p = os.path.join(d, "use_kda.c")
+        with open(p, "w") as f:
+            f.write(src)
+        r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-pedantic", "-fsyntax-only",
+                            "-I", os.path.join(root, "include"), p], capture_output=True, text=True)
+        assert r.returncode == 0, r.stderr
