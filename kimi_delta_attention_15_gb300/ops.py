@@ -128,6 +128,42 @@ def _shape_of(q, v, cu_seqlens, B, scale, lower_bound):
     return make_shape(q.shape[0] // B, H, B, B, scale, lower_bound, G)
 
 
+def _validate(specs):
+    """Sizes, dtypes and layout of the tensors a call hands to the kernels, which see only
+    pointers: (name, tensor or None, element count, dtype or None, optional). Sizes are checked
+    as element counts, so [T, H, 128] and [B, T, H, 128] both pass. Every tensor must then be
+    contiguous and on one CUDA device. Raises ValueError before anything is launched."""
+    present = []
+    for name, t, numel, dtype, optional in specs:
+        if t is None:
+            if not optional:
+                raise ValueError(f"{name} is required")
+            continue
+        if dtype is not None and t.dtype != dtype:
+            raise ValueError(f"{name}: dtype {t.dtype}, expected {dtype}")
+        if numel is not None and t.numel() != numel:
+            raise ValueError(f"{name}: {t.numel()} elements {tuple(t.shape)}, expected {numel}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        present.append((name, t))
+    dev = present[0][1].device if present else None
+    for name, t in present:
+        if t.device.type != "cuda" or t.device != dev:
+            raise ValueError(f"{name}: on {t.device}; every tensor must be on one CUDA device ({dev})")
+
+
+def _token_specs(shape: Shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens):
+    """Specs of the inputs kda_fwd and kda_bwd share."""
+    tok, H, N = shape.B * shape.T, shape.H, shape.N
+    Hqk = H // max(int(shape.groups), 1)
+    bf, f32 = torch.bfloat16, torch.float32
+    return [("q", q, tok * Hqk * 128, bf, False), ("k", k, tok * Hqk * 128, bf, False),
+            ("v", v, tok * H * 128, bf, False), ("g_raw", g_raw, tok * H * 128, bf, False),
+            ("beta_raw", beta_raw, tok * H, bf, False), ("A_log", A_log, H, f32, False),
+            ("dt_bias", dt_bias, H * 128, f32, False), ("h0", h0, N * H * 128 * 128, f32, True),
+            ("cu_seqlens", cu_seqlens, N + 1, torch.int64, True)]
+
+
 def alloc_workspace(shape: Shape, device) -> torch.Tensor:
     return torch.empty(workspace_size(shape), dtype=torch.uint8, device=device)
 
@@ -144,6 +180,10 @@ def fwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B
         o = torch.empty_like(v)
     if hT is None and want_hT:
         hT = torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32, device=q.device)
+    _validate(_token_specs(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens)
+              + [("o", o, v.numel(), torch.bfloat16, False), ("hT", hT, shape.N * shape.H * 128 * 128,
+                                                             torch.float32, True),
+                 ("workspace", workspace, None, None, False)])
     code = lib.kda_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
                        _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), _ptr(o), _ptr(hT),
                        _ptr(workspace), workspace.numel(), _stream_handle(stream))
@@ -166,6 +206,9 @@ def fwd_static_scratch(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seq
         o = torch.empty_like(v)
     if hT is None and want_hT:
         hT = torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32, device=q.device)
+    _validate(_token_specs(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens)
+              + [("o", o, v.numel(), torch.bfloat16, False), ("hT", hT, shape.N * shape.H * 128 * 128,
+                                                             torch.float32, True)])
     code = lib.kda_fwd_static_scratch(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw),
                                       _ptr(beta_raw), _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens),
                                       _ptr(o), _ptr(hT), _stream_handle(stream))
@@ -187,6 +230,17 @@ def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seq
                      dA_log=torch.empty_like(A_log), ddt_bias=torch.empty_like(dt_bias),
                      dh0=(torch.empty(shape.N, shape.H, 128, 128, dtype=torch.float32,
                                       device=q.device) if want_dh0 else None))
+    bf, f32 = torch.bfloat16, torch.float32
+    _validate(_token_specs(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens)
+              + [("do", do, v.numel(), bf, False),
+                 ("dhT", dhT, shape.N * shape.H * 128 * 128, f32, True),
+                 ("dq", grads.get("dq"), q.numel(), bf, False), ("dk", grads.get("dk"), q.numel(), bf, False),
+                 ("dv", grads.get("dv"), v.numel(), bf, False), ("dg_raw", grads.get("dg_raw"), v.numel(), bf, False),
+                 ("dbeta_raw", grads.get("dbeta_raw"), beta_raw.numel(), bf, False),
+                 ("dA_log", grads.get("dA_log"), shape.H, f32, False),
+                 ("ddt_bias", grads.get("ddt_bias"), shape.H * 128, f32, False),
+                 ("dh0", grads.get("dh0"), shape.N * shape.H * 128 * 128, f32, True),
+                 ("workspace", workspace, None, None, False)])
     code = lib.kda_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
                        _ptr(A_log), _ptr(dt_bias), _ptr(h0), _ptr(cu_seqlens), _ptr(do), _ptr(dhT),
                        _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]), _ptr(grads["dg_raw"]),
@@ -208,7 +262,14 @@ def decode(q, k, v, g_raw, beta_raw, A_log, dt_bias, state, *, o=None, scale: fl
         raise ValueError(f"value heads ({H}) must be a multiple of query/key heads ({Hqk})")
     if o is None:
         o = torch.empty_like(v)
-    code = load().kda_decode(n_req, H, H // Hqk, scale, lower_bound, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
+    lib = load()
+    bf, f32 = torch.bfloat16, torch.float32
+    _validate([("q", q, n_req * Hqk * 128, bf, False), ("k", k, n_req * Hqk * 128, bf, False),
+               ("v", v, n_req * H * 128, bf, False), ("g_raw", g_raw, n_req * H * 128, bf, False),
+               ("beta_raw", beta_raw, n_req * H, bf, False), ("A_log", A_log, H, f32, False),
+               ("dt_bias", dt_bias, H * 128, f32, False), ("state", state, n_req * H * 128 * 128, f32, False),
+               ("o", o, n_req * H * 128, bf, False)])
+    code = lib.kda_decode(n_req, H, H // Hqk, scale, lower_bound, _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw), _ptr(beta_raw),
                              _ptr(A_log), _ptr(dt_bias), _ptr(state), _ptr(o), _stream_handle(stream))
     _check(code, "kda_decode")
     return o
