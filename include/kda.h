@@ -42,9 +42,18 @@
  * One workspace must not be used by two calls in flight at the same time.
  *
  * Errors: argument problems are reported synchronously as kda_status codes.
- * Problems found on the device (malformed cu_seqlens, a wait that timed out)
- * set a status word in the workspace; later kernels of the same call skip
- * their work, and kda_get_device_status() returns the word.
+ * Problems found on the device (malformed cu_seqlens, a wait that timed out,
+ * a stale workspace) set a status word in the workspace; later kernels of the
+ * same call skip their work, and kda_get_device_status() returns the word.
+ *
+ * Workspace provenance: kda_fwd stamps the workspace with a hash of its shape
+ * (B, T, H, N, groups, scale, lower_bound, chunk length, packed or fixed) and,
+ * once its last kernel has finished without error, a "forward complete" word.
+ * The first kernel of kda_bwd compares both with its own shape; on a mismatch
+ * (a workspace from another shape, from no forward at all, or from a forward
+ * that failed) it sets KDA_ERR_STALE_WORKSPACE and the backward computes
+ * nothing. Only the shape is stamped: the caller still has to pass the same
+ * input tensors to both calls.
  */
 #ifndef KDA_H_
 #define KDA_H_
@@ -67,7 +76,9 @@ typedef enum {
     KDA_ERR_WORKSPACE = 5,   /* workspace NULL or smaller than required */
     KDA_ERR_OFFSETS = 6,     /* (device) cu_seqlens not 0 .. T_total non-decreasing */
     KDA_ERR_TIMEOUT = 7,     /* (device) a bounded wait inside a kernel gave up */
-    KDA_ERR_CUDA = 8         /* a CUDA launch or attribute call failed */
+    KDA_ERR_CUDA = 8,        /* a CUDA launch or attribute call failed */
+    KDA_ERR_STALE_WORKSPACE = 9 /* (device) kda_bwd got a workspace that does not hold a
+                                   completed kda_fwd of the same shape */
 } kda_status;
 
 typedef struct {
@@ -84,7 +95,12 @@ typedef struct {
                             H counts value heads; q, k, dq, dk hold H / G heads and value
                             head h reads query/key head h / G; dq, dk are the sums over
                             each group (fixed order). Every other tensor is per value head. */
-    int32_t reserved;    /* must be 0 */
+    int32_t chunk_size;  /* chunk length the caller asks for: 0 or 64 (the default), or 32.
+                            The Kimi-K3 fused_chunk validator admits chunk lengths 32 and 64.
+                            The chunk length blocks the computation and does not change the
+                            function computed, so a request for 32 is served by the 64-token
+                            chunk kernels and gives the same results bit for bit. Any other
+                            value returns KDA_ERR_UNSUPPORTED. */
 } kda_shape;
 
 /* Bytes of workspace kda_fwd and kda_bwd need for this shape (the same buffer
@@ -145,8 +161,8 @@ kda_status kda_decode(long long n_req, long long H, long long groups, float scal
                       float* state, kda_bf16* o, void* stream);
 
 /* Synchronises `stream` and returns the device status word of `workspace`
- * (KDA_OK, KDA_ERR_OFFSETS or KDA_ERR_TIMEOUT), or KDA_ERR_CUDA if the
- * stream reported an error. Clears nothing. */
+ * (KDA_OK, KDA_ERR_OFFSETS, KDA_ERR_TIMEOUT or KDA_ERR_STALE_WORKSPACE), or
+ * KDA_ERR_CUDA if the stream reported an error. Clears nothing. */
 kda_status kda_get_device_status(const void* workspace, void* stream);
 
 /* Profiling hook. When `events` is non-NULL (an array of `count` cudaEvent_t
@@ -181,17 +197,29 @@ int kda_set_profile_events(void* const* events, int count);
  *    contents (what must start at zero is cleared by each call). Calls whose
  *    work overlaps on the GPU (other streams, other host threads) race on it:
  *    serialise them.
- *  - Shapes whose kda_workspace_size() exceeds KDA_STATIC_SCRATCH_BYTES (about
- *    100 (chunk of 64 tokens, head) tiles, e.g. T = 1024 with H = 4) return
- *    KDA_ERR_WORKSPACE, and kda_last_error() states both sizes.
+ *  - Only the forward runs, so only the workspace regions the forward writes
+ *    must fit: about 160 (chunk of 64 tokens, head) tiles, e.g. T = 2048 with
+ *    H = 4. Larger shapes return KDA_ERR_WORKSPACE, and kda_last_error()
+ *    states both sizes.
  *  - Forward only: the intermediates it keeps are not available to kda_bwd.
- * Other errors are those of kda_fwd. */
+ *  - Problems found on the device (malformed cu_seqlens, a timed-out wait) go
+ *    to the status word of the scratch array, not to a workspace of the
+ *    caller's: read them with kda_static_scratch_device_status().
+ *  - The cached address is not renewed: after cudaDeviceReset() on a device,
+ *    this entry point must not be called again on it in the same process.
+ * Host-side errors are those of kda_fwd. */
 kda_status kda_fwd_static_scratch(const kda_shape* shape,
                                   const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
                                   const kda_bf16* g_raw, const kda_bf16* beta_raw,
                                   const float* A_log, const float* dt_bias,
                                   const float* h0, const int64_t* cu_seqlens,
                                   kda_bf16* o, float* hT, void* stream);
+
+/* Synchronises `stream` and returns the device status word of the scratch array
+ * that kda_fwd_static_scratch uses on the current device (KDA_OK,
+ * KDA_ERR_OFFSETS or KDA_ERR_TIMEOUT from the last call there), or KDA_ERR_CUDA.
+ * No counterpart on the pages either. */
+kda_status kda_static_scratch_device_status(void* stream);
 
 /* Text of the last CUDA error an entry point of the calling thread turned
  * into KDA_ERR_CUDA ("" if none). Static per-thread buffer. */

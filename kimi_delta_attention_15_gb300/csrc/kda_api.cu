@@ -2,6 +2,7 @@
 // the chunk table built on the device from cu_seqlens, and kernel launches.
 #include <cmath>
 #include <cstdio>
+#include <cstring>
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -122,7 +123,27 @@ __global__ void __launch_bounds__(1024)
     for (int64_t n = tid; n < N; n += blockDim.x) order[atomicAdd(&slot[key_of(n)], 1)] = (int)n;
 }
 
-__global__ void kda_clear_status_kernel(uint8_t* ws) { *reinterpret_cast<int*>(ws) = 0; }
+// Start of a forward: clear the status word, stamp the shape hash, and mark the
+// forward as not complete yet.
+__global__ void kda_clear_status_kernel(uint8_t* ws, uint64_t shape_hash) {
+    *reinterpret_cast<int*>(ws) = 0;
+    *reinterpret_cast<uint64_t*>(ws + kStampHashOff) = shape_hash;
+    *reinterpret_cast<uint32_t*>(ws + kStampDoneOff) = 0u;
+}
+
+// End of a forward: the workspace holds a complete forward unless a kernel raised an error.
+__global__ void kda_fwd_done_kernel(uint8_t* ws) {
+    if (read_status(ws) == 0) *reinterpret_cast<volatile uint32_t*>(ws + kStampDoneOff) = kFwdDone;
+}
+
+// Start of a backward: the workspace must hold a completed forward of the same shape;
+// otherwise every later kernel of the backward finds the status word set and skips.
+__global__ void kda_bwd_check_kernel(uint8_t* ws, uint64_t shape_hash) {
+    if (read_status(ws) != 0) return;
+    const uint64_t stamp = *reinterpret_cast<const volatile uint64_t*>(ws + kStampHashOff);
+    const uint32_t done = *reinterpret_cast<const volatile uint32_t*>(ws + kStampDoneOff);
+    if (stamp != shape_hash || done != kFwdDone) raise_status(ws, KDA_ERR_STALE_WORKSPACE);
+}
 
 // Lets the other translation units of the library set the text kda_last_error returns.
 void set_last_error_text(const char* msg);
@@ -162,12 +183,33 @@ kda_status check_shape(const kda_shape* sh, bool packed) {
         if (sh->N != sh->B || sh->B > 65535) return KDA_ERR_SHAPE;
     }
     if (sh->B * sh->T * sh->H >= (int64_t(1) << 31)) return KDA_ERR_SHAPE;
-    if (sh->groups < 0 || sh->reserved != 0) return KDA_ERR_SHAPE;
+    if (sh->groups < 0) return KDA_ERR_SHAPE;
+    // chunk length: 64 (0 reads as 64) or 32, both served by the 64-token chunk kernels
+    if (sh->chunk_size != 0 && sh->chunk_size != 32 && sh->chunk_size != 64) return KDA_ERR_UNSUPPORTED;
     if (sh->groups > 1 && sh->H % sh->groups != 0) return KDA_ERR_SHAPE;
     return KDA_OK;
 }
 
 int64_t groups_of(const kda_shape* sh) { return sh->groups > 1 ? sh->groups : 1; }
+
+// FNV-1a hash of everything in the shape that decides the workspace's contents, and of
+// whether offsets are given: the provenance stamp kda_fwd leaves and kda_bwd checks.
+uint64_t shape_hash(const kda_shape* sh, bool packed) {
+    uint64_t h = 1469598103934665603ull;
+    auto mix = [&](uint64_t x) {
+        for (int i = 0; i < 8; ++i) {
+            h ^= (x >> (8 * i)) & 0xffu;
+            h *= 1099511628211ull;
+        }
+    };
+    uint32_t sb, lb;
+    memcpy(&sb, &sh->scale, 4);
+    memcpy(&lb, &sh->lower_bound, 4);
+    mix((uint64_t)sh->B); mix((uint64_t)sh->T); mix((uint64_t)sh->H); mix((uint64_t)sh->N);
+    mix((uint64_t)groups_of(sh)); mix(sb); mix(lb);
+    mix((uint64_t)(sh->chunk_size == 32 ? 32 : 64)); mix(packed ? 1u : 0u);
+    return h;
+}
 
 Layout layout_of(const kda_shape* sh, bool packed) {
     return make_layout(sh->B, sh->T, sh->H, sh->N, packed, groups_of(sh));
@@ -189,12 +231,15 @@ kda_status set_smem(K kernel, size_t bytes) {
                        "cudaFuncSetAttribute");
 }
 
-kda_status common_checks(const kda_shape* shape, const int64_t* cu, void* ws, size_t ws_bytes, Layout* lay) {
+// forward_only: the workspace need only hold the regions the forward writes (status,
+// chunk tables, intra-chunk images, S0 and Ut checkpoints: everything before `ds`).
+kda_status common_checks(const kda_shape* shape, const int64_t* cu, void* ws, size_t ws_bytes, Layout* lay,
+                         bool forward_only = false) {
     const bool packed = cu != nullptr;
     kda_status st = check_shape(shape, packed);
     if (st != KDA_OK) return st;
     *lay = layout_of(shape, packed);
-    if (!ws || ws_bytes < lay->total) return KDA_ERR_WORKSPACE;
+    if (!ws || ws_bytes < (forward_only ? lay->ds : lay->total)) return KDA_ERR_WORKSPACE;
     if (!aligned16(ws) || (packed && (reinterpret_cast<uintptr_t>(cu) & 7u))) return KDA_ERR_ALIGN;
     return KDA_OK;
 }
@@ -211,12 +256,23 @@ extern "C" size_t kda_workspace_size(const kda_shape* shape) {
     return a > b ? a : b;
 }
 
-extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
-                              const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log,
-                              const float* dt_bias, const float* h0, const int64_t* cu_seqlens, kda_bf16* o,
-                              float* hT, void* workspace, size_t workspace_bytes, void* stream) {
+namespace kda {
+
+// Bytes of the regions the forward alone writes (the forward-only workspace), 0 for an
+// invalid shape.
+size_t forward_workspace_bytes(const kda_shape* shape, bool packed) {
+    if (check_shape(shape, packed) != KDA_OK) return 0;
+    return layout_of(shape, packed).ds;
+}
+
+// kda_fwd; forward_only: accept a workspace that holds only the forward's regions
+// (the backward cannot run on it).
+kda_status fwd_entry(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                     const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log, const float* dt_bias,
+                     const float* h0, const int64_t* cu_seqlens, kda_bf16* o, float* hT, void* workspace,
+                     size_t workspace_bytes, void* stream, bool forward_only) {
     Layout lay;
-    kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay);
+    kda_status st = common_checks(shape, cu_seqlens, workspace, workspace_bytes, &lay, forward_only);
     if (st != KDA_OK) return st;
     // with no tokens at all (every sequence empty) the token tensors are empty and may be NULL
     const bool has_tokens = shape->B * shape->T > 0;
@@ -234,7 +290,7 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     if ((st = set_smem(kda_fwd_scan_kernel, fwd_scan_smem_bytes())) != KDA_OK) return st;
 
     prof(0, s);
-    kda_clear_status_kernel<<<1, 1, 0, s>>>(ws);
+    kda_clear_status_kernel<<<1, 1, 0, s>>>(ws, shape_hash(shape, cu_seqlens != nullptr));
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
@@ -244,8 +300,20 @@ extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const k
     if (shape->N > 0)
         kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, fwd_scan_smem_bytes(), s>>>(
             h0, o, hT, H, shape->scale, ws, lay);
+    // a forward-only workspace never completes a forward the backward could use
+    if (!forward_only) kda_fwd_done_kernel<<<1, 1, 0, s>>>(ws);
     prof(3, s);
     return cuda_status(cudaGetLastError(), "kda_fwd launch");
+}
+
+}  // namespace kda
+
+extern "C" kda_status kda_fwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                              const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log,
+                              const float* dt_bias, const float* h0, const int64_t* cu_seqlens, kda_bf16* o,
+                              float* hT, void* workspace, size_t workspace_bytes, void* stream) {
+    return fwd_entry(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens, o, hT, workspace,
+                     workspace_bytes, stream, false);
 }
 
 extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
@@ -284,6 +352,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
         return st;
     const dim3 tiles((unsigned)lay.nc_max, (unsigned)H);
     prof(4, s);
+    kda_bwd_check_kernel<<<1, 1, 0, s>>>(ws, shape_hash(shape, cu_seqlens != nullptr));
     if (shape->N > 0)
         kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, bwd_scan_smem_bytes(), s>>>(
             do_, dhT, dh0, H, ws, lay);
@@ -344,6 +413,7 @@ extern "C" const char* kda_status_string(kda_status s) {
         case KDA_ERR_OFFSETS: return "KDA_ERR_OFFSETS";
         case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
         case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+        case KDA_ERR_STALE_WORKSPACE: return "KDA_ERR_STALE_WORKSPACE";
     }
     return "KDA_ERR_UNKNOWN";
 }

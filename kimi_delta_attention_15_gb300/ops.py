@@ -19,7 +19,7 @@ from . import build as _build
 KDA_OK = 0
 _STATUS = {0: "KDA_OK", 1: "KDA_ERR_NULL", 2: "KDA_ERR_ALIGN", 3: "KDA_ERR_SHAPE",
            4: "KDA_ERR_UNSUPPORTED", 5: "KDA_ERR_WORKSPACE", 6: "KDA_ERR_OFFSETS",
-           7: "KDA_ERR_TIMEOUT", 8: "KDA_ERR_CUDA"}
+           7: "KDA_ERR_TIMEOUT", 8: "KDA_ERR_CUDA", 9: "KDA_ERR_STALE_WORKSPACE"}
 
 SCALE = 1.0 / math.sqrt(128.0)
 LOWER_BOUND = -5.0
@@ -38,7 +38,7 @@ class Shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("T", ctypes.c_int64), ("H", ctypes.c_int64),
                 ("N", ctypes.c_int64), ("K", ctypes.c_int32), ("V", ctypes.c_int32),
                 ("scale", ctypes.c_float), ("lower_bound", ctypes.c_float),
-                ("groups", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("groups", ctypes.c_int32), ("chunk_size", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -70,6 +70,8 @@ def load(build_if_missing: bool = True):
         lib.kda_status_string.restype = ctypes.c_char_p
         lib.kda_fwd_static_scratch.argtypes = [ctypes.POINTER(Shape)] + [P] * 11 + [P]
         lib.kda_fwd_static_scratch.restype = ctypes.c_int
+        lib.kda_static_scratch_device_status.argtypes = [P]
+        lib.kda_static_scratch_device_status.restype = ctypes.c_int
         lib.kda_last_error.argtypes = []
         lib.kda_last_error.restype = ctypes.c_char_p
         lib.kda_set_profile_events.argtypes = [P, ctypes.c_int]
@@ -96,10 +98,12 @@ def _stream_handle(stream=None):
 
 
 def make_shape(T: int, H: int, N: int, B: int = 1, scale: float = SCALE,
-               lower_bound: float = LOWER_BOUND, groups: int = 1) -> Shape:
-    """H counts value heads; groups = value heads per query/key head."""
+               lower_bound: float = LOWER_BOUND, groups: int = 1, chunk_size: int = 64) -> Shape:
+    """H counts value heads; groups = value heads per query/key head; chunk_size 64 or 32
+    (the library computes both with 64-token chunks: the chunk length does not change the
+    function)."""
     return Shape(B=B, T=T, H=H, N=N, K=128, V=128, scale=scale, lower_bound=lower_bound, groups=groups,
-                 reserved=0)
+                 chunk_size=chunk_size)
 
 
 def workspace_size(shape: Shape) -> int:
@@ -114,18 +118,18 @@ def _check(code, where):
         raise KdaError(code, where + detail)
 
 
-def _shape_of(q, v, cu_seqlens, B, scale, lower_bound):
+def _shape_of(q, v, cu_seqlens, B, scale, lower_bound, chunk_size=64):
     """Shape from the token tensors: H = value heads (v); q, k may hold H / groups heads."""
     H, Hqk = v.shape[-2], q.shape[-2]
     if Hqk <= 0 or H % Hqk != 0:
         raise ValueError(f"value heads ({H}) must be a multiple of query/key heads ({Hqk})")
     G = H // Hqk
     if cu_seqlens is not None:
-        return make_shape(q.shape[0], H, cu_seqlens.numel() - 1, 1, scale, lower_bound, G)
+        return make_shape(q.shape[0], H, cu_seqlens.numel() - 1, 1, scale, lower_bound, G, chunk_size)
     if q.dim() == 4:
         B_, T = q.shape[0], q.shape[1]
-        return make_shape(T, H, B_, B_, scale, lower_bound, G)
-    return make_shape(q.shape[0] // B, H, B, B, scale, lower_bound, G)
+        return make_shape(T, H, B_, B_, scale, lower_bound, G, chunk_size)
+    return make_shape(q.shape[0] // B, H, B, B, scale, lower_bound, G, chunk_size)
 
 
 def _validate(specs):
@@ -170,10 +174,10 @@ def alloc_workspace(shape: Shape, device) -> torch.Tensor:
 
 def fwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seqlens=None, *, B: int = 1,
         scale: float = SCALE, lower_bound: float = LOWER_BOUND, workspace=None, o=None,
-        hT=None, want_hT: bool = True, stream=None):
+        hT=None, want_hT: bool = True, stream=None, chunk_size: int = 64):
     """kda_fwd. Token tensors [T, H, 128] bf16 (or [B, T, H, 128]); returns (o, hT, workspace)."""
     lib = load()
-    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound)
+    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound, chunk_size)
     if workspace is None:
         workspace = alloc_workspace(shape, q.device)
     if o is None:
@@ -220,10 +224,10 @@ def fwd_static_scratch(q, k, v, g_raw, beta_raw, A_log, dt_bias, h0=None, cu_seq
 
 def bwd(q, k, v, g_raw, beta_raw, A_log, dt_bias, do, workspace, h0=None, cu_seqlens=None,
         dhT=None, *, B: int = 1, scale: float = SCALE, lower_bound: float = LOWER_BOUND,
-        grads=None, want_dh0: bool = True, stream=None):
+        grads=None, want_dh0: bool = True, stream=None, chunk_size: int = 64):
     """kda_bwd with the workspace filled by ``fwd``. Returns a dict of gradients."""
     lib = load()
-    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound)
+    shape = _shape_of(q, v, cu_seqlens, B, scale, lower_bound, chunk_size)
     if grads is None:
         grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v),
                      dg_raw=torch.empty_like(g_raw), dbeta_raw=torch.empty_like(beta_raw),
@@ -277,6 +281,11 @@ def decode(q, k, v, g_raw, beta_raw, A_log, dt_bias, state, *, o=None, scale: fl
 
 def device_status(workspace, stream=None) -> int:
     return int(load().kda_get_device_status(_ptr(workspace), _stream_handle(stream)))
+
+
+def static_scratch_device_status(stream=None) -> int:
+    """The device status word of the last fwd_static_scratch call on the current device."""
+    return int(load().kda_static_scratch_device_status(_stream_handle(stream)))
 
 
 def wait_timeout(workspace, limit_ns: int = 20_000_000):
