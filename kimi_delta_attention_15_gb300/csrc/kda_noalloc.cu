@@ -19,6 +19,11 @@
 
 namespace kda {
 void set_last_error_text(const char* msg);
+size_t forward_workspace_bytes(const kda_shape* shape, bool packed);
+kda_status fwd_entry(const kda_shape* shape, const kda_bf16* q, const kda_bf16* k, const kda_bf16* v,
+                     const kda_bf16* g_raw, const kda_bf16* beta_raw, const float* A_log, const float* dt_bias,
+                     const float* h0, const int64_t* cu_seqlens, kda_bf16* o, float* hT, void* workspace,
+                     size_t workspace_bytes, void* stream, bool forward_only);
 }
 
 namespace {
@@ -32,7 +37,8 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device; looked up on
-// the first call per device.
+// the first call per device and kept for the life of the process (a device reset,
+// which reloads the library's module, is not supported afterwards).
 kda_status scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) {
@@ -64,7 +70,8 @@ extern "C" kda_status kda_fwd_static_scratch(const kda_shape* shape, const kda_b
                                              const float* A_log, const float* dt_bias, const float* h0,
                                              const int64_t* cu_seqlens, kda_bf16* o, float* hT, void* stream) {
     if (!shape) return KDA_ERR_NULL;
-    const size_t need = kda_workspace_size(shape);
+    // the forward alone runs here: it needs only the workspace regions it writes
+    const size_t need = kda::forward_workspace_bytes(shape, cu_seqlens != nullptr);
     if (need == 0) return KDA_ERR_SHAPE;
     if (need > kStaticScratchBytes) {
         char msg[200];
@@ -77,8 +84,18 @@ extern "C" kda_status kda_fwd_static_scratch(const kda_shape* shape, const kda_b
     void* scratch = nullptr;
     const kda_status st = scratch_address(&scratch);
     if (st != KDA_OK) return st;
-    // kda_fwd clears the status word and rebuilds every table it reads; no
+    // the forward clears the status word and rebuilds every table it reads; no
     // other part of the scratch needs to start at zero.
-    return kda_fwd(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens, o, hT, scratch,
-                   kStaticScratchBytes, stream);
+    return kda::fwd_entry(shape, q, k, v, g_raw, beta_raw, A_log, dt_bias, h0, cu_seqlens, o, hT, scratch,
+                          kStaticScratchBytes, stream, true);
+}
+
+// The device status word of the last kda_fwd_static_scratch call on the current device
+// (malformed offsets or a timed-out wait found on the device are reported only there:
+// the caller never sees the scratch array's address).
+extern "C" kda_status kda_static_scratch_device_status(void* stream) {
+    void* scratch = nullptr;
+    const kda_status st = scratch_address(&scratch);
+    if (st != KDA_OK) return st;
+    return kda_get_device_status(scratch, stream);
 }
