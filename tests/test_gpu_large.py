@@ -29,8 +29,11 @@ def _heads(inp, hs):
     return sub
 
 
-@pytest.mark.parametrize("idx,hs", [(2, [0, 7, 19, 31]), (3, [0, 33, 64, 95]), (4, [1, 40, 77, 94])])
-def test_full_size_sampled_heads(idx, hs):
+# every head of the three large workloads (the fp64 oracle takes a few seconds per workload on
+# the host's cores); the printed line holds each output's normalised max error, relative error
+# and cosine
+@pytest.mark.parametrize("idx,hs", [(2, list(range(32))), (3, list(range(96))), (4, list(range(96)))])
+def test_full_size_all_heads(idx, hs):
     w = I.WORKLOADS[idx]
     inp = I.make_inputs(w)
     out = run_fwd_bwd(inp)
@@ -41,11 +44,14 @@ def test_full_size_sampled_heads(idx, hs):
     sub = _heads(inp, hs)
     ref = dict(oracle.forward(sub))
     ref.update(oracle.backward(sub))
+    rep = {}
     for k in ("o", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dA_log", "ddt_bias"):
         x = out[k][:, hs] if k not in ("dA_log", "ddt_bias") else out[k][hs]
-        check(k, x, ref[k])
+        check(k, x, ref[k], rep)
     for k in ("hT", "dh0"):
-        check(k, out[k][:, hs], ref[k])
+        if ref.get(k) is not None:
+            check(k, out[k][:, hs], ref[k], rep)
+    print(w.name, {k: tuple(f"{x:.2e}" for x in v) for k, v in rep.items()})
 
 
 # The other shapes the pages admit: T=17 with 16 heads, T=1024 with 4 heads (every
