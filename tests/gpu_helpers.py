@@ -14,12 +14,14 @@ def run_fwd_bwd(inp, want_bwd=True):
     cu = d["cu_seqlens"] if packed else None
     lb = float(inp.get("lower_bound", ops.LOWER_BOUND))   # the oracle reads the same keys
     scale = float(inp.get("scale", ops.SCALE))
+    cs = int(inp.get("chunk_size", 64))   # the library's chunk-length option; the oracle has none
     o, hT, ws = ops.fwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"],
-                        h0=d.get("h0"), cu_seqlens=cu, lower_bound=lb, scale=scale)
+                        h0=d.get("h0"), cu_seqlens=cu, lower_bound=lb, scale=scale, chunk_size=cs)
     out = dict(o=o, hT=hT)
     if want_bwd:
         g = ops.bwd(d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"], d["do"], ws,
-                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"), lower_bound=lb, scale=scale)
+                    h0=d.get("h0"), cu_seqlens=cu, dhT=d.get("dhT"), lower_bound=lb, scale=scale,
+                    chunk_size=cs)
         out.update(g)
     status = ops.device_status(ws)
     torch.cuda.synchronize()

@@ -70,8 +70,17 @@ def test_host_validation_codes(lib):
     assert _call_fwd(lib, u) == 3                            # groups must divide H
     u = ops.make_shape(64, 6, 1, groups=-1)
     assert _call_fwd(lib, u) == 3
-    u = ops.make_shape(64, 2, 1); u.reserved = 1
-    assert _call_fwd(lib, u) == 3                            # reserved field must be zero
+    for cs in (1, 16, 48, 128, -32):
+        u = ops.make_shape(64, 2, 1, chunk_size=cs)
+        assert _call_fwd(lib, u) == 4                        # chunk length 0, 32 or 64 only
+    assert lib.kda_status_string(9) == b"KDA_ERR_STALE_WORKSPACE"
+
+
+def test_chunk_size_option_accepted_on_the_host(lib):
+    """chunk_size 0, 32 and 64 pass the host checks and need the same workspace."""
+    sizes = {cs: ops.workspace_size(ops.make_shape(1000, 4, 1, chunk_size=cs)) for cs in (0, 32, 64)}
+    assert len(set(sizes.values())) == 1 and sizes[64] > 0
+    assert ops.workspace_size(ops.make_shape(1000, 4, 1, chunk_size=16)) == 0
 
 
 def test_grouped_heads_workspace(lib):

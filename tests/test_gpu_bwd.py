@@ -129,3 +129,17 @@ def test_bitwise_deterministic():
     b = run_fwd_bwd(inp)
     for k in ("o", "hT") + GRADS:
         assert torch.equal(a[k], b[k]), k
+
+
+@pytest.mark.parametrize("lengths", [(17, 33, 65), (300,)])
+def test_chunk_size_32_option(lengths):
+    """chunk_size = 32 (the other chunk length the Kimi-K3 fused_chunk validator admits) is
+    served by the 64-token chunk kernels: the chunk length blocks the computation and does
+    not change the function (the oracle's chunk-form pins hold at C = 32 and C = 64), so
+    the results equal the oracle within the tolerances and chunk_size = 64 bit for bit."""
+    inp = I.make_inputs(I.custom(lengths, 2, h0=True, dhT=True), seed=41)
+    inp32 = dict(inp, chunk_size=32)
+    out32, out64 = run_fwd_bwd(inp32), run_fwd_bwd(inp)
+    _compare(inp, out32, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
+    for k in ("o", "hT") + GRADS:
+        assert torch.equal(out32[k], out64[k]), k
