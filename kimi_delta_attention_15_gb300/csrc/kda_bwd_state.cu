@@ -3,7 +3,8 @@
 // scans, and Ut, dUt, dO of the chunk, with tcgen05 tf32 MMAs (M = 128 over the
 // key channel k):
 //   dQbar = scale dO S0            [c][k]
-//   dW    = -dUt S0                [c][k]
+//   dW    = -dUt S0                [c][k], stored as K-major panels (umma.cuh) for the
+//                                  tcgen05 products of the WY kernel
 //   dKbar = Ut dS_L                [c][k]
 //   dAqk  = scale dO Ut^T          [i][j], kept for j <= i
 //   dgam  = sum_v dS_L[v,k] S0[v,k]  (adjoint of exp(G_L) through the decayed state,
@@ -299,7 +300,6 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             float r[32];
             if (hf == 0) {
                 float* gdQ = reinterpret_cast<float*>(bg + BgOff::DQB);
-                float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
                 tmem_ld32(acc + 0, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) gdQ[j * D + kq] = scale * r[j];
@@ -308,13 +308,13 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 for (int j = 0; j < 32; ++j) gdQ[(32 + j) * D + kq] = scale * r[j];
                 tmem_ld32(acc + 64, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdW[j * D + kq] = -r[j];
+                for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(bg + BgOff::DW + panel_off(j, kq, C)) = -r[j];
             } else {
-                float* gdW = reinterpret_cast<float*>(bg + BgOff::DW);
                 float* gdK = reinterpret_cast<float*>(bg + BgOff::DKB);
                 tmem_ld32(acc + 96, r);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdW[(32 + j) * D + kq] = -r[j];
+                for (int j = 0; j < 32; ++j)
+                    *reinterpret_cast<float*>(bg + BgOff::DW + panel_off(32 + j, kq, C)) = -r[j];
                 tmem_ld32(acc + 128, r);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) gdK[j * D + kq] = r[j];

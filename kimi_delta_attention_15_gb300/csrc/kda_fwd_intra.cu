@@ -7,7 +7,8 @@
 //   Aqk_ij = sum_c q^_ic k^_jc e^{G_ic - G_jc} (j <= i),
 //   T = (I + A)^{-1} diag(beta) by blocked forward substitution,
 //   W = T (K^ * Gamma), U = T V,
-// and stores the images the two state scans consume (kda_internal.cuh).
+// and stores the images the two state scans and the backward chunk kernels consume
+// (kda_internal.cuh).
 // W and U use about fp32-accurate products (mma_sync.cuh: tf32 high parts plus bf16
 // cross terms for W; for U, T's high part in tf32 and its low part in bf16 against the
 // exact bf16 v, two k-steps per bf16 product): the final state and the gate
@@ -278,13 +279,16 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
                 const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
                 const float* pb = s.fa.Pb[r >> 4];
                 const float* sf = s.fa.Sf[r >> 4];
-                float4 qb, kb;
+                float4 qb, kb, kg;
                 qb.x = tf32_round(s.qe[r * P + c] * pb[c]);         kb.x = tf32_round(s.kp[r * P + c] * sf[c]);
                 qb.y = tf32_round(s.qe[r * P + c + 1] * pb[c + 1]); kb.y = tf32_round(s.kp[r * P + c + 1] * sf[c + 1]);
                 qb.z = tf32_round(s.qe[r * P + c + 2] * pb[c + 2]); kb.z = tf32_round(s.kp[r * P + c + 2] * sf[c + 2]);
                 qb.w = tf32_round(s.qe[r * P + c + 3] * pb[c + 3]); kb.w = tf32_round(s.kp[r * P + c + 3] * sf[c + 3]);
+                kg.x = tf32_round(s.ke[r * P + c] * pb[c]);         kg.y = tf32_round(s.ke[r * P + c + 1] * pb[c + 1]);
+                kg.z = tf32_round(s.ke[r * P + c + 2] * pb[c + 2]); kg.w = tf32_round(s.ke[r * P + c + 3] * pb[c + 3]);
                 *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
                 *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
+                *reinterpret_cast<float4*>(img + ImgOff::KT + panel_off(r, c, C)) = kg;
             }
             // transposes by 4x4 blocks: rows c0.. of the source, columns kk0..
             for (int w2 = 0; w2 < 4; ++w2) {

