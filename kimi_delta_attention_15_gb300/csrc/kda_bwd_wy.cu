@@ -33,6 +33,9 @@ namespace kda {
 namespace {
 constexpr int kWyWarps = 16;
 constexpr int kWyThreads = kWyWarps * 32;
+// issues every tcgen05 product (an MMA issue takes tens of cycles, and the rest of its warp
+// waits meanwhile: the last warp has the least other work)
+constexpr int kMmaThread = (kWyWarps - 1) * 32;
 
 struct WySmem {
     // operand tiles, 1024-byte aligned (umma.cuh panels)
@@ -189,7 +192,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         if (!ok) break;
         tc_fence_after();
         // ---- product 1: dT = dW K~^T + dU V^T
-        if (tid == 0) {
+        if (tid == kMmaThread) {
             if (mbar_wait(&s.barW, par) && mbar_wait(&s.barU, par) && mbar_wait(&s.barK, par)) {
                 const uint32_t aW = smem_u32(s.dW), aU = smem_u32(s.dU), bK = smem_u32(s.KV),
                                bV = smem_u32(s.KV + kTileCK);
@@ -236,7 +239,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         __syncthreads();
         tc_fence_after();
         // ---- products 2 and 3; dW and dU are no longer read: the next tile's stream in
-        if (tid == 0) {
+        if (tid == kMmaThread) {
             const uint32_t aS = smem_u32(s.KV), bTT = smem_u32(s.TT), aTN = smem_u32(s.TN), bDT = smem_u32(s.DT);
             for (int ks = 0; ks < C / 8; ++ks)
                 umma_tf32(tm + kD2K, desc_kmajor(aS, 2 * D, ks, 0), desc_kmajor(bTT, C, ks), id128, ks > 0);
@@ -246,17 +249,16 @@ __global__ void __launch_bounds__(kWyThreads, 1)
             for (int ks = 0; ks < C / 8; ++ks)
                 umma_tf32(tm + kD3, desc_kmajor(aTN, C, ks), desc_kmajor(bDT, C, ks), id64, ks > 0);
             umma_commit(&s.barM[2]);
-            if (cn.L > 0) { issue_dW(nxt); issue_dU(nxt); ++nb[0]; ++nb[1]; }
         }
-        // dbeta_j = sum_{i >= j} dT_ij X_ij: eight threads per column j (rows i = p mod 8),
-        // combined by shuffles in a fixed order
-        {
-            const int j = tid >> 3, p = tid & 7;
+        if (tid == 0 && cn.L > 0) { issue_dW(nxt); issue_dU(nxt); ++nb[0]; ++nb[1]; }
+        // dbeta_j = sum_{i >= j} dT_ij X_ij: warps 0..7, four threads per column j (rows i = p
+        // mod 4), combined by shuffles in a fixed order
+        if (warp < 8) {
+            const int j = tid >> 2, p = tid & 3;
             float acc = 0.0f;
 #pragma unroll
-            for (int i = p; i < C; i += 8)
+            for (int i = p; i < C; i += 4)
                 if (i >= j) acc += *reinterpret_cast<const float*>(s.DT + panel_off(i, j, C)) * s.X[i * C + j];
-            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
             acc += __shfl_xor_sync(0xffffffffu, acc, 2);
             acc += __shfl_xor_sync(0xffffffffu, acc, 1);
             if (p == 0) s.dbeta[j] = acc;
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         tc_fence_before();
         __syncthreads();
         tc_fence_after();
-        if (tid == 0) {
+        if (tid == kMmaThread) {
             const uint32_t aXT = smem_u32(s.XT), bM = smem_u32(s.DT);
             for (int ks = 0; ks < C / 8; ++ks)
                 umma_tf32(tm + kD4, desc_kmajor(aXT, C, ks), desc_kmajor(bM, C, ks), id64, ks > 0);
@@ -362,10 +364,12 @@ __global__ void __launch_bounds__(kWyThreads, 1)
     if (tid == 0) {
         if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
         // bulk copies still in flight (only after an aborted tile), bounded: the last phase
-        // issued on each barrier (phases complete in order); then every MMA issued
+        // issued on each barrier (phases complete in order)
         uint64_t* bars[5] = {&s.barW, &s.barU, &s.barK, &s.barX, &s.barB};
         for (int i = 0; i < 5; ++i)
             if (nb[i] > 0) mbar_wait(bars[i], (uint32_t)((nb[i] - 1) & 1));
+    }
+    if (tid == kMmaThread) {   // every MMA issued has completed once this phase flips
         umma_commit(&s.barFin);
         mbar_wait(&s.barFin, 0);
     }
