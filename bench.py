@@ -37,6 +37,10 @@ FLOP_PER_TH_DENSE_TILE = 544_768
 BYTES_PER_TH = 3_590
 METRIC = "fwd+bwd tokens·heads/s and TFLOP/s (% of bf16 TC peak) at T=8192,H=96,K=V=128"
 UNIT = "tokens*heads/s"
+# kernels of one kda_fwd + kda_bwd (plain heads): status/stamp, chunk table, intra-chunk,
+# forward scan, forward-complete stamp; stamp check, backward scan, state products, WY,
+# pair terms, parameter reduction
+LAUNCHES_PER_STEP = 11
 L2_FLUSH_BYTES = 512 << 20
 
 # Per-kernel algorithmic traffic and MMA work per (chunk, head) tile: the
@@ -45,11 +49,11 @@ L2_FLUSH_BYTES = 512 << 20
 KB = 1024
 KERNEL_MODEL = {
     # name: (bytes per tile, flops per tile)
-    "fwd_intra": ((64 + 0.125) * KB + 288.5 * KB, 2.5e6),
+    "fwd_intra": ((64 + 0.125) * KB + 320.5 * KB, 2.5e6),
     "fwd_scan": (256.5 * KB, 7.34e6),
     "bwd_scan": (224.5 * KB, 7.34e6),
     "bwd_state": (320.5 * KB, 6.82e6),
-    "bwd_wy": (208.0 * KB, 4.1e6),
+    "bwd_wy": (208.375 * KB, 5.24e6),
     "bwd_pair": (225.0 * KB, 2.62e6),
 }
 
@@ -57,8 +61,8 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "a084cb56a7ab8394",
-    "per_tile": {"fwd_intra": 333501, "fwd_scan": 244068, "bwd_scan": 211538, "bwd_state": 307172, "bwd_wy": 198855, "bwd_pair": 222081},
+    "sources": "e283bbafdf505e7e",
+    "per_tile": {"fwd_intra": 366179, "fwd_scan": 242634, "bwd_scan": 210192, "bwd_state": 306111, "bwd_wy": 195528, "bwd_pair": 220157},
 }
 
 
@@ -369,7 +373,7 @@ def run_gb300(args, ws, rank, local):
             "gbs": value * BYTES_PER_TH / 1e9, "pct_hbm_peak": value * BYTES_PER_TH / 1e9 / hbm,
             "fwd_ms": sum(v for k, v in kms.items() if k.startswith("fwd")),
             "bwd_ms": sum(v for k, v in kms.items() if k.startswith("bwd")),
-            "roofline": roof, "clocks": clk, "gpu_launches": 9 * args.steps}
+            "roofline": roof, "clocks": clk, "gpu_launches": LAUNCHES_PER_STEP * args.steps}
 
     # end to end through the public API with pinned host buffers
     if not args.no_e2e:
