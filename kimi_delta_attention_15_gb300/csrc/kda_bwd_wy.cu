@@ -166,26 +166,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
                 *reinterpret_cast<uint4*>(V + panel_off(r, c0 + 4 * e, C)) =
                     make_uint4(w[2 * e] << 16, w[2 * e] & 0xffff0000u, w[2 * e + 1] << 16, w[2 * e + 1] & 0xffff0000u);
         }
-        // ---- T [m][j] = X diag(beta); X^T [i][m] and T^T = diag(beta) X^T by strips: thread
-        // (row r of the transposed tile, four columns from i0) reads four rows of X
-        ok = mbar_wait(&s.barX, par) && ok;
-        for (int e = tid; e < C * C / 4; e += kWyThreads) {
-            {   // T: 4 consecutive columns of one row
-                const int m = e >> 4, j = (e & 15) * 4;
-                const float4 x = *reinterpret_cast<const float4*>(s.X + m * C + j);
-                const float4 b = *reinterpret_cast<const float4*>(s.beta + j);
-                *reinterpret_cast<float4*>(s.TN + panel_off(m, j, C)) =
-                    make_float4(tf32_round(x.x * b.x), tf32_round(x.y * b.y), tf32_round(x.z * b.z), tf32_round(x.w * b.w));
-            }
-            const int r = e & (C - 1), i0 = 4 * (e >> 6);
-            const float x0 = s.X[(i0 + 0) * C + r], x1 = s.X[(i0 + 1) * C + r];
-            const float x2 = s.X[(i0 + 2) * C + r], x3 = s.X[(i0 + 3) * C + r];
-            const float br = s.beta[r];
-            *reinterpret_cast<float4*>(s.XT + panel_off(r, i0, C)) =
-                make_float4(tf32_round(x0), tf32_round(x1), tf32_round(x2), tf32_round(x3));
-            *reinterpret_cast<float4*>(s.TT + panel_off(r, i0, C)) =
-                make_float4(tf32_round(x0 * br), tf32_round(x1 * br), tf32_round(x2 * br), tf32_round(x3 * br));
-        }
+        // V and beta are in place: product 1 is issued first and the T panels are built beside it
         fence_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(ok);
@@ -205,6 +186,28 @@ __global__ void __launch_bounds__(kWyThreads, 1)
                 ok = false;
             }
         }
+        // ---- T [m][j] = X diag(beta); X^T [i][m] and T^T = diag(beta) X^T by strips: thread
+        // (row r of the transposed tile, four columns from i0) reads four rows of X. Warps 0..14,
+        // while product 1 runs (the MMA thread's warp stays out)
+        ok = mbar_wait(&s.barX, par) && ok;
+        for (int e = tid; e < C * C / 4 && tid < kMmaThread; e += kMmaThread) {
+            {   // T: 4 consecutive columns of one row
+                const int m = e >> 4, j = (e & 15) * 4;
+                const float4 x = *reinterpret_cast<const float4*>(s.X + m * C + j);
+                const float4 b = *reinterpret_cast<const float4*>(s.beta + j);
+                *reinterpret_cast<float4*>(s.TN + panel_off(m, j, C)) =
+                    make_float4(tf32_round(x.x * b.x), tf32_round(x.y * b.y), tf32_round(x.z * b.z), tf32_round(x.w * b.w));
+            }
+            const int r = e & (C - 1), i0 = 4 * (e >> 6);
+            const float x0 = s.X[(i0 + 0) * C + r], x1 = s.X[(i0 + 1) * C + r];
+            const float x2 = s.X[(i0 + 2) * C + r], x3 = s.X[(i0 + 3) * C + r];
+            const float br = s.beta[r];
+            *reinterpret_cast<float4*>(s.XT + panel_off(r, i0, C)) =
+                make_float4(tf32_round(x0), tf32_round(x1), tf32_round(x2), tf32_round(x3));
+            *reinterpret_cast<float4*>(s.TT + panel_off(r, i0, C)) =
+                make_float4(tf32_round(x0 * br), tf32_round(x1 * br), tf32_round(x2 * br), tf32_round(x3 * br));
+        }
+        fence_async_smem();
         ok = ok && mbar_wait(&s.barM[0], par);
         ok = __syncthreads_and(ok);
         if (!ok) break;
