@@ -20,8 +20,9 @@
 // flight:
 //   warp 0        bulk copies of the panels: lane 0 the three-stage ring, lane 1
 //                 the two-stage ring and, one tile ahead, the next tile's dO rows
-//   warps 4..7    split Ut, dUt into tf32 high + low parts, dO to fp32, and the
-//                 diagonal dgam on the CUDA cores
+//   warps 4..7    split Ut, dUt into tf32 high + low parts and dO to fp32, hand them to
+//                 the MMAs, then the diagonal dgam on the CUDA cores (a stage of the
+//                 S0^T / dS_L^T ring is free once the MMAs and these warps are done with it)
 //   warp 1        the MMAs of a panel into one of two TMEM accumulator sets
 //   warps 8..15   accumulators -> workspace, overlapping the next tile's MMAs
 // S0, dS_L and dO are exact in tf32; Ut and dUt enter as high + low parts.
@@ -77,7 +78,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
     if (tid == 0) {
         for (int i = 0; i < kStA; ++i) {
             mbar_init(&s.fullA[i], 1);
-            mbar_init(&s.emptyA[i], 1);
+            mbar_init(&s.emptyA[i], 1 + 128);   // the MMAs' commit and the 128 splitter threads
         }
         for (int i = 0; i < kStB; ++i) {
             mbar_init(&s.fullB[i], 1);
@@ -178,8 +179,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 const uint32_t acc = tm + 256u * tb;
                 for (int p = 0; p < 4; ++p, ++it) {
                     const int sa = it % kStA, sb = it & 1;
-                    // the splitter has seen both rings' copies of this panel land
-                    if (!mbar_wait(&s.ready[sb], (it >> 1) & 1) ||
+                    // the split operands are ready and the S0^T / dS_L^T panels have landed
+                    if (!mbar_wait(&s.ready[sb], (it >> 1) & 1) || !mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) ||
                         (p == 0 && !mbar_wait(&s.tempty[tb], ((n >> 1) & 1) ^ 1)) || *abort_flag) {
                         ok = false;
                         break;
@@ -228,23 +229,12 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             float dg = 0.0f;
             for (int p = 0; p < 4; ++p, ++it) {
                 const int sa = it % kStA, sg = it & 1;
-                if (!mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) ||
-                    !mbar_wait(&s.fullB[sg], (uint32_t)((it >> 1) & 1)) ||
+                if (!mbar_wait(&s.fullB[sg], (uint32_t)((it >> 1) & 1)) ||
                     (p == 0 && !mbar_wait(&s.dfull[n & 1], (uint32_t)((n >> 1) & 1))) || *abort_flag) {
                     ok = false;
                     break;
                 }
-                const StageA& ga = s.sa[sa];
                 StageB& g = s.sb[sg];
-                // dgam: row k of S0^T and dS_L^T
-#pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const uint32_t off = t * 128u + ((j4 ^ (t & 7)) << 4);
-                    const float4 a = *reinterpret_cast<const float4*>(ga.S0T + off);
-                    const float4 b = *reinterpret_cast<const float4*>(ga.DST + off);
-                    dg = fmaf(a.x, b.x, dg); dg = fmaf(a.y, b.y, dg);
-                    dg = fmaf(a.z, b.z, dg); dg = fmaf(a.w, b.w, dg);
-                }
                 // Ut, dUt -> high (in place) + low parts; dO rows -> fp32 (zero past the chunk)
 #pragma unroll
                 for (int r = 0; r < 4; ++r) {
@@ -272,6 +262,22 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 }
                 fence_async_smem();
                 mbar_arrive(&s.ready[sg]);
+                // dgam: row k of S0^T and dS_L^T, after the split is handed to the MMAs; the
+                // stage of these panels is released by this thread's arrival and the MMAs' commit
+                if (!mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const StageA& ga = s.sa[sa];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const uint32_t off = t * 128u + ((j4 ^ (t & 7)) << 4);
+                    const float4 a = *reinterpret_cast<const float4*>(ga.S0T + off);
+                    const float4 b = *reinterpret_cast<const float4*>(ga.DST + off);
+                    dg = fmaf(a.x, b.x, dg); dg = fmaf(a.y, b.y, dg);
+                    dg = fmaf(a.z, b.z, dg); dg = fmaf(a.w, b.w, dg);
+                }
+                mbar_arrive(&s.emptyA[sa]);
             }
             if (!ok) break;
             const size_t tt = (size_t)chunk * H + (tile - chunk * H);
