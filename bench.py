@@ -37,10 +37,10 @@ FLOP_PER_TH_DENSE_TILE = 544_768
 BYTES_PER_TH = 3_590
 METRIC = "fwd+bwd tokens·heads/s and TFLOP/s (% of bf16 TC peak) at T=8192,H=96,K=V=128"
 UNIT = "tokens*heads/s"
-# kernels of one kda_fwd + kda_bwd (plain heads): status/stamp, chunk table, intra-chunk,
-# forward scan, forward-complete stamp; stamp check, backward scan, state products, WY,
-# pair terms, parameter reduction
-LAUNCHES_PER_STEP = 11
+# kernels of one kda_fwd + kda_bwd (plain heads): chunk table (with the status clear and the
+# provenance stamp), intra-chunk, forward scan; backward scan (with the stamp check), state
+# products, WY, pair terms, parameter reduction
+LAUNCHES_PER_STEP = 8
 L2_FLUSH_BYTES = 512 << 20
 
 # Per-kernel algorithmic traffic and MMA work per (chunk, head) tile: the

@@ -16,7 +16,7 @@ size_t bwd_pair_smem_bytes();
 
 FwdIntraKernel fwd_intra_kernel(bool grouped);
 __global__ void kda_fwd_scan_kernel(const float*, uint16_t*, float*, int, float, uint8_t*, Layout);
-__global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, uint8_t*, Layout);
+__global__ void kda_bwd_scan_kernel(const uint16_t*, const float*, float*, int, uint8_t*, Layout, uint64_t);
 __global__ void kda_bwd_state_kernel(const uint16_t*, int, float, uint8_t*, Layout);
 BwdWyKernel bwd_wy_kernel(bool grouped);
 BwdPairKernel bwd_pair_kernel(bool grouped);
@@ -30,9 +30,11 @@ __global__ void kda_qk_group_reduce_kernel(uint16_t*, uint16_t*, uint8_t*, int64
 // One CTA; N is small next to the token count.
 constexpr int kOrderKeys = 4096;   // distinct chunk counts the scan order tells apart
 
+// It also starts the forward's bookkeeping: clears the status word, stamps the shape hash
+// and marks the forward as not complete yet (the forward scan's last CTA completes it).
 __global__ void __launch_bounds__(1024)
     kda_chunk_table_kernel(const int64_t* __restrict__ cu, int64_t N, int64_t T_total, int64_t T_fixed,
-                           uint8_t* __restrict__ ws, Layout lay) {
+                           uint8_t* __restrict__ ws, Layout lay, uint64_t shape_hash) {
     __shared__ int carry;
     __shared__ int bad;
     __shared__ int scan[1024];
@@ -42,6 +44,10 @@ __global__ void __launch_bounds__(1024)
     const int tid = threadIdx.x;
     auto cu_at = [&](int64_t i) -> int64_t { return cu ? cu[i] : i * T_fixed; };
     if (tid == 0) {
+        *reinterpret_cast<int*>(ws) = 0;
+        *reinterpret_cast<uint64_t*>(ws + kStampHashOff) = shape_hash;
+        *reinterpret_cast<uint32_t*>(ws + kStampDoneOff) = 0u;
+        *reinterpret_cast<uint32_t*>(ws + kFwdCountOff) = 0u;
         carry = 0;
         bad = (cu_at(0) != 0 || cu_at(N) != T_total) ? 1 : 0;
     }
@@ -121,28 +127,6 @@ __global__ void __launch_bounds__(1024)
     }
     __syncthreads();
     for (int64_t n = tid; n < N; n += blockDim.x) order[atomicAdd(&slot[key_of(n)], 1)] = (int)n;
-}
-
-// Start of a forward: clear the status word, stamp the shape hash, and mark the
-// forward as not complete yet.
-__global__ void kda_clear_status_kernel(uint8_t* ws, uint64_t shape_hash) {
-    *reinterpret_cast<int*>(ws) = 0;
-    *reinterpret_cast<uint64_t*>(ws + kStampHashOff) = shape_hash;
-    *reinterpret_cast<uint32_t*>(ws + kStampDoneOff) = 0u;
-}
-
-// End of a forward: the workspace holds a complete forward unless a kernel raised an error.
-__global__ void kda_fwd_done_kernel(uint8_t* ws) {
-    if (read_status(ws) == 0) *reinterpret_cast<volatile uint32_t*>(ws + kStampDoneOff) = kFwdDone;
-}
-
-// Start of a backward: the workspace must hold a completed forward of the same shape;
-// otherwise every later kernel of the backward finds the status word set and skips.
-__global__ void kda_bwd_check_kernel(uint8_t* ws, uint64_t shape_hash) {
-    if (read_status(ws) != 0) return;
-    const uint64_t stamp = *reinterpret_cast<const volatile uint64_t*>(ws + kStampHashOff);
-    const uint32_t done = *reinterpret_cast<const volatile uint32_t*>(ws + kStampDoneOff);
-    if (stamp != shape_hash || done != kFwdDone) raise_status(ws, KDA_ERR_STALE_WORKSPACE);
 }
 
 // Lets the other translation units of the library set the text kda_last_error returns.
@@ -290,8 +274,8 @@ kda_status fwd_entry(const kda_shape* shape, const kda_bf16* q, const kda_bf16* 
     if ((st = set_smem(kda_fwd_scan_kernel, fwd_scan_smem_bytes())) != KDA_OK) return st;
 
     prof(0, s);
-    kda_clear_status_kernel<<<1, 1, 0, s>>>(ws, shape_hash(shape, cu_seqlens != nullptr));
-    kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay);
+    kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay,
+                                              shape_hash(shape, cu_seqlens != nullptr));
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
         intra<<<persistent_grid(lay.nc_max * H), 512, fwd_intra_smem_bytes(), s>>>(
@@ -300,8 +284,6 @@ kda_status fwd_entry(const kda_shape* shape, const kda_bf16* q, const kda_bf16* 
     if (shape->N > 0)
         kda_fwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, fwd_scan_smem_bytes(), s>>>(
             h0, o, hT, H, shape->scale, ws, lay);
-    // a forward-only workspace never completes a forward the backward could use
-    if (!forward_only) kda_fwd_done_kernel<<<1, 1, 0, s>>>(ws);
     prof(3, s);
     return cuda_status(cudaGetLastError(), "kda_fwd launch");
 }
@@ -352,10 +334,9 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
         return st;
     const dim3 tiles((unsigned)lay.nc_max, (unsigned)H);
     prof(4, s);
-    kda_bwd_check_kernel<<<1, 1, 0, s>>>(ws, shape_hash(shape, cu_seqlens != nullptr));
     if (shape->N > 0)
         kda_bwd_scan_kernel<<<dim3((unsigned)H, (unsigned)shape->N), 256, bwd_scan_smem_bytes(), s>>>(
-            do_, dhT, dh0, H, ws, lay);
+            do_, dhT, dh0, H, ws, lay, shape_hash(shape, cu_seqlens != nullptr));
     prof(5, s);
     if (lay.nc_max > 0)
         kda_bwd_state_kernel<<<persistent_grid(lay.nc_max * H), 512, bwd_state_smem_bytes(), s>>>(do_, H, scale, ws,

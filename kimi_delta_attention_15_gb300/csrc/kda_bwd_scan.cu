@@ -36,10 +36,17 @@ size_t bwd_scan_smem_bytes() { return sizeof(BScanSmem) + 1024; }
 
 __global__ void __launch_bounds__(256, 1)
     kda_bwd_scan_kernel(const uint16_t* __restrict__ dO, const float* __restrict__ dhT, float* __restrict__ dh0,
-                        int H, uint8_t* __restrict__ ws, Layout lay) {
+                        int H, uint8_t* __restrict__ ws, Layout lay, uint64_t shape_hash) {
     extern __shared__ uint8_t smem_raw[];
     BScanSmem& s = *reinterpret_cast<BScanSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     if (read_status(ws) != 0) return;
+    // the workspace must hold a completed forward of this shape (its provenance stamp);
+    // every CTA reads the same words, so all of them return or none
+    if (*reinterpret_cast<const volatile uint64_t*>(ws + kStampHashOff) != shape_hash ||
+        *reinterpret_cast<const volatile uint32_t*>(ws + kStampDoneOff) != kFwdDone) {
+        if (threadIdx.x == 0) raise_status(ws, KDA_ERR_STALE_WORKSPACE);
+        return;
+    }
     const int h = blockIdx.x;
     const int n = reinterpret_cast<const int*>(ws + lay.seq_order)[blockIdx.y];
     const int cf = reinterpret_cast<const int*>(ws + lay.seq_first)[n];

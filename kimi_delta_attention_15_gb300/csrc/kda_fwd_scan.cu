@@ -270,6 +270,16 @@ __global__ void __launch_bounds__(256, 1)
     tc_fence_before();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tm, 512);
+    // the last CTA of the scan to finish marks the forward complete, unless a kernel of the
+    // forward raised an error (the backward checks this word)
+    if (tid == 0) {
+        __threadfence();
+        const unsigned total = gridDim.x * gridDim.y;
+        if (atomicAdd(reinterpret_cast<unsigned*>(ws + kFwdCountOff), 1u) == total - 1u) {
+            __threadfence();
+            if (read_status(ws) == 0) *reinterpret_cast<volatile uint32_t*>(ws + kStampDoneOff) = kFwdDone;
+        }
+    }
 }
 
 }  // namespace kda

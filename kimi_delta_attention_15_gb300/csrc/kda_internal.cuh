@@ -144,9 +144,10 @@ __host__ __device__ inline size_t qk_share_offset(const Layout& l) {
 // The status region (the first 256 bytes of the workspace): the device status word at
 // byte 0; the forward's provenance stamp, a hash of its shape at byte 8 and the
 // "forward complete" word at byte 16 (kFwdDone once the forward's last kernel ran
-// without error).
+// without error); at byte 24 the count of forward-scan CTAs that have finished.
 constexpr size_t kStampHashOff = 8;
 constexpr size_t kStampDoneOff = 16;
+constexpr size_t kFwdCountOff = 24;
 constexpr uint32_t kFwdDone = 0x4b444146u;
 
 // Device status word helpers (first int32 of the workspace).
