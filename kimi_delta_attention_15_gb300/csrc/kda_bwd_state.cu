@@ -20,9 +20,9 @@
 // flight:
 //   warp 0        bulk copies of the panels: lane 0 the three-stage ring, lane 1
 //                 the two-stage ring and, one tile ahead, the next tile's dO rows
-//   warps 4..7    split Ut, dUt into tf32 high + low parts and dO to fp32, hand them to
-//                 the MMAs, then the diagonal dgam on the CUDA cores (a stage of the
-//                 S0^T / dS_L^T ring is free once the MMAs and these warps are done with it)
+//   warps 2..7    split Ut, dUt into tf32 high + low parts and dO to fp32 and hand them to
+//                 the MMAs; then warps 4..7 sum the diagonal dgam on the CUDA cores (a stage of
+//                 the S0^T / dS_L^T ring is free once the MMAs and these warps are done with it)
 //   warp 1        the MMAs of a panel into one of two TMEM accumulator sets
 //   warps 8..15   accumulators -> workspace, overlapping the next tile's MMAs
 // S0, dS_L and dO are exact in tf32; Ut and dUt enter as high + low parts.
@@ -38,6 +38,7 @@ constexpr uint32_t kPanelCD = C * 128;   // one 32-column panel of a 64-row tile
 constexpr int kDoPitch = 2 * D + 64;     // bytes per staged dO row (padded against bank conflicts)
 
 constexpr int kStA = 3, kStB = 2;        // stages of the two rings
+constexpr int kSplitThreads = 192;       // warps 2..7 split the operands; warps 4..7 also sum dgam
 struct StageA {
     uint8_t S0T[kPanelDD];   // S0^T   [128 k][32 v]
     uint8_t DST[kPanelDD];   // dS_L^T [128 k][32 v]
@@ -83,7 +84,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
         for (int i = 0; i < kStB; ++i) {
             mbar_init(&s.fullB[i], 1);
             mbar_init(&s.emptyB[i], 1);
-            mbar_init(&s.ready[i], 128);
+            mbar_init(&s.ready[i], kSplitThreads);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
@@ -216,9 +217,10 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             mbar_wait(&s.fin, 0);
         }
         __syncwarp();
-    } else if (warp >= 4 && warp < 8) {
+    } else if (warp >= 2 && warp < 8) {
         // --------------------------------------------------------- splitter
-        const int t = tid - 128;   // row k of the key-major panels
+        const int t2 = tid - 64;    // item index of the split (0 .. 191)
+        const int t = tid - 128;    // row k of the key-major panels, for dgam (warps 4..7)
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x, n = 0; tile < ntiles && ok; tile += gridDim.x) {
@@ -235,10 +237,12 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                     break;
                 }
                 StageB& g = s.sb[sg];
-                // Ut, dUt -> high (in place) + low parts; dO rows -> fp32 (zero past the chunk)
+                // Ut, dUt -> high (in place) + low parts; dO rows -> fp32 (zero past the chunk):
+                // 512 items of 16 bytes, 192 threads
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    const int e = t + 128 * r, c = e >> 3, j4 = e & 7;
+                for (int r = 0; r < 3; ++r) {
+                    const int e = t2 + kSplitThreads * r, c = e >> 3, j4 = e & 7;
+                    if (e >= 4 * C * 2) break;
                     const uint32_t off = c * 128u + ((j4 ^ (c & 7)) << 4);
                     float4 x = *reinterpret_cast<const float4*>(g.UH + off);
                     float4 xh = make_float4(tf32_round(x.x), tf32_round(x.y), tf32_round(x.z), tf32_round(x.w));
@@ -262,6 +266,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 }
                 fence_async_smem();
                 mbar_arrive(&s.ready[sg]);
+                if (t < 0) continue;   // warps 2, 3: the split only
                 // dgam: row k of S0^T and dS_L^T, after the split is handed to the MMAs; the
                 // stage of these panels is released by this thread's arrival and the MMAs' commit
                 if (!mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) || *abort_flag) {
@@ -281,7 +286,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             }
             if (!ok) break;
             const size_t tt = (size_t)chunk * H + (tile - chunk * H);
-            reinterpret_cast<float*>(ws + lay.bg + tt * BgOff::BYTES + BgOff::DGAM)[t] = dg;
+            if (t >= 0) reinterpret_cast<float*>(ws + lay.bg + tt * BgOff::BYTES + BgOff::DGAM)[t] = dg;
             ++n;
         }
         if (!ok) *abort_flag = 1;
