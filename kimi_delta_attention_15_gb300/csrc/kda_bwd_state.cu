@@ -15,11 +15,14 @@
 // Persistent and warp-specialised. Every product contracts over the value
 // channel v, so a tile streams through shared memory as four 32-column value
 // panels, in two rings: the S0^T and dS_L^T panels (two thirds of the bytes) in
-// three stages, Ut, dUt and their split parts in two; a stage stays in use from its
-// copy to the end of the MMAs that read it, so the deeper ring keeps more bytes in
-// flight:
-//   warp 0        bulk copies of the panels: lane 0 the three-stage ring, lane 1
-//                 the two-stage ring and, one tile ahead, the next tile's dO rows
+// two stages, Ut, dUt and their split parts in three. A stage of the second ring stays in
+// use from its copy through the split to the end of the MMAs that read it, the longest
+// hold, so that ring gets the third stage (three stages for the first ring and two for
+// the second: 0.856 ms at T=8192, H=96; the other way round: 0.762 ms):
+//   warp 0        bulk copies of the panels: lane 0 the S0^T / dS_L^T ring (two stages),
+//                 lane 1 the Ut / dUt ring (three stages: a stage is held from its copy
+//                 through the split to the end of its MMAs) and, one tile ahead, the next
+//                 tile's dO rows
 //   warps 2..7    split Ut, dUt into tf32 high + low parts and dO to fp32 and hand them to
 //                 the MMAs; then warps 4..7 sum the diagonal dgam on the CUDA cores (a stage of
 //                 the S0^T / dS_L^T ring is free once the MMAs and these warps are done with it)
@@ -37,7 +40,7 @@ constexpr uint32_t kPanelDD = D * 128;   // one 32-column panel of a 128-row til
 constexpr uint32_t kPanelCD = C * 128;   // one 32-column panel of a 64-row tile (8 KB)
 constexpr int kDoPitch = 2 * D + 64;     // bytes per staged dO row (padded against bank conflicts)
 
-constexpr int kStA = 3, kStB = 2;        // stages of the two rings
+constexpr int kStA = 2, kStB = 3;        // stages of the two rings
 constexpr int kSplitThreads = 192;       // warps 2..7 split the operands; warps 4..7 also sum dgam
 struct StageA {
     uint8_t S0T[kPanelDD];   // S0^T   [128 k][32 v]
@@ -142,8 +145,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                         bulk_g2s(s.sa[sa].S0T, gS0 + p * kPanelDD, kPanelDD, &s.fullA[sa]);
                         bulk_g2s(s.sa[sa].DST, gDS + p * kPanelDD, kPanelDD, &s.fullA[sa]);
                     } else {
-                        const int sb = it & 1;
-                        if (!mbar_wait(&s.emptyB[sb], (uint32_t)(((it >> 1) & 1) ^ 1)) || *abort_flag) {
+                        const int sb = it % kStB;
+                        if (!mbar_wait(&s.emptyB[sb], (uint32_t)(((it / kStB) & 1) ^ 1)) || *abort_flag) {
                             ok = false;
                             break;
                         }
@@ -162,7 +165,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             if (ring_a)
                 for (int j = it - 1; j >= 0 && j >= it - kStA; --j) mbar_wait(&s.fullA[j % kStA], (uint32_t)((j / kStA) & 1));
             else {
-                for (int j = it - 1; j >= 0 && j >= it - kStB; --j) mbar_wait(&s.fullB[j & 1], (uint32_t)((j >> 1) & 1));
+                for (int j = it - 1; j >= 0 && j >= it - kStB; --j) mbar_wait(&s.fullB[j % kStB], (uint32_t)((j / kStB) & 1));
                 for (int j = d_issued - 1; j >= 0 && j >= d_issued - 2; --j)
                     mbar_wait(&s.dfull[j & 1], (uint32_t)((j >> 1) & 1));
             }
@@ -179,9 +182,9 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 const int tb = n & 1;
                 const uint32_t acc = tm + 256u * tb;
                 for (int p = 0; p < 4; ++p, ++it) {
-                    const int sa = it % kStA, sb = it & 1;
+                    const int sa = it % kStA, sb = it % kStB;
                     // the split operands are ready and the S0^T / dS_L^T panels have landed
-                    if (!mbar_wait(&s.ready[sb], (it >> 1) & 1) || !mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) ||
+                    if (!mbar_wait(&s.ready[sb], (uint32_t)((it / kStB) & 1)) || !mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) ||
                         (p == 0 && !mbar_wait(&s.tempty[tb], ((n >> 1) & 1) ^ 1)) || *abort_flag) {
                         ok = false;
                         break;
@@ -230,8 +233,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             const uint8_t* dos = s.dos[n & 1];
             float dg = 0.0f;
             for (int p = 0; p < 4; ++p, ++it) {
-                const int sa = it % kStA, sg = it & 1;
-                if (!mbar_wait(&s.fullB[sg], (uint32_t)((it >> 1) & 1)) ||
+                const int sa = it % kStA, sg = it % kStB;
+                if (!mbar_wait(&s.fullB[sg], (uint32_t)((it / kStB) & 1)) ||
                     (p == 0 && !mbar_wait(&s.dfull[n & 1], (uint32_t)((n >> 1) & 1))) || *abort_flag) {
                     ok = false;
                     break;
