@@ -61,8 +61,8 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "e283bbafdf505e7e",
-    "per_tile": {"fwd_intra": 366179, "fwd_scan": 242634, "bwd_scan": 210192, "bwd_state": 306111, "bwd_wy": 195528, "bwd_pair": 220157},
+    "sources": "b3772659baf93d88",
+    "per_tile": {"fwd_intra": 366144, "fwd_scan": 242885, "bwd_scan": 210215, "bwd_state": 306549, "bwd_wy": 195449, "bwd_pair": 220133},
 }
 
 
