@@ -22,7 +22,8 @@
 // Every term above is per key channel except the row norms of q and k and the row
 // dot products of the L2-norm chains. A cluster of two CTAs takes each tile, CTA r
 // the key channels 64r .. 64r+63; the two exchange those per-row partial sums
-// through distributed shared memory. Half the channels need half the shared memory
+// through distributed shared memory: st.async writes into the peer, counted in bytes on
+// the peer's mbarrier, so that no fence waits for this CTA's own global traffic. Half the channels need half the shared memory
 // (about 107 KB), so two CTAs share an SM and the memory phases of one overlap the
 // arithmetic of the other. Persistent over tiles; the raw q, k, g_raw rows of the
 // cluster's next tile are staged by cp.async in the dAqk and dB tiles, which are
@@ -48,13 +49,17 @@ static_assert(CH == C, "the [64][64] tiles share one layout");
 // lane / 4 and column by lane % 4, or the transpose) are free of bank conflicts.
 // Aligned groups of four columns stay contiguous (16-byte copies keep working).
 __device__ __forceinline__ int sw(int r, int c) { return r * CH + (c ^ (((r & 3) << 3) | (r & 4))); }
-// [64][64] fp32 channel tiles: rows padded to 68 floats (plain addressing with constant
-// offsets; the fragment loads with rows by lane % 4 see two-way bank conflicts)
-constexpr int PCH = CH + 4;
+// [64][64] fp32 channel tiles: rows padded to 72 floats (plain addressing with constant
+// offsets). A row stride of 8 banks keeps the two access patterns these tiles see free of
+// bank conflicts: mma fragments with the row by lane % 4 and the column by lane / 4, and
+// 8-byte element pairs with the row by lane / 4 and the column pair by lane % 4.
+constexpr int PCH = CH + 8;
 __device__ __forceinline__ int pidx(int r, int c) { return r * PCH + c; }
 
+// block-pair factors f_IJ of the lower triangle J <= I, at fidx(I, J)
+__device__ __forceinline__ int fidx(int I, int J) { return I * (I + 1) / 2 + J; }
 struct PairFactors {
-    float F[NSUB][NSUB][CH];
+    float F[NSUB * (NSUB + 1) / 2][CH];
     float Pb[NSUB][CH];
     float Sf[NSUB][CH];
     float Db[NSUB][CH];
@@ -75,7 +80,9 @@ struct PairSmem {
     alignas(16) float dtb[CH];
     float red[kPairWarps];
     float go;
+    int bad;            // a partial-sum wait timed out: later waits are skipped
     uint16_t braw[C];
+    alignas(8) uint64_t mb_xn, mb_xd;   // the peer's 512 bytes of xn, of xd (one phase per tile)
 };
 static_assert(sizeof(PairSmem) <= 113 * 1024, "two CTAs per SM");
 
@@ -96,6 +103,42 @@ __device__ __forceinline__ void st_cluster(const float* local, uint32_t rank, fl
 __device__ __forceinline__ void st_both(float* local, uint32_t peer, float v) {
     *local = v;
     st_cluster(local, peer, v);
+}
+
+// v into the same shared-memory location of CTA `rank`, counted as 4 bytes on that CTA's
+// mbarrier at the location of `bar`
+__device__ __forceinline__ void st_async_peer(const float* local, const uint64_t* bar, uint32_t rank, float v) {
+    uint32_t ra, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(smem_u32(local)), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(smem_u32(bar)), "r"(rank));
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(ra),
+                 "r"(__float_as_uint(v)), "r"(rb)
+                 : "memory");
+}
+// one test of a phase of an mbarrier completed by the peer's writes; acquire at cluster
+// scope, so that those writes are visible afterwards
+__device__ __forceinline__ bool mbar_test_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n"
+        " mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+// the rest of a bounded wait (kWaitLimitNs), out of line: the tile loop keeps its registers
+__device__ __noinline__ bool mbar_wait_cluster_slow(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_test_cluster(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    return mbar_test_cluster(a, parity) || mbar_wait_cluster_slow(a, parity);
 }
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -123,9 +166,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     constexpr uint32_t kAll = 0xffffffffu;
 
     // Both CTAs of the cluster run or neither: rank 0 reads the status word and passes
-    // its decision on. The first barrier also makes sure both CTAs have started before
-    // either writes into the other's shared memory; every later step is taken by both
-    // CTAs alike (same tiles, same exits), so every cluster barrier is met by both.
+    // its decision on. The first barrier also makes sure both CTAs have started, and
+    // their mbarriers are initialised, before either writes into the other's shared
+    // memory; every later step is taken by both CTAs alike (same tiles, same exits), so
+    // every cluster barrier is met by both and every partial sum one CTA waits for is
+    // sent by the other. A CTA receives its peer's partial sums of a tile only after the
+    // peer has read its own of the tile before (each exchange is answered by the next
+    // one), so one buffer of each suffices.
+    if (tid == 0) {
+        mbar_init(&s.mb_xn, 1);
+        mbar_init(&s.mb_xd, 1);
+        s.bad = 0;
+        fence_mbar_init();
+    }
     cluster_arrive();
     cluster_wait();
     if (half == 0 && tid == 0) st_both(&s.go, peer, read_status(ws) == 0 ? 1.0f : 0.0f);
@@ -169,6 +222,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     stage_tile(tile_i, ci);
     float alog = alog_next;
     uint16_t braw = braw_next;
+    uint32_t par = 0;   // phase parity of mb_xn and mb_xd for this tile
+    // after a __syncthreads: wait for the peer's partial sums (skipped once a wait has
+    // timed out, which is reported in the status word)
+    auto wait_peer = [&](uint64_t* bar) {
+        if (s.bad == 0 && !mbar_wait_cluster(bar, par)) {
+            s.bad = 1;
+            raise_status(ws, KDA_ERR_TIMEOUT);
+        }
+    };
     while (true) {
     const int nxt = tile_i + step;
     const ChunkInfo cn = nxt < ntiles ? chunks[nxt / H] : ChunkInfo{0, 0, 0, 0};
@@ -180,6 +242,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     const float a_h = __expf(alog);
 
     if (tid < C) s.braw[tid] = braw;
+    if (tid == 0) {   // this tile's phase of both exchanges: 2 x 64 floats from the peer each
+        mbar_arrive_expect_tx(&s.mb_xn, 2 * C * 4);
+        mbar_arrive_expect_tx(&s.mb_xd, 2 * C * 4);
+    }
     cp_async_wait_all();
     __syncthreads();
     // ---- rows: a half-warp per row, lane l the channels cb + 4(l % 16) .. +3 of row
@@ -248,11 +314,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
         for (int b = 0; b < RB; ++b) {
             const int r = 16 * b + 2 * warp + hl;
-            if ((lane & 15) == 0) st_both(&s.xn[half][0][r], peer, sq[b]);
-            if ((lane & 15) == 1) st_both(&s.xn[half][1][r], peer, sk[b]);
+            if ((lane & 15) < 2) {
+                float* x = &s.xn[half][lane & 15][r];
+                const float v = (lane & 15) == 0 ? sq[b] : sk[b];
+                *x = v;
+                st_async_peer(x, &s.mb_xn, peer, v);
+            }
         }
     }
-    cluster_arrive();
     // gates and beta need no norm: computed while the peer's partials arrive
     {
         const float dtv[4] = {dt4.x, dt4.y, dt4.z, dt4.w};
@@ -269,7 +338,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
             if ((lane & 15) == 0) s.beta[r] = r < L ? sigmoidf(bf2f(s.braw[r])) : 0.0f;
         }
     }
-    cluster_wait();
+    __syncthreads();
+    wait_peer(&s.mb_xn);
 #pragma unroll
     for (int b = 0; b < RB; ++b) {
         const int r = 16 * b + 2 * warp + hl;
@@ -316,9 +386,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
         s.fa.Pb[0][c] = 1.0f; s.fa.Pb[1][c] = d0; s.fa.Pb[2][c] = d0 * d1; s.fa.Pb[3][c] = d0 * d1 * d2;
         s.fa.gl[c] = d0 * d1 * d2 * d3;
         s.fa.Sf[3][c] = 1.0f; s.fa.Sf[2][c] = d3; s.fa.Sf[1][c] = d2 * d3; s.fa.Sf[0][c] = d1 * d2 * d3;
-        s.fa.F[0][0][c] = 1.0f / d0; s.fa.F[1][1][c] = 1.0f / d1; s.fa.F[2][2][c] = 1.0f / d2; s.fa.F[3][3][c] = 1.0f / d3;
-        s.fa.F[1][0][c] = 1.0f; s.fa.F[2][1][c] = 1.0f; s.fa.F[3][2][c] = 1.0f;
-        s.fa.F[2][0][c] = d1; s.fa.F[3][1][c] = d2; s.fa.F[3][0][c] = d1 * d2;
+        s.fa.F[fidx(0, 0)][c] = 1.0f / d0; s.fa.F[fidx(1, 1)][c] = 1.0f / d1;
+        s.fa.F[fidx(2, 2)][c] = 1.0f / d2; s.fa.F[fidx(3, 3)][c] = 1.0f / d3;
+        s.fa.F[fidx(1, 0)][c] = 1.0f; s.fa.F[fidx(2, 1)][c] = 1.0f; s.fa.F[fidx(3, 2)][c] = 1.0f;
+        s.fa.F[fidx(2, 0)][c] = d1; s.fa.F[fidx(3, 1)][c] = d2; s.fa.F[fidx(3, 0)][c] = d1 * d2;
     }
     __syncthreads();
 
@@ -361,7 +432,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) accB[nt][e] = accA[nt][e] = 0.0f;
         for (int J = 0; J <= I; ++J) {
-            const float* f = s.fa.F[I][J];
+            const float* f = s.fa.F[fidx(I, J)];
             float fc[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) fc[nt] = f[chw + nt * 8 + gid];
@@ -409,7 +480,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.0f;
         for (int I = J; I < NSUB; ++I) {
-            const float* f = s.fa.F[I][J];
+            const float* f = s.fa.F[fidx(I, J)];
             float fc[NT];
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) fc[nt] = f[chw + nt * 8 + gid];
@@ -511,11 +582,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
 #pragma unroll
         for (int b = 0; b < RB; ++b) {
             const int r = 16 * b + 2 * warp + hl;
-            if ((lane & 15) == 0) st_both(&s.xd[half][0][r], peer, pq[b]);
-            if ((lane & 15) == 1) st_both(&s.xd[half][1][r], peer, pkd[b]);
+            if ((lane & 15) < 2) {
+                float* x = &s.xd[half][lane & 15][r];
+                const float v = (lane & 15) == 0 ? pq[b] : pkd[b];
+                *x = v;
+                st_async_peer(x, &s.mb_xd, peer, v);
+            }
         }
-        cluster_arrive();
-        cluster_wait();
+        __syncthreads();
+        wait_peer(&s.mb_xd);
 #pragma unroll
         for (int b = 0; b < RB; ++b) {
             const int r = 16 * b + 2 * warp + hl;
@@ -630,7 +705,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 2)
     ci = cn;
     alog = alog_next;
     braw = braw_next;
+    par ^= 1u;
     }
+    // neither CTA leaves while the other may still write into it (only after a timed-out wait
+    // can a write be outstanding here)
+    cluster_arrive();
+    cluster_wait();
 }
 
 
