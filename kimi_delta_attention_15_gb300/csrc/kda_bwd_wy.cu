@@ -36,13 +36,16 @@ constexpr int kWyThreads = kWyWarps * 32;
 // issues every tcgen05 product (an MMA issue takes tens of cycles, and the rest of its warp
 // waits meanwhile: the last warp has the least other work)
 constexpr int kMmaThread = (kWyWarps - 1) * 32;
+// row pitch of the staged raw v rows (bf16): 272 bytes, so that eight consecutive rows
+// read at one column hit eight different 16-byte bank groups
+constexpr int kVsPitch = D + 8;
 
 struct WySmem {
     // operand tiles, 1024-byte aligned (umma.cuh panels)
     uint8_t dW[kTileCK];       // dW [64 i][128 c] (bulk copy)
     uint8_t dU[kTileCK];       // dU [64 i][128 v] (bulk copy)
     uint8_t KV[2 * kTileCK];   // K~ [64 j][128 c] (bulk copy) | V [64 j][128 v] (from the raw
-                               // rows, staged bf16 in its first half); after product 1 the
+                               // rows, staged bf16 at a 272-byte pitch in its first 17 KB); after product 1 the
                                // stacked [dW^T ; dU^T] [256][64 i]
     uint8_t XT[kTileCC];       // X^T [64 i][64 m]
     uint8_t TT[kTileCC];       // T^T [64 j][64 i]
@@ -123,7 +126,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         for (int seg = tid; seg < C * (D / 8); seg += kWyThreads) {
             const int r = seg >> 4, c8 = (seg & 15) * 8;
             const bool valid = r < cn.L;
-            cp_async16_zfill(stv + r * D + c8, v + ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8, valid);
+            cp_async16_zfill(stv + r * kVsPitch + c8, v + ((size_t)(cn.t0 + (valid ? r : 0)) * H + hn) * D + c8, valid);
         }
         cp_async_commit();
     };
@@ -154,11 +157,13 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         cp_async_wait_all();
         __syncthreads();
         {
-            const uint4 v0 = *reinterpret_cast<const uint4*>(stv + tid * 16);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(stv + tid * 16 + 8);
+            // thread: row r, columns c0 .. c0 + 15; consecutive lanes take consecutive rows, so
+            // the panel stores below (16-byte chunk j ^ (r & 7)) are free of bank conflicts
+            const int r = tid & (C - 1), c0 = (tid >> 6) * 16;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(stv + r * kVsPitch + c0);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(stv + r * kVsPitch + c0 + 8);
             if (tid < C) s.beta[tid] = tid < L ? sigmoidf(bf2f(braw)) : 0.0f;
             __syncthreads();   // every staged row is in registers: V overwrites the staging
-            const int r = tid >> 3, c0 = (tid & 7) * 16;
             const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
             uint8_t* V = s.KV + kTileCK;
 #pragma unroll
