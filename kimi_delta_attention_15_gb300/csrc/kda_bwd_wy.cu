@@ -54,7 +54,7 @@ struct WySmem {
     float X[C * C];            // X row-major (bulk copy)
     float Bm[C * C];           // B row-major (bulk copy)
     float beta[C];
-    float dbeta[C];
+    float dbeta[4][C];         // partial sums of dT_ij X_ij over the rows i = p mod 4
     float db2[2][C];           // halves of sum_j dA_ij B_ij
     uint64_t barW, barU, barK, barX, barB, barM[4], barFin;
     uint32_t tmem;
@@ -259,17 +259,16 @@ __global__ void __launch_bounds__(kWyThreads, 1)
             umma_commit(&s.barM[2]);
         }
         if (tid == 0 && cn.L > 0) { issue_dW(nxt); issue_dU(nxt); ++nb[0]; ++nb[1]; }
-        // dbeta_j = sum_{i >= j} dT_ij X_ij: warps 0..7, four threads per column j (rows i = p
-        // mod 4), combined by shuffles in a fixed order
+        // dbeta_j = sum_{i >= j} dT_ij X_ij: warps 0..7, thread (column j = lane-consecutive,
+        // rows i = p mod 4), so that a warp reads 32 consecutive columns of one row; the four
+        // partial sums are combined in a fixed order at the end of the tile
         if (warp < 8) {
-            const int j = tid >> 2, p = tid & 3;
+            const int j = tid & (C - 1), p = tid >> 6;
             float acc = 0.0f;
 #pragma unroll
             for (int i = p; i < C; i += 4)
                 if (i >= j) acc += *reinterpret_cast<const float*>(s.DT + panel_off(i, j, C)) * s.X[i * C + j];
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            if (p == 0) s.dbeta[j] = acc;
+            s.dbeta[p][j] = acc;
         }
         ok = ok && mbar_wait(&s.barM[2], par);
         ok = __syncthreads_and(ok);
@@ -359,7 +358,10 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         }
         tc_fence_before();
         __syncthreads();
-        if (tid < C) reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] = s.dbeta[tid] + (s.db2[0][tid] + s.db2[1][tid]);
+        if (tid < C)
+            reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] =
+                ((s.dbeta[0][tid] + s.dbeta[1][tid]) + (s.dbeta[2][tid] + s.dbeta[3][tid])) +
+                (s.db2[0][tid] + s.db2[1][tid]);
         // B is read: the next tile's B streams in
         if (tid == 0 && cn.L > 0) { issue_B(nxt); ++nb[4]; }
         if (cn.L <= 0) break;
