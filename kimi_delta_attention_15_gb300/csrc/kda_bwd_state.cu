@@ -234,8 +234,10 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
             float dg = 0.0f;
             for (int p = 0; p < 4; ++p, ++it) {
                 const int sa = it % kStA, sg = it % kStB;
-                if (!mbar_wait(&s.fullB[sg], (uint32_t)((it / kStB) & 1)) ||
-                    (p == 0 && !mbar_wait(&s.dfull[n & 1], (uint32_t)((n >> 1) & 1))) || *abort_flag) {
+                // warp-uniform decisions: each warp's arrivals are made by one lane
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.fullB[sg], (uint32_t)((it / kStB) & 1)) &&
+                                                 (p != 0 || mbar_wait(&s.dfull[n & 1], (uint32_t)((n >> 1) & 1))) &&
+                                                 !*abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -268,11 +270,12 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                     *reinterpret_cast<float4*>(g.STK + off) = d;
                 }
                 fence_async_smem();
-                mbar_arrive(&s.ready[sg]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cnt(&s.ready[sg], 32);
                 if (t < 0) continue;   // warps 2, 3: the split only
                 // dgam: row k of S0^T and dS_L^T, after the split is handed to the MMAs; the
                 // stage of these panels is released by this thread's arrival and the MMAs' commit
-                if (!mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) || *abort_flag) {
+                if (!__all_sync(0xffffffffu, mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) && !*abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -285,7 +288,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                     dg = fmaf(a.x, b.x, dg); dg = fmaf(a.y, b.y, dg);
                     dg = fmaf(a.z, b.z, dg); dg = fmaf(a.w, b.w, dg);
                 }
-                mbar_arrive(&s.emptyA[sa]);
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cnt(&s.emptyA[sa], 32);
             }
             if (!ok) break;
             const size_t tt = (size_t)chunk * H + (tile - chunk * H);
@@ -344,7 +348,8 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 for (int j = 0; j < 32; ++j) gdA[i * C + j0 + j] = (j0 + j <= i) ? scale * r[j] : 0.0f;
             }
             tc_fence_before();
-            mbar_arrive(&s.tempty[tb]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cnt(&s.tempty[tb], 32);
             ++n;
         }
         if (!ok) *abort_flag = 1;
