@@ -273,50 +273,45 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
             pair_task(std::integral_constant<int, 1>{}, std::integral_constant<int, 1>{}, 6 + ((warp - NSUB) >> 1),
                       img, (warp - NSUB) & 1);
         } else {
-            // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G) and their transposes
+            // ---- elementwise images: Q^*Gamma, K^*exp(G_L - G), K^*Gamma and the transposes of
+            // the first two, by 4x4 blocks (rows 4rb.., columns 4cb..): each thread stores a
+            // block's rows and, from the same registers, its columns. A warp takes 4 x 8 blocks
+            // (lane: rb += lane / 8, cb += lane % 8): row stores of 128 contiguous bytes and
+            // column stores of 64, loads of eight consecutive 16-byte chunks of one row
             const int et = tid - 384, ew = warp - 12;
-            for (int idx = et; idx < C * D / 4; idx += 128) {
-                const int r = idx >> 5, c = (idx & 31) * 4;          // [64][128], 4 columns per thread
-                const float* pb = s.fa.Pb[r >> 4];
-                const float* sf = s.fa.Sf[r >> 4];
-                float4 qb, kb, kg;
-                qb.x = tf32_round(s.qe[r * P + c] * pb[c]);         kb.x = tf32_round(s.kp[r * P + c] * sf[c]);
-                qb.y = tf32_round(s.qe[r * P + c + 1] * pb[c + 1]); kb.y = tf32_round(s.kp[r * P + c + 1] * sf[c + 1]);
-                qb.z = tf32_round(s.qe[r * P + c + 2] * pb[c + 2]); kb.z = tf32_round(s.kp[r * P + c + 2] * sf[c + 2]);
-                qb.w = tf32_round(s.qe[r * P + c + 3] * pb[c + 3]); kb.w = tf32_round(s.kp[r * P + c + 3] * sf[c + 3]);
-                kg.x = tf32_round(s.ke[r * P + c] * pb[c]);         kg.y = tf32_round(s.ke[r * P + c + 1] * pb[c + 1]);
-                kg.z = tf32_round(s.ke[r * P + c + 2] * pb[c + 2]); kg.w = tf32_round(s.ke[r * P + c + 3] * pb[c + 3]);
-                *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c, C)) = qb;
-                *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c, C)) = kb;
-                *reinterpret_cast<float4*>(img + ImgOff::KT + panel_off(r, c, C)) = kg;
-            }
-            // transposes by 4x4 blocks: rows c0.. of the source, columns kk0..
-            for (int w2 = 0; w2 < 4; ++w2) {
-                const int wi = ew + 4 * w2;
-                const int kk0 = 4 * ((wi & 3) * 8 + (lane & 7)), c0 = 4 * ((wi >> 2) * 4 + (lane >> 3));
-                const float4 pb4 = *reinterpret_cast<const float4*>(&s.fa.Pb[c0 >> 4][kk0]);
-                const float4 sf4 = *reinterpret_cast<const float4*>(&s.fa.Sf[c0 >> 4][kk0]);
-                const float pbv[4] = {pb4.x, pb4.y, pb4.z, pb4.w}, sfv[4] = {sf4.x, sf4.y, sf4.z, sf4.w};
-                float qv[4][4], kv[4][4];
+            for (int g = ew; g < (C / 16) * (D / 32); g += 4) {
+                const int rb = 4 * (g >> 2) + (lane >> 3), cb = 8 * (g & 3) + (lane & 7);
+                const int r0 = 4 * rb, c0 = 4 * cb;
+                const float4 pb = *reinterpret_cast<const float4*>(&s.fa.Pb[r0 >> 4][c0]);
+                const float4 sf = *reinterpret_cast<const float4*>(&s.fa.Sf[r0 >> 4][c0]);
+                float qb[4][4], kb[4][4];
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float4 a = *reinterpret_cast<const float4*>(&s.qe[(c0 + e) * P + kk0]);
-                    const float4 b = *reinterpret_cast<const float4*>(&s.kp[(c0 + e) * P + kk0]);
-                    qv[e][0] = a.x; qv[e][1] = a.y; qv[e][2] = a.z; qv[e][3] = a.w;
-                    kv[e][0] = b.x; kv[e][1] = b.y; kv[e][2] = b.z; kv[e][3] = b.w;
+                    const int r = r0 + e;
+                    const float4 qh = *reinterpret_cast<const float4*>(&s.qe[r * P + c0]);
+                    const float4 kp = *reinterpret_cast<const float4*>(&s.kp[r * P + c0]);
+                    const float4 kh = *reinterpret_cast<const float4*>(&s.ke[r * P + c0]);
+                    const float qv[4] = {qh.x * pb.x, qh.y * pb.y, qh.z * pb.z, qh.w * pb.w};
+                    const float kv[4] = {kp.x * sf.x, kp.y * sf.y, kp.z * sf.z, kp.w * sf.w};
+#pragma unroll
+                    for (int f = 0; f < 4; ++f) {
+                        qb[e][f] = tf32_round(scale * qv[f]);   // the transposed image carries the scale
+                        kb[e][f] = tf32_round(kv[f]);
+                    }
+                    *reinterpret_cast<float4*>(img + ImgOff::QB + panel_off(r, c0, C)) =
+                        make_float4(tf32_round(qv[0]), tf32_round(qv[1]), tf32_round(qv[2]), tf32_round(qv[3]));
+                    *reinterpret_cast<float4*>(img + ImgOff::KB + panel_off(r, c0, C)) =
+                        make_float4(kb[e][0], kb[e][1], kb[e][2], kb[e][3]);
+                    *reinterpret_cast<float4*>(img + ImgOff::KT + panel_off(r, c0, C)) =
+                        make_float4(tf32_round(kh.x * pb.x), tf32_round(kh.y * pb.y), tf32_round(kh.z * pb.z),
+                                    tf32_round(kh.w * pb.w));
                 }
 #pragma unroll
-                for (int e2 = 0; e2 < 4; ++e2) {
-                    float4 qb, kb;
-                    float* qp = &qb.x;
-                    float* kq = &kb.x;
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        qp[e] = tf32_round(scale * (qv[e][e2] * pbv[e2]));
-                        kq[e] = tf32_round(kv[e][e2] * sfv[e2]);
-                    }
-                    *reinterpret_cast<float4*>(img + ImgOff::QBT + panel_off(kk0 + e2, c0, D)) = qb;
-                    *reinterpret_cast<float4*>(img + ImgOff::KBT + panel_off(kk0 + e2, c0, D)) = kb;
+                for (int f = 0; f < 4; ++f) {
+                    *reinterpret_cast<float4*>(img + ImgOff::QBT + panel_off(c0 + f, r0, D)) =
+                        make_float4(qb[0][f], qb[1][f], qb[2][f], qb[3][f]);
+                    *reinterpret_cast<float4*>(img + ImgOff::KBT + panel_off(c0 + f, r0, D)) =
+                        make_float4(kb[0][f], kb[1][f], kb[2][f], kb[3][f]);
                 }
             }
             if (et < D) reinterpret_cast<float*>(img + ImgOff::GAML)[et] = s.fa.gl[et];
