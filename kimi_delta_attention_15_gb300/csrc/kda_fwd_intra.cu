@@ -323,30 +323,32 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
             const int r = idx >> 6, cc = idx & 63;
             s.T[r * PA + cc] = s.X[r * PA + cc] * s.beta[cc];
         }
-        for (int idx = tid; idx < C * C / 4; idx += blockDim.x) {
-            const int r = idx >> 4, cc = (idx & 15) * 4;
-            *reinterpret_cast<float4*>(img + ImgOff::XM + (r * C + cc) * 4) =
-                *reinterpret_cast<const float4*>(&s.X[r * PA + cc]);
-            if ((cc >> 4) > (r >> 4))
-                *reinterpret_cast<float4*>(img + ImgOff::BM + (r * C + cc) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float4 a = make_float4(tf32_round(s.Aqk[r * PA + cc]), tf32_round(s.Aqk[r * PA + cc + 1]),
-                                         tf32_round(s.Aqk[r * PA + cc + 2]), tf32_round(s.Aqk[r * PA + cc + 3]));
-            *reinterpret_cast<float4*>(img + ImgOff::AQK + panel_off(r, cc, C)) = a;
-        }
         if (warp < 8) {
-            // (scale Aqk)^T by 4x4 blocks
-            const int r0 = 4 * ((warp & 1) * 8 + (lane & 7)), c0 = 4 * ((warp >> 1) * 4 + (lane >> 3));
+            // Aqk and (scale Aqk)^T by 4x4 blocks (rows i0.., columns j0..), both from the same
+            // registers: row stores of 128 contiguous bytes, column stores of 64
+            const int j0 = 4 * ((warp & 1) * 8 + (lane & 7)), i0 = 4 * ((warp >> 1) * 4 + (lane >> 3));
             float av[4][4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const float4 a = *reinterpret_cast<const float4*>(&s.Aqk[(c0 + e) * PA + r0]);
+                const float4 a = *reinterpret_cast<const float4*>(&s.Aqk[(i0 + e) * PA + j0]);
                 av[e][0] = a.x; av[e][1] = a.y; av[e][2] = a.z; av[e][3] = a.w;
+                *reinterpret_cast<float4*>(img + ImgOff::AQK + panel_off(i0 + e, j0, C)) =
+                    make_float4(tf32_round(a.x), tf32_round(a.y), tf32_round(a.z), tf32_round(a.w));
             }
 #pragma unroll
             for (int e2 = 0; e2 < 4; ++e2) {
                 const float4 at = make_float4(tf32_round(scale * av[0][e2]), tf32_round(scale * av[1][e2]),
                                               tf32_round(scale * av[2][e2]), tf32_round(scale * av[3][e2]));
-                *reinterpret_cast<float4*>(img + ImgOff::AQKT + panel_off(r0 + e2, c0, C)) = at;
+                *reinterpret_cast<float4*>(img + ImgOff::AQKT + panel_off(j0 + e2, i0, C)) = at;
+            }
+        } else {
+            // X and the zero upper blocks of B (warps 8..15)
+            for (int idx = tid - 256; idx < C * C / 4; idx += 256) {
+                const int r = idx >> 4, cc = (idx & 15) * 4;
+                *reinterpret_cast<float4*>(img + ImgOff::XM + (r * C + cc) * 4) =
+                    *reinterpret_cast<const float4*>(&s.X[r * PA + cc]);
+                if ((cc >> 4) > (r >> 4))
+                    *reinterpret_cast<float4*>(img + ImgOff::BM + (r * C + cc) * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
         __syncthreads();
