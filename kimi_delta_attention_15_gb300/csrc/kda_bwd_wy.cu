@@ -55,7 +55,7 @@ struct WySmem {
     float Bm[C * C];           // B row-major (bulk copy)
     float beta[C];
     float dbeta[4][C];         // partial sums of dT_ij X_ij over the rows i = p mod 4
-    float db2[2][C];           // halves of sum_j dA_ij B_ij
+    float db2[C];              // sum_j dA_ij B_ij
     uint64_t barW, barU, barK, barX, barB, barM[4], barFin;
     uint32_t tmem;
 };
@@ -334,6 +334,11 @@ __global__ void __launch_bounds__(kWyThreads, 1)
         ok = __syncthreads_and(ok);
         if (!ok) break;
         tc_fence_after();
+        // dA rows from TMEM (warps 0..7, a row per lane) into the free M tile, its 16-byte
+        // chunks swizzled by the row (chunk j/4 ^ (i & 7)), so that both the row-per-lane
+        // writes and the row-wise reads below are free of bank conflicts
+        float* const dAs = reinterpret_cast<float*>(s.DT);
+        auto dA_at = [](int i, int j) { return i * C + ((((j >> 2) ^ (i & 7))) << 2) + (j & 3); };
         if (warp < 8) {
             const int hcol = warp >> 2;
             uint32_t r[32];
@@ -341,27 +346,40 @@ __global__ void __launch_bounds__(kWyThreads, 1)
             tmem_wait_ld(r);
             if (lrow) {
                 const int i = mrow, j0 = 32 * hcol;
-                const float bi = s.beta[i];
-                float* gdB = reinterpret_cast<float*>(wy + WyOff::DB) + i * C + j0;
-                float acc = 0.0f;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
-                    const float4 bm = *reinterpret_cast<const float4*>(s.Bm + i * C + j0 + j);
                     float d[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) d[e] = (j0 + j + e < i) ? -__uint_as_float(r[j + e]) : 0.0f;
-                    acc += d[0] * bm.x + d[1] * bm.y + d[2] * bm.z + d[3] * bm.w;
-                    *reinterpret_cast<float4*>(gdB + j) = make_float4(bi * d[0], bi * d[1], bi * d[2], bi * d[3]);
+                    *reinterpret_cast<float4*>(dAs + dA_at(i, j0 + j)) = make_float4(d[0], d[1], d[2], d[3]);
                 }
-                s.db2[hcol][i] = acc;
             }
         }
         tc_fence_before();
         __syncthreads();
+        // dB = diag(beta) dA as whole rows (16 lanes x 16 bytes per row), and the row sums of
+        // dA_ij B_ij over the 16 lanes of a row in a fixed order
+        {
+            float* gdB = reinterpret_cast<float*>(wy + WyOff::DB);
+            const int jc = tid & 15, j = 4 * jc;
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int i = (tid >> 4) + 32 * h2;
+                const float4 d = *reinterpret_cast<const float4*>(dAs + dA_at(i, j));
+                const float4 bm = *reinterpret_cast<const float4*>(s.Bm + i * C + j);
+                const float bi = s.beta[i];
+                *reinterpret_cast<float4*>(gdB + i * C + j) = make_float4(bi * d.x, bi * d.y, bi * d.z, bi * d.w);
+                float acc = d.x * bm.x + d.y * bm.y + d.z * bm.z + d.w * bm.w;
+#pragma unroll
+                for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+                if (jc == 0) s.db2[i] = acc;
+            }
+        }
+        __syncthreads();
         if (tid < C)
             reinterpret_cast<float*>(wy + WyOff::DBETA)[tid] =
                 ((s.dbeta[0][tid] + s.dbeta[1][tid]) + (s.dbeta[2][tid] + s.dbeta[3][tid])) +
-                (s.db2[0][tid] + s.db2[1][tid]);
+                s.db2[tid];
         // B is read: the next tile's B streams in
         if (tid == 0 && cn.L > 0) { issue_B(nxt); ++nb[4]; }
         if (cn.L <= 0) break;
