@@ -75,7 +75,11 @@ __global__ void __launch_bounds__(256, 1)
     for (int c0 = 64 * half; c0 < 64 * half + 64; c0 += 32) {
         float r[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = dhT ? dhT[sidx + (size_t)v * D + c0 + j] : 0.0f;
+        for (int j = 0; j < 32; j += 4) {   // a row per lane: 16-byte loads
+            const float4 x = dhT ? *reinterpret_cast<const float4*>(dhT + sidx + (size_t)v * D + c0 + j)
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            r[j] = x.x; r[j + 1] = x.y; r[j + 2] = x.z; r[j + 3] = x.w;
+        }
         tmem_st32(tS + lane_base + c0, r);
     }
 
@@ -250,7 +254,8 @@ __global__ void __launch_bounds__(256, 1)
             float r[32];
             tmem_ld32(tS + lane_base + c0, r);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) dh0[sidx + (size_t)v * D + c0 + j] = r[j];
+            for (int j = 0; j < 32; j += 4)   // a row per lane: 16-byte stores
+                *reinterpret_cast<float4*>(dh0 + sidx + (size_t)v * D + c0 + j) = make_float4(r[j], r[j + 1], r[j + 2], r[j + 3]);
         }
     }
     if (tid == 0) {

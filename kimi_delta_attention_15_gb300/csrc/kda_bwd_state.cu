@@ -344,8 +344,14 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 float* gdA = reinterpret_cast<float*>(bg + BgOff::DAQK);
                 const int i = kq, j0 = 32 * hf;
                 tmem_ld32(acc + 192 + j0, r);
+                // a row per lane: 16-byte stores (a warp store covers 32 rows)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdA[i * C + j0 + j] = (j0 + j <= i) ? scale * r[j] : 0.0f;
+                for (int j = 0; j < 32; j += 4) {
+                    float a4[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) a4[e] = (j0 + j + e <= i) ? scale * r[j + e] : 0.0f;
+                    *reinterpret_cast<float4*>(gdA + i * C + j0 + j) = make_float4(a4[0], a4[1], a4[2], a4[3]);
+                }
             }
             tc_fence_before();
             __syncwarp();
