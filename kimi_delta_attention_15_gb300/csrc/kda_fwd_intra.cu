@@ -150,19 +150,22 @@ __global__ void __launch_bounds__(kIntraWarps * 32, 1)
         for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
             for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
+        // element pairs (columns col, col + 1 of one row): 8-byte shared and global stores
 #pragma unroll
         for (int nt = 0; nt < NTN; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int row = I * SUB + gid + (e >> 1) * 8;
-                const int col = J * SUB + (nt0 + nt) * 8 + tig * 2 + (e & 1);
-                const float val = acc[nt][e];
+            for (int hh = 0; hh < 2; ++hh) {
+                const int row = I * SUB + gid + hh * 8;
+                const int col = J * SUB + (nt0 + nt) * 8 + tig * 2;
+                const float v0 = acc[nt][2 * hh], v1 = acc[nt][2 * hh + 1];
                 if constexpr (m == 0) {
-                    const float b = col < row ? val : 0.0f;
-                    s.A[row * PA + col] = b * s.beta[row];
-                    reinterpret_cast<float*>(img + ImgOff::BM)[row * C + col] = b;
+                    const float b0 = col < row ? v0 : 0.0f, b1 = col + 1 < row ? v1 : 0.0f;
+                    const float br = s.beta[row];
+                    *reinterpret_cast<float2*>(&s.A[row * PA + col]) = make_float2(b0 * br, b1 * br);
+                    *reinterpret_cast<float2*>(img + ImgOff::BM + (row * C + col) * 4) = make_float2(b0, b1);
                 } else {
-                    s.Aqk[row * PA + col] = col <= row ? val : 0.0f;
+                    *reinterpret_cast<float2*>(&s.Aqk[row * PA + col]) =
+                        make_float2(col <= row ? v0 : 0.0f, col + 1 <= row ? v1 : 0.0f);
                 }
             }
     };
