@@ -301,8 +301,12 @@ __global__ void __launch_bounds__(kWyThreads, 1)
             umma_commit(&s.barM[3]);
         }
         // ---- dKt (fp32) and dv (bf16) from product 2: lane = channel c (or v), columns = rows j.
-        // Warp (quarter q4, group warp / 4): dKt rows 0..31 | dKt 32..63 | dv 0..31 | dv 32..63
+        // Warp (quarter q4, group warp / 4): dKt rows 0..31 | dKt 32..63 | dv 0..31 | dv 32..63.
+        // Staged row-major in the stacked operand's tile (product 2 has read it): dKt leaves as
+        // one bulk copy, dv as 16-byte pieces of its rows
         ok = ok && mbar_wait(&s.barM[1], par);
+        float* const dks = reinterpret_cast<float*>(s.KV);                   // dKt [64 j][128 c]
+        uint16_t* const dvs = reinterpret_cast<uint16_t*>(s.KV + kTileCK);   // dv [64 j][128 v]
         if (__all_sync(0xffffffffu, ok)) {
             tc_fence_after();
             const int grp = warp >> 2, c = 32 * q4 + lane, j0 = 32 * (grp & 1);
@@ -310,22 +314,32 @@ __global__ void __launch_bounds__(kWyThreads, 1)
             tmem_ld32_issue(tm + (grp < 2 ? kD2K : kD2V) + ((uint32_t)(32 * q4) << 16) + j0, r);
             tmem_wait_ld(r);
             if (grp < 2) {
-                float* gdK = reinterpret_cast<float*>(wy + WyOff::DKT) + c;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) gdK[(j0 + j) * D] = __uint_as_float(r[j]);
+                for (int j = 0; j < 32; ++j) dks[(j0 + j) * D + c] = __uint_as_float(r[j]);
             } else {
-                uint16_t* gv = dv + ((size_t)ci.t0 * H + h) * D + c;
 #pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    if (j0 + j < L) gv[(size_t)(j0 + j) * H * D] = f2bf(__uint_as_float(r[j]));
+                for (int j = 0; j < 32; ++j) dvs[(j0 + j) * D + c] = f2bf(__uint_as_float(r[j]));
             }
         }
+        fence_async_smem();
         tc_fence_before();
         ok = __syncthreads_and(ok);
         if (!ok) break;
+        if (tid == 0) {
+            bulk_s2g(wy + WyOff::DKT, dks, (uint32_t)kTileCK);
+            bulk_commit();
+        }
+        for (int idx = tid; idx < C * (D / 8); idx += kWyThreads) {
+            const int j = idx >> 4, c8 = (idx & 15) * 8;
+            if (j < L)
+                *reinterpret_cast<uint4*>(dv + ((size_t)(ci.t0 + j) * H + h) * D + c8) =
+                    *reinterpret_cast<const uint4*>(dvs + j * D + c8);
+        }
+        __syncthreads();   // the dv rows are read: the next tile's raw v rows may overwrite them
         // the stacked operand is read: the next tile's K~ and raw v rows stream into its place
+        // (K~ once the dKt copy has read its staging)
         if (cn.L > 0) {
-            if (tid == 0) { issue_K(nxt); ++nb[2]; }
+            if (tid == 0) { bulk_wait_read_all(); issue_K(nxt); ++nb[2]; }
             stage_v(nxt, cn);
         }
         // ---- dA = -strict_lower(X^T M), dB = diag(beta) dA, dbeta_i += sum_{j<i} dA_ij B_ij
@@ -390,6 +404,7 @@ __global__ void __launch_bounds__(kWyThreads, 1)
     }
     cp_async_wait_all();
     if (tid == 0) {
+        bulk_wait_all();   // the last dKt copy
         if (!ok) raise_status(ws, KDA_ERR_TIMEOUT);
         // bulk copies still in flight (only after an aborted tile), bounded: the last phase
         // issued on each barrier (phases complete in order)
