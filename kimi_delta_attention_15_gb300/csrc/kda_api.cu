@@ -34,7 +34,7 @@ constexpr int kOrderKeys = 4096;   // distinct chunk counts the scan order tells
 // and marks the forward as not complete yet (the forward scan's last CTA completes it).
 __global__ void __launch_bounds__(1024)
     kda_chunk_table_kernel(const int64_t* __restrict__ cu, int64_t N, int64_t T_total, int64_t T_fixed,
-                           uint8_t* __restrict__ ws, Layout lay, uint64_t shape_hash) {
+                           uint8_t* __restrict__ ws, Layout lay, uint64_t shape_hash, int full_workspace) {
     __shared__ int carry;
     __shared__ int bad;
     __shared__ int scan[1024];
@@ -50,6 +50,11 @@ __global__ void __launch_bounds__(1024)
         *reinterpret_cast<uint32_t*>(ws + kFwdCountOff) = 0u;
         carry = 0;
         bad = (cu_at(0) != 0 || cu_at(N) != T_total) ? 1 : 0;
+    }
+    // the parameter reduction's counters (the backward's region: full workspaces only)
+    if (full_workspace) {
+        int* cnt = reinterpret_cast<int*>(ws + param_scratch_offset(lay) + (size_t)lay.H * kParamGroups * (D + 4) * 4);
+        for (int64_t i = tid; i < lay.H; i += blockDim.x) cnt[i] = 0;
     }
     __syncthreads();
     for (int64_t b = 0; b < N; b += blockDim.x) {
@@ -275,7 +280,7 @@ kda_status fwd_entry(const kda_shape* shape, const kda_bf16* q, const kda_bf16* 
 
     prof(0, s);
     kda_chunk_table_kernel<<<1, 1024, 0, s>>>(cu_seqlens, shape->N, T_total, cu_seqlens ? 0 : shape->T, ws, lay,
-                                              shape_hash(shape, cu_seqlens != nullptr));
+                                              shape_hash(shape, cu_seqlens != nullptr), forward_only ? 0 : 1);
     prof(1, s);
     if (lay.nc_max > 0 && T_total > 0)
         intra<<<persistent_grid(lay.nc_max * H), 512, fwd_intra_smem_bytes(), s>>>(
@@ -355,7 +360,7 @@ extern "C" kda_status kda_bwd(const kda_shape* shape, const kda_bf16* q, const k
         kda_qk_group_reduce_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, s>>>(dq, dk, ws, tokens, lay);
     }
     prof(8, s);
-    kda_param_reduce_kernel<<<(unsigned)H, 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);
+    kda_param_reduce_kernel<<<dim3((unsigned)H, (unsigned)kParamGroups), 128, 0, s>>>(H, dA_log, ddt_bias, ws, lay);
     prof(9, s);
     return cuda_status(cudaGetLastError(), "kda_bwd launch");
 }

@@ -748,18 +748,22 @@ __global__ void __launch_bounds__(256)
     }
 }
 
-// Deterministic sum of the per-chunk parameter partials, per head: eight running sums
-// over the chunks (chunk index mod 8), then combined in a fixed order. Each chunk
-// holds one ddt_bias partial per channel and two dA_log partials (one per channel
-// half). Empty chunk records only follow the last real chunk.
+// Deterministic sum of the per-chunk parameter partials, per head. CTA (h, g) sums the
+// chunks g, g + 8, g + 16, ... of head h in order (each chunk holds one ddt_bias partial per
+// channel and two dA_log partials, one per channel half) into the scratch region; the last
+// of a head's eight CTAs to finish (a counter per head) adds the eight sums in the order
+// g = 0 .. 7 and resets the counter. Empty chunk records only follow the last real chunk.
 __global__ void __launch_bounds__(128)
     kda_param_reduce_kernel(int H, float* __restrict__ dA_log, float* __restrict__ ddt_bias,
                             uint8_t* __restrict__ ws, Layout lay) {
-    const int h = blockIdx.x, c = threadIdx.x;
+    const int h = blockIdx.x, g = blockIdx.y, c = threadIdx.x;
     if (read_status(ws) != 0) return;
     const ChunkInfo* chunks = reinterpret_cast<const ChunkInfo*>(ws + lay.chunks);
     const float* part = reinterpret_cast<const float*>(ws + lay.part);
+    float* sums = reinterpret_cast<float*>(ws + param_scratch_offset(lay));
+    int* cnt = reinterpret_cast<int*>(sums + (size_t)H * kParamGroups * (D + 4));
     __shared__ int nreal;
+    __shared__ int last;
     if (c == 0) {
         int lo = 0, hi = (int)lay.nc_max;   // first empty record (binary search)
         while (lo < hi) {
@@ -771,28 +775,33 @@ __global__ void __launch_bounds__(128)
     }
     __syncthreads();
     const int n = nreal;
-    float acc[8], accA[8];
-#pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] = accA[u] = 0.0f;
-    int ch = 0;
-    for (; ch + 8 <= n; ch += 8) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
-            acc[u] += p[c];
-            if (c == 0) accA[u] += p[D] + p[D + 1];
-        }
+    float acc = 0.0f, accA = 0.0f;
+    for (int ch = g; ch < n; ch += kParamGroups) {
+        const float* p = part + ((size_t)ch * H + h) * (D + 4);
+        acc += p[c];
+        if (c == 0) accA += p[D] + p[D + 1];
     }
-    for (int u = 0; ch + u < n; ++u) {
-        const float* p = part + ((size_t)(ch + u) * H + h) * (D + 4);
-        acc[u] += p[c];
-        if (c == 0) accA[u] += p[D] + p[D + 1];
-    }
+    float* mine = sums + ((size_t)h * kParamGroups + g) * (D + 4);
+    mine[c] = acc;
+    if (c == 0) mine[D] = accA;
+    __threadfence();
+    __syncthreads();
+    if (c == 0) last = atomicAdd(cnt + h, 1) == kParamGroups - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const volatile float* all = sums + (size_t)h * kParamGroups * (D + 4);
     float tot = 0.0f, totA = 0.0f;
 #pragma unroll
-    for (int u = 0; u < 8; ++u) { tot += acc[u]; totA += accA[u]; }
+    for (int u = 0; u < kParamGroups; ++u) {
+        tot += all[u * (D + 4) + c];
+        if (c == 0) totA += all[u * (D + 4) + D];
+    }
     ddt_bias[h * D + c] = tot;
-    if (c == 0) dA_log[h] = totA;
+    if (c == 0) {
+        dA_log[h] = totA;
+        cnt[h] = 0;   // ready for the next backward on this workspace
+    }
 }
 
 }  // namespace kda

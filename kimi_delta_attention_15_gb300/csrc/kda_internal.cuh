@@ -99,6 +99,12 @@ __host__ __device__ inline int64_t chunk_slots(int64_t B, int64_t T, int64_t N, 
     return packed ? (B * T) / C + N + 1 : B * ((T + C - 1) / C);
 }
 
+// Chunk classes (chunk index mod kParamGroups) of the parameter reduction, one CTA each.
+constexpr int kParamGroups = 8;
+__host__ __device__ inline size_t param_scratch_bytes(int64_t H) {
+    return (size_t)H * kParamGroups * (D + 4) * 4 + (size_t)H * 4;
+}
+
 __host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, int64_t N, bool packed,
                                               int64_t G = 1) {
     Layout l;
@@ -121,8 +127,16 @@ __host__ __device__ inline Layout make_layout(int64_t B, int64_t T, int64_t H, i
     l.part = o;        o = align_up(o + (size_t)tiles * (D + 4) * 4, 1024);
     // G > 1: every value head's fp32 share of dq and dk, [B T][H][2][128], summed per group
     o = align_up(o + (G > 1 ? (size_t)(B * T) * H * 2 * D * 4 : 0), 1024);
+    // the parameter reduction's per-(head, chunk class) sums and per-head counters (last region)
+    o = align_up(o + param_scratch_bytes(H), 1024);
     l.total = o;
     return l;
+}
+
+// Offset of the parameter reduction's scratch: [H][kParamGroups][D + 4] fp32 sums, then H
+// counters of finished (head, chunk class) CTAs.
+__host__ __device__ inline size_t param_scratch_offset(const Layout& l) {
+    return l.total - align_up(param_scratch_bytes(l.H), 1024);
 }
 
 // Kernels with a plain and a grouped-head instantiation, handed out by host accessors
