@@ -61,7 +61,7 @@ KERNEL_MODEL = {
 # on T=4096 H=32, 2,048 tiles). Valid only for the kernel sources it was measured on:
 # `sources` is a hash of csrc/, checked at run time.
 MEASURED_TRAFFIC = {
-    "sources": "7715475c090559ec",
+    "sources": "dfbafb8bc21cad1e",
     "per_tile": {"fwd_intra": 366081, "fwd_scan": 244082, "bwd_scan": 211530, "bwd_state": 308172, "bwd_wy": 196808, "bwd_pair": 221721},
 }
 

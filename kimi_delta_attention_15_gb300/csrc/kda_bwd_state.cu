@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(kStWarps * 32, 1)
                 if (lane == 0) mbar_arrive_cnt(&s.ready[sg], 32);
                 if (t < 0) continue;   // warps 2, 3: the split only
                 // dgam: row k of S0^T and dS_L^T, after the split is handed to the MMAs; the
-                // stage of these panels is released by this thread's arrival and the MMAs' commit
+                // stage of these panels is released by this warp's arrival (32 counts) and the MMAs' commit
                 if (!__all_sync(0xffffffffu, mbar_wait(&s.fullA[sa], (uint32_t)((it / kStA) & 1)) && !*abort_flag)) {
                     ok = false;
                     break;
