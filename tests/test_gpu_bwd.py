@@ -143,3 +143,20 @@ def test_chunk_size_32_option(lengths):
     _compare(inp, out32, keys=("o", "hT", "dq", "dk", "dv", "dg_raw", "dbeta_raw", "dh0", "ddt_bias"))
     for k in ("o", "hT") + GRADS:
         assert torch.equal(out32[k], out64[k]), k
+
+
+def test_backward_twice_on_one_forward():
+    """kda_bwd may run more than once on the workspace of one kda_fwd (the per-head counters of
+    the parameter reduction reset themselves): the second call writes the same gradients."""
+    from gpu_helpers import to_dev
+    from kimi_delta_attention_15_gb300 import ops
+    inp = I.make_inputs(I.custom((300, 70, 129), 3, h0=True, dhT=True), seed=29)
+    d = to_dev(inp)
+    args = (d["q"], d["k"], d["v"], d["g_raw"], d["beta_raw"], d["A_log"], d["dt_bias"])
+    o, hT, ws = ops.fwd(*args, h0=d["h0"], cu_seqlens=d["cu_seqlens"])
+    g1 = ops.bwd(*args, d["do"], ws, h0=d["h0"], cu_seqlens=d["cu_seqlens"], dhT=d["dhT"])
+    g2 = ops.bwd(*args, d["do"], ws, h0=d["h0"], cu_seqlens=d["cu_seqlens"], dhT=d["dhT"])
+    torch.cuda.synchronize()
+    assert ops.device_status(ws) == 0
+    for k in GRADS:
+        assert torch.equal(g1[k], g2[k]), k
